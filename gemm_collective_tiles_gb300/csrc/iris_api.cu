@@ -1,0 +1,509 @@
+// Host side of the C ABI declared in include/gemm_collective_tiles.h:
+// argument checks, workspace layout, TMA tensor maps, and the launch of the
+// persistent fused kernel (fused_kernel.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_collective_tiles.h"
+#include "fused_kernel.cuh"
+
+using namespace gct;
+
+namespace {
+
+constexpr int BN_WIDE = 256, STAGES_WIDE = 4;
+constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
+constexpr size_t WS_HEADER = 256;
+constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+bool g_attr_done[64] = {false};
+
+EncodeTiledFn encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return nullptr;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+    return Smem<BN, STAGES>::BYTES;
+}
+
+int ensure_attrs(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (dev < 0 || dev >= 64) return IRIS_ECUDA;
+    if (g_attr_done[dev]) return IRIS_OK;
+    if (cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN_WIDE, STAGES_WIDE>())) != cudaSuccess)
+        return IRIS_ECUDA;
+    if (cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN_NARROW, STAGES_NARROW>())) != cudaSuccess)
+        return IRIS_ECUDA;
+    g_attr_done[dev] = true;
+    return IRIS_OK;
+}
+
+int num_sms_current(int* n) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IRIS_ECUDA;
+    if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IRIS_ECUDA;
+    return IRIS_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Resolved configuration.
+struct Cfg {
+    int tile_n, group_m, gemm_ctas, comm_block, replicate, bias_on_m, grid;
+    unsigned long long wait_ns;
+    uint32_t debug_skip;
+};
+
+int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
+    iris_b200_config z;
+    std::memset(&z, 0, sizeof(z));
+    if (!c) c = &z;
+    if (c->tile_m != 0 && c->tile_m != BM) return IRIS_EINVAL;
+    if (c->tile_k != 0 && c->tile_k != BK) return IRIS_EINVAL;
+    if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256) return IRIS_EINVAL;
+    out.tile_n = c->tile_n ? c->tile_n : (N <= 128 ? 128 : 256);
+    if (c->group_m < 0) return IRIS_EINVAL;
+    out.group_m = c->group_m ? c->group_m : 8;
+    out.comm_block = c->comm_block ? c->comm_block : 65536;
+    if (out.comm_block < 0 || out.comm_block % 8 != 0) return IRIS_EINVAL;
+    out.replicate = c->replicate_outputs ? 1 : 0;
+    out.bias_on_m = c->bias_on_m ? 1 : 0;
+    int sms = 0;
+    if (num_sms_current(&sms) != IRIS_OK) return IRIS_ECUDA;
+    if (c->grid < 0 || c->grid > sms) return IRIS_EINVAL;
+    out.grid = c->grid ? c->grid : sms;
+    if (c->gemm_ctas < -1 || c->gemm_ctas > out.grid) return IRIS_EINVAL;
+    if (c->gemm_ctas != 0)
+        out.gemm_ctas = c->gemm_ctas;
+    else
+        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? -1 : out.grid;
+    out.wait_ns = c->wait_ns ? c->wait_ns : DEFAULT_WAIT_NS;
+    if (c->debug_skip_flag < 0) return IRIS_EINVAL;
+    out.debug_skip = static_cast<uint32_t>(c->debug_skip_flag);
+    return IRIS_OK;
+}
+
+// Sizes of the workspace pieces for one call.
+struct WsLayout {
+    size_t flags_off, n_flags, partial_off, partial_elems, total;
+};
+
+WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n) {
+    WsLayout L{};
+    L.flags_off = WS_HEADER;
+    const int64_t mb = cdiv(M, BM), nb = cdiv(N, tile_n);
+    if (op == IRIS_OP_ALL_GATHER_MATMUL)
+        L.n_flags = static_cast<size_t>(W) * mb;
+    else if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
+        L.n_flags = static_cast<size_t>(W) * mb * nb;
+    L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
+    if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
+        L.partial_elems = static_cast<size_t>(M) * N;
+    L.total = round_up(L.partial_off + L.partial_elems * 4 * (L.partial_elems ? W : 0), 256);
+    return L;
+}
+
+bool aligned16(size_t x) { return (x & 15) == 0; }
+
+// tensor [off, off+bytes) inside a heap region, 16-byte aligned
+int check_region(const iris_b200_heap* h, size_t off, size_t bytes) {
+    if (!aligned16(off)) return IRIS_EALIGN;
+    if (off > h->rank_stride || bytes > h->rank_stride - off) return IRIS_EINVAL;
+    return IRIS_OK;
+}
+
+int check_heap(const iris_b200_heap* h) {
+    if (!h || !h->base) return IRIS_EINVAL;
+    if (h->world < 1 || h->world > IRIS_MAX_WORLD) return IRIS_EINVAL;
+    if (!aligned16(h->rank_stride) || !aligned16(reinterpret_cast<uintptr_t>(h->base))) return IRIS_EALIGN;
+    return IRIS_OK;
+}
+
+int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t d0, uint64_t d1, uint64_t d2,
+             uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? IRIS_OK : IRIS_ECUDA;
+}
+
+void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks, const Cfg& c) {
+    p.M = static_cast<int>(M_rows);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.m_blocks = m_blocks;
+    p.n_blocks = static_cast<int>(cdiv(N, c.tile_n));
+    p.k_blocks = static_cast<int>(cdiv(K, BK));
+    p.group_m = c.group_m;
+    p.n_tiles = p.m_blocks * p.n_blocks;
+    p.gemm_ctas = c.gemm_ctas;
+    p.lookahead = static_cast<uint32_t>(c.grid);
+    p.replicate = c.replicate;
+    p.bias_on_m = c.bias_on_m;
+    p.wait_ns = c.wait_ns;
+    p.debug_skip = c.debug_skip;
+}
+
+int launch(Params& p, const Cfg& c, cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IRIS_ECUDA;
+    int rc = ensure_attrs(dev);
+    if (rc != IRIS_OK) return rc;
+    if (c.tile_n == BN_WIDE) {
+        fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>
+            <<<c.grid, NUM_THREADS, smem_bytes<BN_WIDE, STAGES_WIDE>(), stream>>>(p);
+    } else {
+        fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>
+            <<<c.grid, NUM_THREADS, smem_bytes<BN_NARROW, STAGES_NARROW>(), stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? IRIS_OK : IRIS_ECUDA;
+}
+
+bool dims_ok(int64_t M, int64_t N, int64_t K) {
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    return M >= 0 && N >= 0 && K >= 0 && M <= lim && N <= lim && K <= lim;
+}
+
+int prepare_ws(Params& p, void* ws, size_t ws_bytes, iris_op op, int64_t M, int64_t N, int W,
+               const Cfg& c) {
+    const WsLayout L = ws_layout(op, M, N, W, c.tile_n);
+    if (!ws || ws_bytes < L.total) return IRIS_ENOWS;
+    if (!aligned16(reinterpret_cast<uintptr_t>(ws))) return IRIS_EALIGN;
+    p.ws = reinterpret_cast<WsHeader*>(ws);
+    p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.flags_off);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partial_off);
+    p.partial_elems = L.partial_elems;
+    return IRIS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* iris_b200_strerror(int code) {
+    switch (code) {
+        case IRIS_OK: return "ok";
+        case IRIS_EINVAL: return "invalid argument";
+        case IRIS_EALIGN: return "misaligned offset or row pitch (16-byte rule)";
+        case IRIS_ENOWS: return "workspace missing or too small";
+        case IRIS_ECUDA: return "CUDA error";
+        case IRIS_ETIMEOUT: return "a bounded device wait gave up";
+        case IRIS_EUNSUPPORTED: return "unsupported request";
+        default: return "unknown error";
+    }
+}
+
+int iris_b200_num_sms(int* n) {
+    if (!n) return IRIS_EINVAL;
+    return num_sms_current(n);
+}
+
+int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int world, iris_dtype dtype,
+                             const iris_b200_config* cfg, size_t* bytes) {
+    if (!bytes || !dims_ok(M, N, K) || world < 1 || world > IRIS_MAX_WORLD) return IRIS_EINVAL;
+    if (op < IRIS_OP_ALL_GATHER_MATMUL || op > IRIS_OP_CONCURRENT) return IRIS_EINVAL;
+    (void)dtype;
+    int tile_n = 256;
+    if (cfg && cfg->tile_n) {
+        if (cfg->tile_n != 128 && cfg->tile_n != 256) return IRIS_EINVAL;
+        tile_n = cfg->tile_n;
+    } else if (N <= 128) {
+        tile_n = 128;
+    }
+    int64_t Mrows = M;
+    if (op == IRIS_OP_MATMUL_ALL_GATHER) Mrows = 0;  // no flags or partials
+    *bytes = ws_layout(op, Mrows, N, world, tile_n).total;
+    return IRIS_OK;
+}
+
+int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t off_B, size_t off_bias,
+                                size_t off_out, size_t off_gathered, int64_t M, int64_t N, int64_t K,
+                                iris_dtype dtype, const iris_b200_config* cfg, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+    int rc = check_heap(heap);
+    if (rc) return rc;
+    if (!dims_ok(M, N, K) || (dtype != IRIS_F16 && dtype != IRIS_BF16)) return IRIS_EINVAL;
+    const int W = heap->world;
+    if (K % W != 0) return IRIS_EINVAL;
+    const int64_t K_l = K / W;
+    if (K_l % 8 != 0 || N % 8 != 0) return IRIS_EALIGN;
+    Cfg c;
+    if ((rc = resolve_cfg(cfg, IRIS_OP_ALL_GATHER_MATMUL, N, c))) return rc;
+    if ((rc = check_region(heap, off_A, size_t(M) * K_l * 2))) return rc;
+    if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
+    if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
+    if ((rc = check_region(heap, off_gathered, size_t(M) * K * 2))) return rc;
+    const bool has_bias = off_bias != IRIS_NO_BIAS;
+    if (has_bias && (rc = check_region(heap, off_bias, size_t(c.bias_on_m ? M : N) * 2))) return rc;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.op = OP_AG_MM;
+    p.W = W;
+    p.bf16 = dtype == IRIS_BF16;
+    const int mblocks = static_cast<int>(cdiv(M, BM));
+    fill_geometry(p, M, N, K, mblocks, c);
+    p.mb_per_rank = mblocks;
+    p.K_local = static_cast<int>(K_l);
+    p.heap = static_cast<char*>(heap->base);
+    p.rank_stride = heap->rank_stride;
+    p.off_A = off_A;
+    p.off_out = off_out;
+    p.off_gathered = off_gathered;
+    p.off_bias = has_bias ? off_bias : 0;
+    p.has_bias = has_bias;
+    p.n_gemm = (M > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    p.n_comm = static_cast<uint32_t>(mblocks) * W;
+    if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_ALL_GATHER_MATMUL, M, N, W, c))) return rc;
+    if (p.n_gemm > 0 && K > 0) {
+        char* g = p.heap + off_gathered;
+        if ((rc = make_map(&p.tmA, g, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
+            return rc;
+    }
+    return launch(p, c, stream);
+}
+
+static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                            size_t off_bias, size_t off_out, int64_t M, int64_t N, int64_t K,
+                            iris_dtype dtype, const iris_b200_config* cfg, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+    int rc = check_heap(heap);
+    if (rc) return rc;
+    if (!dims_ok(M, N, K) || (dtype != IRIS_F16 && dtype != IRIS_BF16)) return IRIS_EINVAL;
+    const int W = heap->world;
+    int64_t N_l = N;
+    if (op == IRIS_OP_MATMUL_REDUCE_SCATTER) {
+        if (N % W != 0) return IRIS_EINVAL;
+        N_l = N / W;
+    }
+    if (K % 8 != 0 || N % 8 != 0 || N_l % 8 != 0) return IRIS_EALIGN;
+    Cfg c;
+    if ((rc = resolve_cfg(cfg, op, N, c))) return rc;
+    if ((rc = check_region(heap, off_A, size_t(M) * K * 2))) return rc;
+    if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
+    if ((rc = check_region(heap, off_out, size_t(M) * N_l * 2))) return rc;
+    const bool has_bias = off_bias != IRIS_NO_BIAS;
+    if (has_bias && (rc = check_region(heap, off_bias, size_t(c.bias_on_m ? M : N) * 2))) return rc;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.op = (op == IRIS_OP_MATMUL_REDUCE_SCATTER) ? OP_MM_RS : OP_MM_AR;
+    p.W = W;
+    p.bf16 = dtype == IRIS_BF16;
+    const int mblocks = static_cast<int>(cdiv(M, BM));
+    fill_geometry(p, M, N, K, mblocks, c);
+    p.mb_per_rank = mblocks;
+    p.N_local = static_cast<int>(N_l);
+    p.heap = static_cast<char*>(heap->base);
+    p.rank_stride = heap->rank_stride;
+    p.off_A = off_A;
+    p.off_out = off_out;
+    p.off_bias = has_bias ? off_bias : 0;
+    p.has_bias = has_bias;
+    const uint64_t tiles = (M > 0 && N > 0) ? uint64_t(p.n_tiles) : 0;
+    if (tiles * W >= 0x7FFFFFFFull) return IRIS_EINVAL;
+    p.n_gemm = static_cast<uint32_t>(tiles * W);
+    p.n_comm = static_cast<uint32_t>(tiles);
+    if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
+    if (p.n_gemm > 0 && K > 0) {
+        if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64, BK))) return rc;
+    }
+    return launch(p, c, stream);
+}
+
+int iris_b200_matmul_reduce_scatter(const iris_b200_heap* heap, size_t off_A, size_t off_B, size_t off_bias,
+                                    size_t off_out, int64_t M, int64_t N, int64_t K, iris_dtype dtype,
+                                    const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    return mm_reduce_common(IRIS_OP_MATMUL_REDUCE_SCATTER, heap, off_A, off_B, off_bias, off_out, M, N, K,
+                            dtype, cfg, workspace, workspace_bytes, stream);
+}
+
+int iris_b200_matmul_all_reduce(const iris_b200_heap* heap, size_t off_A, size_t off_B, size_t off_bias,
+                                size_t off_out, int64_t M, int64_t N, int64_t K, iris_dtype dtype,
+                                const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    return mm_reduce_common(IRIS_OP_MATMUL_ALL_REDUCE, heap, off_A, off_B, off_bias, off_out, M, N, K, dtype,
+                            cfg, workspace, workspace_bytes, stream);
+}
+
+int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t off_B, size_t off_bias,
+                                size_t off_out, int64_t M, int64_t N, int64_t K, iris_dtype dtype,
+                                const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    int rc = check_heap(heap);
+    if (rc) return rc;
+    if (!dims_ok(M, N, K) || (dtype != IRIS_F16 && dtype != IRIS_BF16)) return IRIS_EINVAL;
+    const int W = heap->world;
+    if (M % W != 0) return IRIS_EINVAL;
+    const int64_t M_l = M / W;
+    if (K % 8 != 0 || N % 8 != 0) return IRIS_EALIGN;
+    Cfg c;
+    if ((rc = resolve_cfg(cfg, IRIS_OP_MATMUL_ALL_GATHER, N, c))) return rc;
+    if ((rc = check_region(heap, off_A, size_t(M_l) * K * 2))) return rc;
+    if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
+    if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
+    const bool has_bias = off_bias != IRIS_NO_BIAS;
+    if (has_bias && (rc = check_region(heap, off_bias, size_t(c.bias_on_m ? M_l : N) * 2))) return rc;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.op = OP_MM_AG;
+    p.W = W;
+    p.bf16 = dtype == IRIS_BF16;
+    const int mbpr = static_cast<int>(cdiv(M_l, BM));
+    fill_geometry(p, M_l, N, K, mbpr * W, c);
+    p.mb_per_rank = mbpr;
+    p.heap = static_cast<char*>(heap->base);
+    p.rank_stride = heap->rank_stride;
+    p.off_A = off_A;
+    p.off_out = off_out;
+    p.off_bias = has_bias ? off_bias : 0;
+    p.has_bias = has_bias;
+    p.n_gemm = (M_l > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    p.n_comm = 0;
+    if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_MATMUL_ALL_GATHER, 0, N, W, c))) return rc;
+    if (p.n_gemm > 0 && K > 0) {
+        if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
+            return rc;
+    }
+    return launch(p, c, stream);
+}
+
+int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                         iris_dtype gemm_dtype, iris_coll coll, const iris_b200_heap* heap,
+                                         size_t off_in, size_t off_out, int64_t count, iris_dtype coll_dtype,
+                                         const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    if (!dims_ok(M, N, K) || count < 0) return IRIS_EINVAL;
+    if (gemm_dtype != IRIS_F16 && gemm_dtype != IRIS_BF16) return IRIS_EINVAL;
+    const bool has_gemm = M > 0 && N > 0;
+    if (has_gemm) {
+        if (!C || (K > 0 && (!A || !B))) return IRIS_EINVAL;
+        if (K % 8 != 0 || N % 8 != 0) return IRIS_EALIGN;
+        if (!aligned16(reinterpret_cast<uintptr_t>(A)) || !aligned16(reinterpret_cast<uintptr_t>(B)) ||
+            !aligned16(reinterpret_cast<uintptr_t>(C)))
+            return IRIS_EALIGN;
+    }
+    int rc;
+    int W = 1;
+    int esz = 4;
+    if (count > 0) {
+        if ((rc = check_heap(heap))) return rc;
+        W = heap->world;
+        if (coll != IRIS_COLL_ALL_GATHER && coll != IRIS_COLL_ALL_REDUCE && coll != IRIS_COLL_REDUCE_SCATTER)
+            return IRIS_EINVAL;
+        if (coll == IRIS_COLL_ALL_GATHER) {
+            esz = (coll_dtype == IRIS_F32) ? 4 : (coll_dtype == IRIS_F16 || coll_dtype == IRIS_BF16) ? 2 : 0;
+            if (!esz) return IRIS_EINVAL;
+        } else if (coll_dtype != IRIS_F32) {
+            return IRIS_EUNSUPPORTED;
+        }
+        if ((count * esz) % 16 != 0) return IRIS_EALIGN;
+        if (coll == IRIS_COLL_REDUCE_SCATTER && count % (4 * W) != 0) return IRIS_EALIGN;
+    }
+    Cfg c;
+    if ((rc = resolve_cfg(cfg, IRIS_OP_CONCURRENT, N, c))) return rc;
+    if (count > 0) {
+        if (size_t(c.comm_block) * esz % 16 != 0) return IRIS_EALIGN;
+        const size_t in_bytes = size_t(count) * esz;
+        const size_t out_bytes = coll == IRIS_COLL_ALL_GATHER   ? in_bytes * W
+                                 : coll == IRIS_COLL_ALL_REDUCE ? in_bytes
+                                                                : in_bytes / W;
+        if ((rc = check_region(heap, off_in, in_bytes))) return rc;
+        if ((rc = check_region(heap, off_out, out_bytes))) return rc;
+        // an in-place collective must use the same offsets exactly; partial overlap is refused
+        if (off_in != off_out && off_in < off_out + out_bytes && off_out < off_in + in_bytes) return IRIS_EINVAL;
+        if (off_in == off_out && coll != IRIS_COLL_ALL_REDUCE) return IRIS_EINVAL;
+    }
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.op = OP_CONC;
+    p.W = W;
+    p.bf16 = gemm_dtype == IRIS_BF16;
+    p.coll = coll == IRIS_COLL_ALL_GATHER ? COLL_AG : coll == IRIS_COLL_ALL_REDUCE ? COLL_AR : COLL_RS;
+    const int mblocks = static_cast<int>(cdiv(M, BM));
+    fill_geometry(p, M, N, K, mblocks, c);
+    p.mb_per_rank = mblocks;
+    p.C = C;
+    p.n_gemm = has_gemm ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    if (count > 0) {
+        p.heap = static_cast<char*>(heap->base);
+        p.rank_stride = heap->rank_stride;
+        p.off_in = off_in;
+        p.off_cout = off_out;
+        p.count = count;
+        p.comm_block = c.comm_block;
+        p.elem_bytes = esz;
+        const int64_t chunks = cdiv(count, c.comm_block);
+        const int64_t items = (coll == IRIS_COLL_ALL_GATHER) ? chunks * W : chunks;
+        if (items >= 0x7FFFFFFF) return IRIS_EINVAL;
+        p.n_comm = static_cast<uint32_t>(items);
+    }
+    if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_CONCURRENT, 0, N, W, c))) return rc;
+    if (p.n_gemm > 0 && K > 0) {
+        if ((rc = make_map(&p.tmA, A, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
+        if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK))) return rc;
+    }
+    return launch(p, c, stream);
+}
+
+int iris_b200_query_status(void* workspace, cudaStream_t stream, int* device_status, int* where, int* index) {
+    if (!workspace) return IRIS_EINVAL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return IRIS_ECUDA;
+    WsHeader h;
+    if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return IRIS_ECUDA;
+    if (device_status) *device_status = h.status;
+    if (where) *where = h.err_where;
+    if (index) *index = h.err_index;
+    if (h.status != 0) {
+        const int zero[4] = {0, 0, 0, 0};
+        // clear status, abort epoch, where, index (bytes 16..31 of the header)
+        if (cudaMemcpy(static_cast<char*>(workspace) + 16, zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return IRIS_ECUDA;
+        return IRIS_ETIMEOUT;
+    }
+    return IRIS_OK;
+}
+
+}  // extern "C"

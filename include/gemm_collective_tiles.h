@@ -1,0 +1,249 @@
+/*
+ * gemm_collective_tiles.h -- C ABI of the GB300 (sm_103a) fused GEMM + collective library.
+ *
+ * One persistent kernel per call interleaves dense GEMM tiles (tcgen05 tensor
+ * cores, TMA-fed shared-memory pipeline, fp32 accumulators in tensor memory)
+ * with collective-communication tiles (vectorised copy / reduce) that are
+ * linked to the GEMM tiles by release/acquire ready-flags.
+ *
+ * The W ranks of the collective are emulated on one GPU as W regions of a
+ * symmetric heap: region r starts at heap->base + r * heap->rank_stride, and a
+ * tensor that "lives on every rank" sits at the same byte offset in every
+ * region (the heap_bases address translation of the iris symmetric heap,
+ * iris docs "Fused Communication and Compute Operations", atomic_sub:
+ * heap_bases holds each rank's heap base and a pointer moves between ranks by
+ * its offset).  Collective results are reproduced bit for bit on the device.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Matrices are row-major ("NN"): A is M x K with K contiguous, B is K x N
+ *    with N contiguous, outputs are rows x N with N contiguous.  Element type
+ *    of A, B, bias and 16-bit outputs: IRIS_F16 or IRIS_BF16 (A and B always
+ *    share one type).  Accumulation is fp32.
+ *  - Tensor arguments named off_* are BYTE OFFSETS into a heap region (the
+ *    same offset in every region that holds the tensor).  Every offset must be
+ *    16-byte aligned and every row must be a multiple of 16 bytes (the tensor
+ *    memory accelerator's rule), i.e. K, N, K/W, N/W as the op requires must be
+ *    multiples of 8 elements.  M may be anything (ragged row tails are masked).
+ *    IRIS_NO_BIAS as off_bias means "no bias".
+ *  - Ownership: the caller owns the heap, the workspace and the stream.  The
+ *    library allocates no device memory per call; it keeps only a per-process
+ *    cache of kernel attributes.
+ *  - Asynchrony: every op enqueues one kernel on `stream` and returns.  The
+ *    iris ops' async_op=False (a barrier at the end) is the caller
+ *    synchronising the stream; iris_b200_query_status() does that and reports
+ *    device-side failures.
+ *  - Workspace: `workspace` is caller-allocated device memory of at least
+ *    iris_b200_workspace_size() bytes, ZERO-FILLED ONCE before its first use.
+ *    It holds the queue counters, the launch epoch, a status word, the
+ *    ready-flags and (reduce ops) the fp32 partial products.  It may be reused
+ *    by any later call on the same stream without clearing (flags carry the
+ *    launch epoch).  Two calls that share a workspace must not overlap in time.
+ *  - Config: NULL or a zero-filled struct selects the defaults field by field.
+ *  - Return value: IRIS_OK (0) or a negative IRIS_E* code; nothing is launched
+ *    when an error is returned.  There is no silent fallback path.
+ */
+#ifndef GEMM_COLLECTIVE_TILES_H
+#define GEMM_COLLECTIVE_TILES_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define IRIS_API __attribute__((visibility("default")))
+#else
+#define IRIS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define IRIS_OK 0
+#define IRIS_EINVAL (-1)      /* null pointer, bad size, world size, divisibility, config value */
+#define IRIS_EALIGN (-2)      /* offset or row pitch not a multiple of 16 bytes */
+#define IRIS_ENOWS (-3)       /* workspace missing or smaller than iris_b200_workspace_size() */
+#define IRIS_ECUDA (-4)       /* CUDA runtime / driver error (launch, attribute, tensor map) */
+#define IRIS_ETIMEOUT (-5)    /* a bounded device wait gave up (reported by query_status) */
+#define IRIS_EUNSUPPORTED (-6) /* valid request this build does not implement */
+
+#define IRIS_NO_BIAS ((size_t)-1)
+#define IRIS_MAX_WORLD 16
+
+typedef enum { IRIS_F16 = 0, IRIS_BF16 = 1, IRIS_F32 = 2 } iris_dtype;
+
+typedef enum {
+    IRIS_COLL_ALL_GATHER = 0,
+    IRIS_COLL_ALL_REDUCE = 1,
+    IRIS_COLL_REDUCE_SCATTER = 2
+} iris_coll;
+
+typedef enum {
+    IRIS_OP_ALL_GATHER_MATMUL = 0,
+    IRIS_OP_MATMUL_REDUCE_SCATTER = 1,
+    IRIS_OP_MATMUL_ALL_GATHER = 2,
+    IRIS_OP_MATMUL_ALL_REDUCE = 3,
+    IRIS_OP_CONCURRENT = 4
+} iris_op;
+
+/* Tuning knobs (the iris FusedConfig / concurrent gemm_wgs).  0 = default. */
+typedef struct {
+    int tile_m;            /* GEMM tile rows: 128 (only value) */
+    int tile_n;            /* GEMM tile columns: 128 or 256 (default 256) */
+    int tile_k;            /* K step per pipeline stage: 64 (only value) */
+    int group_m;           /* GROUP_M tile swizzle width in M blocks (default 8) */
+    int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
+                              prefer the comm queue and every CTA spills to the
+                              other queue when its own runs dry.  0 = op default;
+                              -1 = balanced (every CTA draws from both queues so
+                              that both finish together). */
+    int stages;            /* reserved: pipeline depth is fixed per tile_n */
+    int comm_block;        /* concurrent mode: elements per comm tile (default 65536) */
+    int replicate_outputs; /* 1: also write the W-1 identical copies of replicated
+                              outputs into the other heap regions */
+    int bias_on_m;         /* 1: bias has one entry per output row (length M) */
+    int grid;              /* persistent CTAs (default: one per SM) */
+    unsigned long long wait_ns; /* limit of every device-side wait (default 2e9 ns) */
+    int debug_skip_flag;   /* test hook: 0 = off; k > 0 makes the kernel never
+                              release ready-flag k-1, so the tile waiting on it
+                              runs into its bounded wait (IRIS_ETIMEOUT from
+                              query_status).  Never set it in production. */
+} iris_b200_config;
+
+/* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */
+typedef struct {
+    void* base;
+    size_t rank_stride;    /* multiple of 16 bytes */
+    int world;             /* W, 1..IRIS_MAX_WORLD */
+} iris_b200_heap;
+
+/*
+ * Workspace bytes needed by `op` for this problem (M, N, K in the op's own
+ * convention as below; for IRIS_OP_CONCURRENT pass the GEMM's M, N, K).
+ * Writes *bytes.  Errors: IRIS_EINVAL for a null `bytes` or bad sizes.
+ */
+IRIS_API int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int world,
+                             iris_dtype dtype, const iris_b200_config* cfg, size_t* bytes);
+
+/*
+ * all_gather_matmul  -- iris docs "Fused Communication and Compute
+ * Operations", all_gather_matmul: output = all_gather(A_sharded) @ B + bias,
+ * A_sharded (M, K_local), B (K, N) with K = K_local * world_size.
+ *
+ *   off_A        region r holds rank r's shard A_r: M x (K/W), 16-bit.
+ *   off_B        region 0 holds B: K x N (shared by every rank).
+ *   off_bias     region 0 holds bias: N (or M with bias_on_m) entries, or IRIS_NO_BIAS.
+ *   off_out      region 0 receives out = gathered @ B + bias: M x N, 16-bit
+ *                (with replicate_outputs, every region receives the same bits).
+ *   off_gathered region 0 receives the gathered A: M x K, shard s in columns
+ *                [s*K/W, (s+1)*K/W) -- bit-exact copies of the shards.
+ * Comm tiles copy each shard's row block into the gathered buffer and release
+ * a per-(shard, row block) flag; GEMM tiles acquire the flags of the shards
+ * they consume just before loading them.
+ * Requires K % W == 0, (K/W) % 8 == 0, N % 8 == 0.
+ */
+IRIS_API int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                                size_t off_bias, size_t off_out, size_t off_gathered,
+                                int64_t M, int64_t N, int64_t K, iris_dtype dtype,
+                                const iris_b200_config* cfg, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * matmul_reduce_scatter -- iris docs, matmul_reduce_scatter: output =
+ * reduce_scatter(A @ B + bias) along N; output (M, N_local), N_local = N / W.
+ *
+ *   off_A    region r holds A_r: M x K.       off_B  region r holds B_r: K x N.
+ *   off_bias region r holds rank r's bias (N entries, or M with bias_on_m);
+ *            every rank adds its own bias to its partial, so the sum holds W biases.
+ *   off_out  region r receives out_r: M x N_local, 16-bit:
+ *            out_r = RNE16( sum_{s=0..W-1} (A_s @ B_s + bias_s)[:, r*N_local:(r+1)*N_local] )
+ *            with the partials kept in fp32 (in the workspace) and summed in
+ *            rank order 0..W-1.
+ * Requires N % W == 0, (N/W) % 8 == 0, K % 8 == 0.
+ */
+IRIS_API int iris_b200_matmul_reduce_scatter(const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                                    size_t off_bias, size_t off_out, int64_t M, int64_t N,
+                                    int64_t K, iris_dtype dtype, const iris_b200_config* cfg,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
+ * matmul_all_gather -- iris docs, matmul_all_gather: output = all_gather(A @ B
+ * + bias) along M; A (M_local, K) per rank, output (M_local * W, N).
+ *
+ *   M        the GATHERED row count (M_local = M / W).
+ *   off_A    region r holds A_r: (M/W) x K.   off_B  region 0 holds B: K x N (shared).
+ *   off_bias region 0: N entries (or M/W with bias_on_m, the same on every rank).
+ *   off_out  region 0 receives out: M x N, rows [r*M/W, (r+1)*M/W) = RNE16(A_r @ B + bias)
+ *            (with replicate_outputs, every region receives the same bits).
+ * Requires M % W == 0, K % 8 == 0, N % 8 == 0.
+ */
+IRIS_API int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                                size_t off_bias, size_t off_out, int64_t M, int64_t N,
+                                int64_t K, iris_dtype dtype, const iris_b200_config* cfg,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * matmul_all_reduce -- iris docs, matmul_all_reduce: output = all_reduce(A @ B + bias).
+ *
+ *   off_A, off_B, off_bias  per region as for matmul_reduce_scatter.
+ *   off_out  region 0 receives out: M x N = RNE16(rank-order fp32 sum of the
+ *            W partials); with replicate_outputs every region receives it.
+ * Requires K % 8 == 0, N % 8 == 0.
+ */
+IRIS_API int iris_b200_matmul_all_reduce(const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                                size_t off_bias, size_t off_out, int64_t M, int64_t N,
+                                int64_t K, iris_dtype dtype, const iris_b200_config* cfg,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * concurrent_gemm_collective -- ROCm/iris PR #544 "Add iris.concurrent":
+ * an independent GEMM runs concurrently with a collective in one persistent
+ * kernel with a GEMM queue and a comm queue; cfg->gemm_ctas is the explicit
+ * CTA split (the pages' gemm_wgs).
+ *
+ *   A, B, C    plain device pointers: C (M x N, gemm_dtype) = RNE16(A @ B), no bias.
+ *              M, N or K may be 0 (K = 0 writes zeros); M = 0 or N = 0 runs the
+ *              collective alone.
+ *   coll       the collective over the W heap regions, elements of coll_dtype:
+ *     IRIS_COLL_ALL_REDUCE     (IRIS_F32)  out_r[i] = sum_{s=0..W-1} in_s[i] (fp32,
+ *                              rank order) for every r; `count` elements per rank;
+ *                              off_out == off_in runs it in place.
+ *     IRIS_COLL_REDUCE_SCATTER (IRIS_F32)  out_r[i] = (sum_s in_s)[r*count/W + i];
+ *                              count % (4W) == 0.
+ *     IRIS_COLL_ALL_GATHER     (any type)  out_r[s*count + i] = in_s[i] for every r.
+ *   count      elements per rank's input (0 runs the GEMM alone); count *
+ *              element size must be a multiple of 16 bytes.
+ */
+IRIS_API int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, int64_t M,
+                                         int64_t N, int64_t K, iris_dtype gemm_dtype,
+                                         iris_coll coll, const iris_b200_heap* heap,
+                                         size_t off_in, size_t off_out, int64_t count,
+                                         iris_dtype coll_dtype, const iris_b200_config* cfg,
+                                         void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, reads the workspace status word written by the last
+ * kernels that used `workspace`, clears it, and returns IRIS_OK or
+ * IRIS_ETIMEOUT (a bounded device wait gave up; the kernel then stopped early,
+ * released its resources and left its outputs incomplete).  *device_status
+ * (may be NULL) receives the raw status; *where / *index (may be NULL) tell
+ * which wait gave up (see the kernel source) and on which flag.
+ */
+IRIS_API int iris_b200_query_status(void* workspace, cudaStream_t stream, int* device_status,
+                           int* where, int* index);
+
+/* Human-readable text of an IRIS_* code (static storage). */
+IRIS_API const char* iris_b200_strerror(int code);
+
+/* Number of SMs of the current device (the default persistent grid). */
+IRIS_API int iris_b200_num_sms(int* n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_COLLECTIVE_TILES_H */

@@ -1,0 +1,114 @@
+"""The C ABI library builds for sm_103a, loads, exports every entry point the
+header declares, and rejects bad arguments before touching the GPU.  CPU only."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gemm_collective_tiles_gb300 as gct
+from gemm_collective_tiles_gb300 import _native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_collective_tiles.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(iris_b200_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = N.load()
+    names = _declared()
+    assert set(names) == set(N.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", N.lib_path()], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (iris_b200_\w+)", out.stdout))
+    assert exported == set(names)
+
+
+def test_strerror_and_codes():
+    for code in (0, -1, -2, -3, -4, -5, -6, 123):
+        assert isinstance(N.strerror(code), str) and N.strerror(code)
+    assert N.strerror(N.IRIS_ETIMEOUT).startswith("a bounded")
+
+
+def test_workspace_size_layout():
+    lib = N.load()
+    out = ctypes.c_size_t(0)
+    # all_gather_matmul: header + W * m_blocks flags
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 4096, 14336, 4096, 8, N.IRIS_BF16,
+                                        None, ctypes.byref(out)) == 0
+    assert out.value == 256 + ((8 * 32 * 4 + 255) // 256) * 256
+    # reduce-scatter: flags per (rank, tile) + W fp32 partials of M x N
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 4096, 4096, 4096, 4, N.IRIS_F16,
+                                        None, ctypes.byref(out)) == 0
+    flags = 4 * 32 * 16 * 4
+    assert out.value == 256 + flags + 4 * 4096 * 4096 * 4
+    cfg = gct.make_config(tile_n=128)
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_ALL_REDUCE, 256, 256, 64, 2, N.IRIS_F16,
+                                        ctypes.byref(cfg), ctypes.byref(out)) == 0
+    assert out.value == 256 + 256 + 2 * 256 * 256 * 4
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_CONCURRENT, 8192, 8192, 8192, 8, N.IRIS_BF16,
+                                        None, ctypes.byref(out)) == 0
+    assert out.value == 256
+    # bad arguments
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_CONCURRENT, -1, 8, 8, 1, 0, None, ctypes.byref(out)) == N.IRIS_EINVAL
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_CONCURRENT, 8, 8, 8, 0, 0, None, ctypes.byref(out)) == N.IRIS_EINVAL
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_CONCURRENT, 8, 8, 8, 17, 0, None, ctypes.byref(out)) == N.IRIS_EINVAL
+    assert lib.iris_b200_workspace_size(9, 8, 8, 8, 1, 0, None, ctypes.byref(out)) == N.IRIS_EINVAL
+    assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, None, None) == N.IRIS_EINVAL
+    bad = gct.make_config(tile_n=96)
+    assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, ctypes.byref(bad), ctypes.byref(out)) == N.IRIS_EINVAL
+
+
+def _heap(world=2, stride=1 << 20, base=1 << 20):
+    return N.iris_b200_heap(base, stride, world)
+
+
+def test_argument_checks_before_any_gpu_work():
+    lib = N.load()
+    h = _heap()
+    hp = ctypes.byref(h)
+    # null heap
+    assert lib.iris_b200_all_gather_matmul(None, 0, 0, N.IRIS_NO_BIAS, 0, 0, 8, 8, 16, 0, None, None, 0, None) == N.IRIS_EINVAL
+    # world out of range
+    bad = _heap(world=0)
+    assert lib.iris_b200_matmul_all_reduce(ctypes.byref(bad), 0, 0, N.IRIS_NO_BIAS, 0, 8, 8, 8, 0, None, None, 0, None) == N.IRIS_EINVAL
+    # misaligned heap stride / base
+    bad = _heap(stride=(1 << 20) + 8)
+    assert lib.iris_b200_matmul_all_reduce(ctypes.byref(bad), 0, 0, N.IRIS_NO_BIAS, 0, 8, 8, 8, 0, None, None, 0, None) == N.IRIS_EALIGN
+    bad = _heap(base=(1 << 20) + 4)
+    assert lib.iris_b200_matmul_all_reduce(ctypes.byref(bad), 0, 0, N.IRIS_NO_BIAS, 0, 8, 8, 8, 0, None, None, 0, None) == N.IRIS_EALIGN
+    # K not divisible by W; K_local not a multiple of 8; N not a multiple of 8
+    assert lib.iris_b200_all_gather_matmul(hp, 0, 0, N.IRIS_NO_BIAS, 0, 0, 8, 8, 15, 0, None, None, 0, None) == N.IRIS_EINVAL
+    assert lib.iris_b200_all_gather_matmul(hp, 0, 0, N.IRIS_NO_BIAS, 0, 0, 8, 8, 12, 0, None, None, 0, None) == N.IRIS_EALIGN
+    assert lib.iris_b200_all_gather_matmul(hp, 0, 0, N.IRIS_NO_BIAS, 0, 0, 8, 12, 16, 0, None, None, 0, None) == N.IRIS_EALIGN
+    # unsupported dtype for a GEMM operand
+    assert lib.iris_b200_all_gather_matmul(hp, 0, 0, N.IRIS_NO_BIAS, 0, 0, 8, 8, 16, 2, None, None, 0, None) == N.IRIS_EINVAL
+    # reduce-scatter: N not divisible by W, N/W not a multiple of 8
+    assert lib.iris_b200_matmul_reduce_scatter(hp, 0, 0, N.IRIS_NO_BIAS, 0, 8, 12, 8, 0, None, None, 0, None) in (N.IRIS_EINVAL, N.IRIS_EALIGN)
+    assert lib.iris_b200_matmul_reduce_scatter(hp, 0, 0, N.IRIS_NO_BIAS, 0, 8, 8, 8, 0, None, None, 0, None) == N.IRIS_EALIGN
+    # all-gather along M: M not divisible by W
+    assert lib.iris_b200_matmul_all_gather(hp, 0, 0, N.IRIS_NO_BIAS, 0, 7, 8, 8, 0, None, None, 0, None) == N.IRIS_EINVAL
+    # negative sizes
+    assert lib.iris_b200_matmul_all_reduce(hp, 0, 0, N.IRIS_NO_BIAS, 0, -8, 8, 8, 0, None, None, 0, None) == N.IRIS_EINVAL
+    # concurrent: misaligned GEMM pointer, bad collective sizes
+    assert lib.iris_b200_concurrent_gemm_collective(8, 16, 32, 8, 8, 8, 0, 1, None, 0, 0, 0, 2, None, None, 0, None) == N.IRIS_EALIGN
+    assert lib.iris_b200_concurrent_gemm_collective(None, None, None, 0, 0, 0, 0, 1, hp, 0, 0, 3, 2, None, None, 0, None) == N.IRIS_EALIGN
+    assert lib.iris_b200_concurrent_gemm_collective(None, None, None, 0, 0, 0, 0, 1, hp, 0, 0, 8, 1, None, None, 0, None) == N.IRIS_EUNSUPPORTED
+    assert lib.iris_b200_concurrent_gemm_collective(None, None, None, 0, 0, 0, 0, 7, hp, 0, 0, 8, 2, None, None, 0, None) == N.IRIS_EINVAL
+    assert lib.iris_b200_concurrent_gemm_collective(None, None, None, 0, 0, 0, 0, 2, hp, 0, 0, 12, 2, None, None, 0, None) == N.IRIS_EALIGN
+    # query_status needs a workspace
+    assert lib.iris_b200_query_status(None, None, None, None, None) == N.IRIS_EINVAL
+
+
+def test_config_builder_rejects_unknown_keys():
+    c = gct.make_config(tile_n=128, gemm_ctas=-1, wait_ns=10**6)
+    assert c.tile_n == 128 and c.gemm_ctas == -1 and c.wait_ns == 10**6
+    with pytest.raises(KeyError):
+        gct.make_config(bogus=1)
