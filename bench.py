@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GEMM + collective kernels on GB300.
+
+One step = one call of the fused op over one batch of synthetic input: by
+default matmul_reduce_scatter, W=4 emulated ranks, A_r and B_r 4096 x 4096
+fp16, bias fp16 (N = 4096), uniform inputs (seed 1) -- all W ranks' GEMMs,
+the fp32 partials, the rank-order reduction and the scatter run inside the
+one persistent kernel.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--config '{"gemm_ctas": 100}']
+
+--impl reference times the CPU oracle (the plain definition of the same op)
+on this machine's host cores, each step a bounded sample of the workload.
+Under torchrun every rank runs an independent replica (the emulated ranks all
+live on one GPU; there is no data-path collective between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "fused AG+GEMM / GEMM+RS TFLOPS on 1 GB300; % of max(tensor, HBM) roofline"
+DEFAULT_WORKLOAD = "mm_rs_w4_4096"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_NAME = "fused_gemm_coll_kernel"
+OP_NAMES = {"ag_mm": "all_gather_matmul", "mm_rs": "matmul_reduce_scatter",
+            "mm_ag": "matmul_all_gather", "mm_ar": "matmul_all_reduce"}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gemm_collective_tiles_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this workload,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (OpenBLAS queried directly when loaded)."""
+    try:
+        import numpy  # noqa: F401
+        with open("/proc/self/maps") as f:
+            libs = {line.split()[-1] for line in f if "openblas" in line.lower() and line.split()[-1].startswith("/")}
+        for lib in libs:
+            try:
+                fn = ctypes.CDLL(lib).openblas_get_num_threads
+                fn.restype = ctypes.c_int
+                n = int(fn())
+                if n > 0:
+                    return n
+            except (OSError, AttributeError):
+                continue
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ CPU side
+
+def oracle_rows(wl: dict, x, rows: int):
+    """Run the oracle on the first `rows` output rows of every rank (all of N
+    and K): returns the flops that sample represents."""
+    import oracle
+    op, W = wl["op"], wl["W"]
+    if op == "mm_rs":
+        oracle.matmul_reduce_scatter([a[:rows] for a in x.A], x.B, x.bias)
+        return 2.0 * W * rows * wl["N"] * wl["K"]
+    if op == "mm_ar":
+        oracle.matmul_all_reduce([a[:rows] for a in x.A], x.B, x.bias)
+        return 2.0 * W * rows * wl["N"] * wl["K"]
+    if op == "ag_mm":
+        oracle.all_gather_matmul([a[:rows] for a in x.A], x.B[0], x.bias)
+        return 2.0 * rows * wl["N"] * wl["K"]
+    oracle.matmul_all_gather([a[:rows] for a in x.A], x.B[0], x.bias)
+    return 2.0 * W * rows * wl["N"] * wl["K"]
+
+
+def oracle_sampled(wl: dict, x, n: int, seed: int):
+    """Oracle on n sampled output elements: returns the flops they represent."""
+    import oracle
+    op, W, M, N, K = wl["op"], wl["W"], wl["M"], wl["N"], wl["K"]
+    if op == "mm_rs":
+        ii, jj = synthetic.sample_indices(M, N // W, seed, n=n, tile_m=1, tile_n=1)
+        ii, jj = ii[:n].numpy(), jj[:n].numpy()
+        oracle.matmul_reduce_scatter_at(x.A, x.B, x.bias, seed % W, ii, jj)
+        return 2.0 * W * K * len(ii)
+    ii, jj = synthetic.sample_indices(M, N, seed, n=n, tile_m=1, tile_n=1)
+    ii, jj = ii[:n].numpy(), jj[:n].numpy()
+    if op == "mm_ar":
+        oracle.matmul_all_reduce_at(x.A, x.B, x.bias, ii, jj)
+        return 2.0 * W * K * len(ii)
+    if op == "ag_mm":
+        oracle.all_gather_matmul_at(x.A, x.B[0], x.bias, ii, jj)
+        return 2.0 * K * len(ii)
+    oracle.matmul_all_gather_at(x.A, x.B[0], x.bias, ii, jj)
+    return 2.0 * K * len(ii)
+
+
+def cpu_baseline(wl: dict, x, target_s: float = 12.0):
+    """The oracle, as it stands, on a bounded row-slice of the workload."""
+    rows = 32
+    t0 = time.perf_counter()
+    flops = oracle_rows(wl, x, rows)
+    dt = time.perf_counter() - t0
+    rows = int(min(wl["M"] if wl["op"] != "mm_ag" else wl["M"] // wl["W"], max(rows, rows * target_s / max(dt, 1e-3) * 0.8)))
+    t0 = time.perf_counter()
+    flops = oracle_rows(wl, x, rows)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {rows} output rows of every rank (full N={wl['N']}, K={wl['K']}), "
+                      f"{flops:.3g} flop in {dt:.2f} s (fp64 dot products, numpy BLAS)"}
+
+
+def run_reference(args, wl, name):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = synthetic.make_fused_inputs(**wl)
+    steps, warm = args.steps, args.warmup
+    budget = 150.0
+    t0 = time.perf_counter()
+    oracle_sampled(wl, x, 16, 0)
+    t16 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_sampled(wl, x, 64, 0)
+    t64 = time.perf_counter() - t0
+    per = max((t64 - t16) / 48, 1e-6)
+    fixed = max(t16 - 16 * per, 0.0)
+    n = int(max(1, min(4096, (budget / (steps + warm) - fixed) / per)))
+    for i in range(warm):
+        oracle_sampled(wl, x, n, 1 + i)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flops += oracle_sampled(wl, x, n, 1000 + i)
+    dt = time.perf_counter() - t0
+    val = flops / dt / 1e12
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, name, {}),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} sampled output elements per step (fp64 dot products over all W ranks)"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU side
+
+def workload_config(wl, name, cfg):
+    d = {"workload": f"{OP_NAMES[wl['op']]} W={wl['W']} M={wl['M']} N={wl['N']} K={wl['K']} "
+                     f"{wl['dtype']}{' +bias' if wl.get('bias') else ''} ({name})",
+         "op": OP_NAMES[wl["op"]], "world_size_emulated": wl["W"], "M": wl["M"], "N": wl["N"],
+         "K": wl["K"], "seed": wl["seed"], "dist": wl["dist"]}
+    d.update({k: v for k, v in cfg.items()})
+    return d
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--config", default="{}", help="JSON dict of iris_b200_config fields")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    wl = dict(synthetic.WORKLOADS[args.workload])
+    cfg = json.loads(args.config)
+
+    if args.impl == "reference":
+        return run_reference(args, wl, args.workload)
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    from gemm_collective_tiles_gb300 import query_status
+    from gemm_collective_tiles_gb300.runner import FusedProblem
+
+    x = synthetic.make_fused_inputs(**wl)
+    prob = FusedProblem(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"], wl["dtype"], bias=wl.get("bias", False),
+                        config=cfg)
+    prob.upload(x.A, x.B, x.bias)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(args.warmup):
+        prob.run(stream)
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after warm-up: {rc}")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                      # evict L2 between steps (outside the step events)
+        starts[i].record(stream)
+        prob.run(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after timed steps: {rc}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = prob.flops()
+    value = flops * K * world / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / K
+
+    # roofline of the one kernel per step
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])   # fp16 and bf16 share the nominal dense rate (ratio 1)
+    achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json) x 1.0 fp16/bf16 nominal ratio",
+                "kernel": KERNEL_NAME, "median_ms": statistics.median(step_ms)}
+
+    # end to end: pinned host inputs -> heap, fused op, outputs -> pinned host
+    pin_A = [a.pin_memory() for a in x.A]
+    pin_B = [b.pin_memory() for b in x.B]
+    pin_bias = x.bias.pin_memory() if x.bias is not None else None
+    out_views = [prob.heap.view(prob.out, r) for r in range(wl["W"])] if wl["op"] == "mm_rs" else \
+        [prob.heap.view(prob.out, 0)]
+    host_out = [torch.empty(v.shape, dtype=v.dtype).pin_memory() for v in out_views]
+    h2d = prob.input_bytes()
+    d2h = sum(v.numel() * v.element_size() for v in out_views)
+    E = max(3, args.e2e_steps)
+    for i in range(3 + E):
+        if i == 3:
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        prob.upload(pin_A, pin_B, pin_bias, non_blocking=True)
+        prob.run(stream)
+        for h, v in zip(host_out, out_views):
+            h.copy_(v, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    if pg:
+        t = torch.tensor([e2e_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after e2e steps: {rc}")
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        del flush
+        cpu = cpu_baseline(wl, x)
+    cfg_out = workload_config(wl, args.workload, cfg)
+    cfg_out["l2"] = "flushed before every step (258 MB memset outside the step's events)"
+    cfg_out["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU"
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic", "config": cfg_out,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K,
+            "clocks": clocks, "wall_s_timed_region": wall}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
