@@ -21,6 +21,8 @@ IRIS_ETIMEOUT = -5
 IRIS_EUNSUPPORTED = -6
 IRIS_NO_BIAS = ctypes.c_size_t(-1).value
 IRIS_MAX_WORLD = 16
+IRIS_NOALLOC_MAX_FLAGS = 16384
+IRIS_NOALLOC_SCRATCH_BYTES = 256 + 4 * IRIS_NOALLOC_MAX_FLAGS
 
 IRIS_F16, IRIS_BF16, IRIS_F32 = 0, 1, 2
 IRIS_COLL_ALL_GATHER, IRIS_COLL_ALL_REDUCE, IRIS_COLL_REDUCE_SCATTER = 0, 1, 2
@@ -31,6 +33,7 @@ IRIS_COLL_ALL_GATHER, IRIS_COLL_ALL_REDUCE, IRIS_COLL_REDUCE_SCATTER = 0, 1, 2
 EXPORTS = (
     "iris_b200_workspace_size",
     "iris_b200_all_gather_matmul",
+    "iris_b200_all_gather_matmul_noalloc",
     "iris_b200_matmul_reduce_scatter",
     "iris_b200_matmul_all_gather",
     "iris_b200_matmul_all_reduce",
@@ -76,6 +79,7 @@ def _declare(lib):
     sig = {
         "iris_b200_workspace_size": (ci, [ci, i64, i64, i64, ci, ci, cfgp, P(sz)]),
         "iris_b200_all_gather_matmul": (ci, [heapp, sz, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp, sz, vp]),
+        "iris_b200_all_gather_matmul_noalloc": (ci, [heapp, sz, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp]),
         "iris_b200_matmul_reduce_scatter": (ci, [heapp, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp, sz, vp]),
         "iris_b200_matmul_all_gather": (ci, [heapp, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp, sz, vp]),
         "iris_b200_matmul_all_reduce": (ci, [heapp, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp, sz, vp]),
@@ -131,6 +135,10 @@ def iris_b200_workspace_size(op, M, N, K, world, dtype, cfg, bytes_out):
 
 def iris_b200_all_gather_matmul(*args):
     return load().iris_b200_all_gather_matmul(*args)
+
+
+def iris_b200_all_gather_matmul_noalloc(*args):
+    return load().iris_b200_all_gather_matmul_noalloc(*args)
 
 
 def iris_b200_matmul_reduce_scatter(*args):

@@ -507,3 +507,45 @@ int iris_b200_query_status(void* workspace, cudaStream_t stream, int* device_sta
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation variant of all_gather_matmul: the workspace (header + flags)
+// is a static device array of this translation unit instead of caller memory.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[IRIS_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the static scratch on the current device; the first call
+// per device looks it up and zero-fills it on `stream`.
+int noalloc_scratch(cudaStream_t stream, void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IRIS_ECUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return IRIS_ECUDA;
+        if (cudaMemsetAsync(p, 0, IRIS_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return IRIS_ECUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return IRIS_OK;
+}
+}  // namespace
+
+extern "C" int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, size_t off_A, size_t off_B,
+                                                   size_t off_bias, size_t off_out, size_t off_gathered,
+                                                   int64_t M, int64_t N, int64_t K, iris_dtype dtype,
+                                                   const iris_b200_config* cfg, cudaStream_t stream) {
+    if (!heap || heap->world < 1 || heap->world > IRIS_MAX_WORLD || M < 0) return IRIS_EINVAL;
+    const int64_t flags = int64_t(heap->world) * ((M + BM - 1) / BM);
+    if (flags > IRIS_NOALLOC_MAX_FLAGS) return IRIS_ENOWS;
+    void* scratch = nullptr;
+    int rc = noalloc_scratch(stream, &scratch);
+    if (rc != IRIS_OK) return rc;
+    // queue counters and status start at zero for this call; the epoch (first
+    // 4 bytes) carries over so flags left by earlier calls never match
+    if (cudaMemsetAsync(static_cast<char*>(scratch) + 4, 0, 28, stream) != cudaSuccess) return IRIS_ECUDA;
+    return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, cfg,
+                                       scratch, IRIS_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -226,6 +226,39 @@ IRIS_API int iris_b200_concurrent_gemm_collective(const void* A, const void* B, 
                                          cudaStream_t stream);
 
 /*
+ * all_gather_matmul without a caller-provided workspace.  This entry point
+ * has no counterpart on the pages; it exists for callers that cannot
+ * allocate device memory themselves -- e.g. code running where cudaMalloc is
+ * forbidden or unavailable (inside a CUDA-graph capture, a custom allocator's
+ * own bootstrap, or a host framework that owns every allocation) -- and still
+ * want the fused op.  The caller passes the heap (inputs and outputs) exactly
+ * as for iris_b200_all_gather_matmul.  The queue counters, launch epoch,
+ * status word and ready-flags live instead in a fixed static device array of
+ * IRIS_NOALLOC_SCRATCH_BYTES bytes inside this library (every GPU that loads
+ * the library holds it until the process exits).
+ *   - Limit: W * ceil(M / 128) ready-flags must fit, i.e. W * ceil(M/128) <=
+ *     IRIS_NOALLOC_MAX_FLAGS; larger problems return IRIS_ENOWS and launch
+ *     nothing.
+ *   - The first call on a device looks up the array's device address and
+ *     zero-fills it (cudaMemsetAsync on `stream`); make that first call before
+ *     any stream capture.  Every call then clears the queue counters and the
+ *     status word (one cudaMemsetAsync of 28 bytes on `stream`) and launches
+ *     the kernel.  No call allocates or frees memory.
+ *   - All calls share the one array: calls whose kernels overlap on the GPU
+ *     (different streams, or several host threads) race and must not be made.
+ *   - A bounded device wait that gives up is recorded in the array and
+ *     cleared by the next call; it is not reported to the caller (use the
+ *     workspace entry point and iris_b200_query_status when that is needed).
+ */
+#define IRIS_NOALLOC_MAX_FLAGS 16384
+#define IRIS_NOALLOC_SCRATCH_BYTES (256 + 4 * IRIS_NOALLOC_MAX_FLAGS)
+IRIS_API int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, size_t off_A,
+                                                 size_t off_B, size_t off_bias, size_t off_out,
+                                                 size_t off_gathered, int64_t M, int64_t N,
+                                                 int64_t K, iris_dtype dtype,
+                                                 const iris_b200_config* cfg, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word written by the last
  * kernels that used `workspace`, clears it, and returns IRIS_OK or
  * IRIS_ETIMEOUT (a bounded device wait gave up; the kernel then stopped early,
