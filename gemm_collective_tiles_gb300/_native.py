@@ -58,6 +58,10 @@ class iris_b200_config(ctypes.Structure):
         ("grid", ctypes.c_int),
         ("wait_ns", ctypes.c_ulonglong),
         ("debug_skip_flag", ctypes.c_int),
+        ("trace_buf", ctypes.c_ulonglong),
+        ("trace_cap", ctypes.c_int),
+        ("reduce_mode", ctypes.c_int),
+        ("rank_inner", ctypes.c_int),
     ]
 
 

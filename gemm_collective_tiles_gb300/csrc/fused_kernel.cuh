@@ -4,14 +4,15 @@
 // swizzle, explicit GEMM/comm CTA split; iris docs "Fused Communication and
 // Compute Operations" for the four dependent ops).
 //
-// CTA layout (320 threads, one CTA per SM):
-//   warp 0      scheduler + TMA producer (lane 0): claims work items from the
-//               two global queues with atomics, publishes them into a small
-//               shared-memory item ring and, for GEMM items, streams the A/B
-//               K-blocks into a STAGES-deep shared-memory pipeline with TMA.
+// CTA layout (352 threads, one CTA per SM):
+//   warp 0      scheduler (lane 0): claims work items from the two global
+//               queues with atomics and publishes them into a small
+//               shared-memory item ring, ahead of the warps that run them.
 //   warp 1      tensor-memory owner; lane 0 issues tcgen05.mma (128 x BN x 16
 //               steps, fp32 accumulators in TMEM, double-buffered).
-//   warps 2..9  workers: GEMM epilogue (tcgen05.ld -> +bias -> fp16/bf16 or
+//   warp 2      TMA producer (lane 0): for GEMM items streams the A/B K-blocks
+//               into a STAGES-deep shared-memory pipeline.
+//   warps 3..10 workers: GEMM epilogue (tcgen05.ld -> +bias -> fp16/bf16 or
 //               fp32 partial -> global) and comm tiles (128-bit vector copy /
 //               rank-order fp32 reduce), so the comm tiles of one SM run
 //               while its tensor cores work on the next GEMM tile.
@@ -33,7 +34,8 @@ constexpr int BM = 128;           // tile rows (tcgen05 M for cta_group::1)
 constexpr int BK = 64;            // K per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int NUM_WORKER_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_WORKER_WARPS;
+constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
+constexpr int NUM_THREADS = 32 * (FIRST_WORKER_WARP + NUM_WORKER_WARPS);
 constexpr int RING = 8;           // work-item ring depth
 constexpr uint32_t ITEM_END = 0xFFFFFFFFu;
 constexpr uint32_t ITEM_COMM = 0x80000000u;
@@ -53,6 +55,7 @@ enum : int {
     WAIT_WORKER_SYNC = 10,
     WAIT_TEARDOWN_TMA = 11,
     WAIT_TEARDOWN_MMA = 12,
+    WAIT_ITEM_FULL_TMA = 13,
 };
 
 // First 256 bytes of the workspace.
@@ -94,6 +97,40 @@ struct Params {
     int elem_bytes;
     unsigned long long wait_ns;
     uint32_t debug_skip;               // flag index + 1 that is never released (0 = none)
+    int reduce_mode;                   // reduce ops: 0 = last arriving rank reduces, 1 = comm queue
+    int rank_inner;                    // reduce ops: 1 = rank index fastest in the GEMM item order
+    unsigned long long* trace;         // optional per-CTA event trace (nullptr = off)
+    int trace_cap;                     // events per (CTA, role)
+};
+
+// Optional timeline: each CTA owns 4 role streams (scheduler, MMA, TMA,
+// workers) of trace_cap (event, globaltimer ns) pairs; slot 0 of a stream
+// holds its event count.
+enum : int { TR_SCHED = 0, TR_MMA = 1, TR_TMA = 2, TR_WORK = 3 };
+enum : unsigned long long { EV_CLAIM = 1, EV_BEGIN = 2, EV_END = 3, EV_READY = 4 };
+struct Tracer {
+    unsigned long long* buf = nullptr;
+    int cap = 0, n = 0;
+    __device__ void init(const Params& p, int role) {
+        if (p.trace && p.trace_cap > 1) {
+            buf = p.trace + (static_cast<size_t>(blockIdx.x) * 4 + role) * p.trace_cap * 2;
+            cap = p.trace_cap;
+            n = 1;
+        }
+    }
+    __device__ __forceinline__ void rec(unsigned long long ev, uint32_t item) {
+        if (buf && n < cap) {
+            buf[2 * n] = (ev << 56) | item;
+            buf[2 * n + 1] = global_timer_ns();
+            ++n;
+        }
+    }
+    __device__ void finish() {
+        if (buf) {
+            buf[0] = static_cast<unsigned long long>(n - 1);
+            buf[1] = 0;
+        }
+    }
 };
 
 struct Ctl {
@@ -113,6 +150,22 @@ __device__ __noinline__ void raise_timeout(const Ctl& c, int where, int index) {
     }
     __threadfence();
     atomicExch(&c.ws->abort_epoch, c.epoch);
+}
+
+// Epoch-tagged arrival counter (high 32 bits: launch epoch, low 32: count):
+// returns this arrival's count within the current launch (1 = first).  A
+// counter left by an earlier (or aborted) launch is restarted, so no per-launch
+// reset is needed.  Lock-free: each failed CAS means another arrival succeeded.
+__device__ __forceinline__ uint32_t arrive_count(unsigned long long* ctr, uint32_t epoch) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    while (true) {
+        const unsigned long long want = (static_cast<uint32_t>(cur >> 32) == epoch)
+                                            ? cur + 1
+                                            : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        if (prev == cur) return static_cast<uint32_t>(want);
+        cur = prev;
+    }
 }
 
 // Bounded wait on an mbarrier phase. false = gave up (timeout or abort).
@@ -175,15 +228,31 @@ __device__ __forceinline__ void swizzle_tile(const Params& p, uint32_t t, int& m
 }
 
 // The GEMM item -> (rank, m block, n block, output tile).
+// Reduce ops run W GEMMs over the same output tiles.  By default the items of
+// one GROUP_M swizzle group are ordered rank by rank (all of rank 0's tiles of
+// the group, then rank 1's, ...), so the L2 holds one rank's A rows and B at a
+// time; with rank_inner the rank index moves fastest instead.
 struct GemmCoord {
     int rank, mb, nb;
     uint32_t tile;
 };
+__device__ __forceinline__ uint32_t group_tiles(const Params& p) {
+    return static_cast<uint32_t>(p.group_m) * p.n_blocks;
+}
 __device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t g) {
     GemmCoord gc;
     if (p.op == OP_MM_RS || p.op == OP_MM_AR) {
-        gc.tile = g / p.W;
-        gc.rank = static_cast<int>(g % p.W);
+        if (p.rank_inner) {
+            gc.tile = g / p.W;
+            gc.rank = static_cast<int>(g % p.W);
+        } else {
+            const uint32_t T = group_tiles(p);
+            const uint32_t sg = g / (T * p.W);
+            const uint32_t Tsg = min(T, static_cast<uint32_t>(p.n_tiles) - sg * T);
+            const uint32_t local = g - sg * T * p.W;
+            gc.rank = static_cast<int>(local / Tsg);
+            gc.tile = sg * T + (local - static_cast<uint32_t>(gc.rank) * Tsg);
+        }
     } else {
         gc.tile = g;
         gc.rank = 0;
@@ -191,6 +260,14 @@ __device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t g) {
     swizzle_tile(p, gc.tile, gc.mb, gc.nb);
     if (p.op == OP_MM_AG) gc.rank = gc.mb / p.mb_per_rank;
     return gc;
+}
+// Inverse for the reduce ops: the GEMM item of (output tile t, rank s).
+__device__ __forceinline__ uint32_t gemm_index(const Params& p, uint32_t t, int s) {
+    if (p.rank_inner) return t * p.W + s;
+    const uint32_t T = group_tiles(p);
+    const uint32_t sg = t / T;
+    const uint32_t Tsg = min(T, static_cast<uint32_t>(p.n_tiles) - sg * T);
+    return sg * T * p.W + static_cast<uint32_t>(s) * Tsg + (t - sg * T);
 }
 
 // all_gather_matmul: number of gather items that must be claimed before GEMM
@@ -230,6 +307,7 @@ struct Smem {
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
+    uint32_t* bcast;
 
     __device__ void carve(uint8_t* raw) {
         uintptr_t a = reinterpret_cast<uintptr_t>(raw);
@@ -248,21 +326,26 @@ struct Smem {
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
+        bcast = u + RING + 2;
     }
     __device__ uint8_t* a_tile(uint32_t s) const { return tiles + s * STAGE_BYTES; }
     __device__ uint8_t* b_tile(uint32_t s) const { return tiles + s * STAGE_BYTES + A_BYTES; }
 };
 
-// ============================================================ producer
+// ============================================================ scheduler
+// Claims work items from the two global queues and publishes them, in claim
+// order, into the CTA's item ring.  An item is published only after every item
+// it depends on has been claimed (by this or another CTA), so the ring order of
+// every CTA is a topological order of the dependency graph and no CTA can wait
+// on work that nobody will run.
 template <int BN, int STAGES>
-__device__ void run_producer(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
-    uint32_t stage = 0, phase = 0, ring_n = 0;
-    uint32_t issued_phase[STAGES];
-    uint32_t used_mask = 0;
+__device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
+    Tracer tr;
+    tr.init(p, TR_SCHED);
+    uint32_t ring_n = 0;
     bool gemm_dry = (p.n_gemm == 0), comm_dry = (p.n_comm == 0);
     const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
     const bool prefer_gemm = p.gemm_ctas < 0 || static_cast<int>(blockIdx.x) < p.gemm_ctas;
-    const int b_rank_dim = reduce_op ? 1 : 0;
 
     auto publish = [&](uint32_t item) -> bool {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
@@ -270,12 +353,116 @@ __device__ void run_producer(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& 
         sm.ring[slot] = item;
         mbar_arrive(&sm.item_full[slot]);
         ++ring_n;
+        tr.rec(EV_CLAIM, item);
         return true;
     };
 
+    // Take one GEMM item (after claiming the gather items it depends on).
+    auto take_gemm = [&](bool& got) -> bool {
+        got = false;
+        if (gemm_dry) return true;
+        const uint32_t g = atomicAdd(&p.ws->gemm_ctr, 1u);
+        if (g >= p.n_gemm) {
+            gemm_dry = true;
+            return true;
+        }
+        if (p.op == OP_AG_MM) {
+            const uint32_t la = min(g + p.lookahead, p.n_gemm - 1);
+            const uint32_t need = gather_need(p, la);
+            while (!comm_dry && ld_relaxed_gpu(&p.ws->comm_ctr) < need) {
+                const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
+                if (c >= p.n_comm) {
+                    comm_dry = true;
+                    break;
+                }
+                if (!publish(ITEM_COMM | c)) return false;
+            }
+        }
+        if (!publish(g)) return false;
+        got = true;
+        return true;
+    };
+
+    // Take one comm item.  Reduce ops: claim the GEMM items it depends on
+    // first (help), or -- with only_if_ready -- take it only when all its
+    // partials are already flagged (never blocks).
+    auto take_comm = [&](bool& got, bool only_if_ready) -> bool {
+        got = false;
+        if (comm_dry) return true;
+        if (reduce_op && only_if_ready) {
+            const uint32_t c = ld_relaxed_gpu(&p.ws->comm_ctr);
+            if (c >= p.n_comm) return true;
+            if (ld_relaxed_gpu(&p.ws->gemm_ctr) < gemm_index(p, c, p.W - 1) + 1) return true;
+            for (int s = 0; s < p.W; ++s)
+                if (ld_relaxed_gpu(&p.flags[gemm_index(p, c, s)]) != ctl.epoch) return true;
+            if (atomicCAS(&p.ws->comm_ctr, c, c + 1) != c) return true;
+            if (!publish(ITEM_COMM | c)) return false;
+            got = true;
+            return true;
+        }
+        const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
+        if (c >= p.n_comm) {
+            comm_dry = true;
+            return true;
+        }
+        if (reduce_op) {
+            const uint32_t need = gemm_index(p, c, p.W - 1) + 1;
+            while (!gemm_dry && ld_relaxed_gpu(&p.ws->gemm_ctr) < need) {
+                const uint32_t g = atomicAdd(&p.ws->gemm_ctr, 1u);
+                if (g >= p.n_gemm) {
+                    gemm_dry = true;
+                    break;
+                }
+                if (!publish(g)) return false;
+            }
+        }
+        if (!publish(ITEM_COMM | c)) return false;
+        got = true;
+        return true;
+    };
+
+    bool ok = true;
+    while (ok && !(gemm_dry && comm_dry)) {
+        bool gemm_first = prefer_gemm;
+        if (p.gemm_ctas < 0 && !comm_dry && !gemm_dry && !reduce_op && p.op != OP_AG_MM) {
+            // balanced: keep the two queues' fractional progress equal
+            const unsigned long long gc = min(ld_relaxed_gpu(&p.ws->gemm_ctr), p.n_gemm);
+            const unsigned long long cc = min(ld_relaxed_gpu(&p.ws->comm_ctr), p.n_comm);
+            gemm_first = gc * p.n_comm <= cc * p.n_gemm;
+        }
+        bool got = false;
+        if (reduce_op && gemm_first && !gemm_dry) {
+            ok = take_comm(got, true);
+            if (!ok) break;
+        }
+        if (gemm_first) {
+            ok = take_gemm(got);
+            if (ok && !got) ok = take_comm(got, false);
+        } else {
+            ok = take_comm(got, false);
+            if (ok && !got) ok = take_gemm(got);
+        }
+    }
+    if (ok) publish(ITEM_END);
+    tr.finish();
+}
+
+// ============================================================ TMA producer
+// Follows the item ring; for every GEMM item streams its K-blocks of A and B
+// into the STAGES-deep shared-memory pipeline (acquiring the gather flags of
+// all_gather_matmul shards just before their first K-block).
+template <int BN, int STAGES>
+__device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
+    Tracer tr;
+    tr.init(p, TR_TMA);
+    uint32_t stage = 0, phase = 0, ring_n = 0;
+    uint32_t issued_phase[STAGES];
+    uint32_t used_mask = 0;
+    const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
+
     auto load_gemm = [&](uint32_t g) -> bool {
         const GemmCoord gc = decode_gemm(p, g);
-        int a_row, a_rank, b_rank;
+        int a_row, a_rank;
         if (p.op == OP_MM_AG) {
             a_row = (gc.mb % p.mb_per_rank) * BM;
             a_rank = gc.rank;
@@ -283,7 +470,7 @@ __device__ void run_producer(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& 
             a_row = gc.mb * BM;
             a_rank = reduce_op ? gc.rank : 0;
         }
-        b_rank = b_rank_dim ? gc.rank : 0;
+        const int b_rank = reduce_op ? gc.rank : 0;
         int acquired = 0;  // all_gather_matmul: shards whose flags are held
         for (int kb = 0; kb < p.k_blocks; ++kb) {
             if (p.op == OP_AG_MM) {
@@ -314,96 +501,19 @@ __device__ void run_producer(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& 
         return true;
     };
 
-    // Take one GEMM item (after claiming the gather items it depends on).
-    auto take_gemm = [&](bool& got) -> bool {
-        got = false;
-        if (gemm_dry) return true;
-        const uint32_t g = atomicAdd(&p.ws->gemm_ctr, 1u);
-        if (g >= p.n_gemm) {
-            gemm_dry = true;
-            return true;
-        }
-        if (p.op == OP_AG_MM) {
-            const uint32_t la = min(g + p.lookahead, p.n_gemm - 1);
-            const uint32_t need = gather_need(p, la);
-            while (!comm_dry && ld_relaxed_gpu(&p.ws->comm_ctr) < need) {
-                const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
-                if (c >= p.n_comm) {
-                    comm_dry = true;
-                    break;
-                }
-                if (!publish(ITEM_COMM | c)) return false;
-            }
-        }
-        if (!publish(g)) return false;
-        if (!load_gemm(g)) return false;
-        got = true;
-        return true;
-    };
-
-    // Take one comm item.  Reduce ops: claim the GEMM items it depends on
-    // first (help), or -- with only_if_ready -- take it only when all its
-    // partials are already flagged (never blocks).
-    auto take_comm = [&](bool& got, bool only_if_ready) -> bool {
-        got = false;
-        if (comm_dry) return true;
-        if (reduce_op && only_if_ready) {
-            const uint32_t c = ld_relaxed_gpu(&p.ws->comm_ctr);
-            if (c >= p.n_comm) return true;
-            if (ld_relaxed_gpu(&p.ws->gemm_ctr) < (c + 1) * static_cast<uint32_t>(p.W))
-                return true;
-            for (int s = 0; s < p.W; ++s)
-                if (ld_relaxed_gpu(&p.flags[c * p.W + s]) != ctl.epoch) return true;
-            if (atomicCAS(&p.ws->comm_ctr, c, c + 1) != c) return true;
-            if (!publish(ITEM_COMM | c)) return false;
-            got = true;
-            return true;
-        }
-        const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
-        if (c >= p.n_comm) {
-            comm_dry = true;
-            return true;
-        }
-        if (reduce_op) {
-            const uint32_t need = (c + 1) * static_cast<uint32_t>(p.W);
-            while (!gemm_dry && ld_relaxed_gpu(&p.ws->gemm_ctr) < need) {
-                const uint32_t g = atomicAdd(&p.ws->gemm_ctr, 1u);
-                if (g >= p.n_gemm) {
-                    gemm_dry = true;
-                    break;
-                }
-                if (!publish(g)) return false;
-                if (!load_gemm(g)) return false;
-            }
-        }
-        if (!publish(ITEM_COMM | c)) return false;
-        got = true;
-        return true;
-    };
-
-    bool ok = true;
-    while (ok && !(gemm_dry && comm_dry)) {
-        bool gemm_first = prefer_gemm;
-        if (p.gemm_ctas < 0 && !comm_dry && !gemm_dry && !reduce_op && p.op != OP_AG_MM) {
-            // balanced: keep the two queues' fractional progress equal
-            const unsigned long long gc = min(ld_relaxed_gpu(&p.ws->gemm_ctr), p.n_gemm);
-            const unsigned long long cc = min(ld_relaxed_gpu(&p.ws->comm_ctr), p.n_comm);
-            gemm_first = gc * p.n_comm <= cc * p.n_gemm;
-        }
-        bool got = false;
-        if (reduce_op && gemm_first && !gemm_dry) {
-            ok = take_comm(got, true);
-            if (!ok) break;
-        }
-        if (gemm_first) {
-            ok = take_gemm(got);
-            if (ok && !got) ok = take_comm(got, false);
-        } else {
-            ok = take_comm(got, false);
-            if (ok && !got) ok = take_gemm(got);
-        }
+    while (true) {
+        const uint32_t slot = ring_n % RING, use = ring_n / RING;
+        if (!wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_TMA)) break;
+        const uint32_t item = sm.ring[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++ring_n;
+        if (item == ITEM_END) break;
+        if (item & ITEM_COMM) continue;
+        tr.rec(EV_BEGIN, item);
+        if (!load_gemm(item)) break;
+        tr.rec(EV_END, item);
     }
-    if (ok) ok = publish(ITEM_END);
+    tr.finish();
     // drain: every TMA load issued into a stage has landed before the CTA exits
     for (int s = 0; s < STAGES; ++s)
         if (used_mask & (1u << s)) drain_bar(ctl, &sm.full[s], issued_phase[s], WAIT_TEARDOWN_TMA);
@@ -415,6 +525,8 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
     constexpr uint32_t IDESC_F16 = make_idesc(0, BM, BN);
     constexpr uint32_t IDESC_BF16 = make_idesc(1, BM, BN);
     const uint32_t idesc = p.bf16 ? IDESC_BF16 : IDESC_F16;
+    Tracer tr;
+    tr.init(p, TR_MMA);
     uint32_t stage = 0, phase = 0, ring_n = 0, acc_i = 0;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
@@ -427,6 +539,7 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
         const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
         if (!wait_bar(ctl, &sm.acc_empty[buf], (ause & 1) ^ 1, WAIT_ACC_EMPTY)) break;
         tc_fence_after();
+        tr.rec(EV_BEGIN, item);
         const uint32_t d = tmem + buf * BN;
         bool ok = true;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -455,8 +568,10 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
         }
         if (!ok) break;
         umma_commit(&sm.acc_full[buf]);
+        tr.rec(EV_END, item);
         ++acc_i;
     }
+    tr.finish();
     // drain: every MMA issued by this thread has completed
     umma_commit(sm.final_bar);
     drain_bar(ctl, sm.final_bar, 0, WAIT_TEARDOWN_MMA);
@@ -470,6 +585,9 @@ struct WorkerCtx {
     int h;      // column half of the accumulator this warp drains
     uint32_t wphase;
 };
+
+template <int BN, int STAGES>
+__device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx& wc);
 
 // barrier over the 8 worker warps built on an mbarrier (bounded, abortable)
 template <int BN, int STAGES>
@@ -487,12 +605,13 @@ __device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES>& sm
 // GEMM epilogue of one tile: TMEM -> registers -> (+bias) -> global.
 template <int BN, int STAGES>
 __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem,
-                         uint32_t g, uint32_t acc_i, WorkerCtx& wc) {
+                         uint32_t g, uint32_t acc_i, WorkerCtx& wc, Tracer& tr) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
     bool ok = true;
     if (wc.lane == 0) ok = wait_bar(ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL);
     if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return false;
     tc_fence_after();
+    tr.rec(EV_READY, g);
 
     const GemmCoord gc = decode_gemm(p, g);
     const int r_in_tile = wc.q * 32 + wc.lane;
@@ -585,7 +704,25 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
         // publish this rank's partial tile: all 8 warps' stores, then the flag
         __threadfence();
         if (!worker_sync(ctl, sm, wc)) return false;
-        if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1) st_release_gpu(&p.flags[g], ctl.epoch);
+        if (p.reduce_mode == 0) {
+            // the rank whose partial completes the tile reduces it now, while
+            // the other partials are still in L2
+            if (wc.w == 0 && wc.lane == 0) {
+                uint32_t last = 0;
+                if (p.debug_skip != g + 1)
+                    last = arrive_count(reinterpret_cast<unsigned long long*>(p.flags) + gc.tile, ctl.epoch) ==
+                           static_cast<uint32_t>(p.W);
+                __threadfence();
+                *sm.bcast = last;
+            }
+            if (!worker_sync(ctl, sm, wc)) return false;
+            if (*reinterpret_cast<volatile uint32_t*>(sm.bcast)) {
+                __threadfence();
+                reduce_body<BN, STAGES>(p, gc.tile, wc);
+            }
+        } else if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1) {
+            st_release_gpu(&p.flags[g], ctl.epoch);
+        }
     }
     return true;
 }
@@ -602,23 +739,23 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
                        static_cast<size_t>(mb) * BM * vpr;
     uint4* dst = reinterpret_cast<uint4*>(p.heap + p.off_gathered) + static_cast<size_t>(mb) * BM * Kv +
                  static_cast<size_t>(s) * vpr;
-    const int total = rows * vpr;
-    const int tid = wc.w * 32 + wc.lane;
-    constexpr int U = 8;
-    for (int base = tid; base < total; base += NUM_WORKER_WARPS * 32 * U) {
-        uint4 v[U];
+    // warp w copies rows w, w+8, ...; lanes walk the row's 16-byte vectors
+    constexpr int RU = 2, CU = 4;
+    for (int r0 = wc.w; r0 < rows; r0 += NUM_WORKER_WARPS * RU) {
+        for (int v0 = wc.lane; v0 < vpr; v0 += 32 * CU) {
+            uint4 v[RU][CU];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = base + u * NUM_WORKER_WARPS * 32;
-            if (idx < total) v[u] = src[idx];
-        }
+            for (int u = 0; u < RU; ++u)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = base + u * NUM_WORKER_WARPS * 32;
-            if (idx < total) {
-                const int r = idx / vpr, cv = idx - r * vpr;
-                dst[static_cast<size_t>(r) * Kv + cv] = v[u];
-            }
+                for (int k = 0; k < CU; ++k)
+                    if (r0 + u * NUM_WORKER_WARPS < rows && v0 + 32 * k < vpr)
+                        v[u][k] = src[static_cast<size_t>(r0 + u * NUM_WORKER_WARPS) * vpr + v0 + 32 * k];
+#pragma unroll
+            for (int u = 0; u < RU; ++u)
+#pragma unroll
+                for (int k = 0; k < CU; ++k)
+                    if (r0 + u * NUM_WORKER_WARPS < rows && v0 + 32 * k < vpr)
+                        dst[static_cast<size_t>(r0 + u * NUM_WORKER_WARPS) * Kv + v0 + 32 * k] = v[u][k];
         }
     }
     fence_proxy_async_global();
@@ -635,71 +772,90 @@ __device__ bool reduce_tile(const Params& p, const Ctl& ctl, uint32_t c, WorkerC
     bool ok = true;
     if (wc.lane == 0) {
         for (int s = 0; s < p.W && ok; ++s) {
-            const int fi = static_cast<int>(c) * p.W + s;
+            const int fi = static_cast<int>(gemm_index(p, c, s));
             ok = wait_flag(ctl, &p.flags[fi], WAIT_FLAG_PARTIAL, fi);
         }
     }
     if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return false;
+    reduce_body<BN, STAGES>(p, c, wc);
+    return true;
+}
+
+// The reduce itself: warp w takes rows w, w+8, ... of output tile c; lane l
+// takes the 16-byte column chunks l, l+32, ... of each row, so every load and
+// store instruction of a warp covers 512 contiguous bytes.  SC ranks of a row
+// are loaded together before their adds; partials are summed in rank order
+// 0..W-1 in fp32.
+template <int BN, int STAGES>
+__device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx& wc) {
+    constexpr int CPL = BN / 4 / 32;  // float4 chunks per lane per row
+    constexpr int SC = 4;             // ranks per load batch
     int mb, nb;
     swizzle_tile(p, c, mb, nb);
     const int rows = min(BM, p.M - mb * BM);
     const int cols = min(BN, p.N - nb * BN);
-    const int vpr = cols / 4;
-    const int total = rows * vpr;
-    const int tid = wc.w * 32 + wc.lane;
-    constexpr int U = 2;
-    for (int base = tid; base < total; base += NUM_WORKER_WARPS * 32 * U) {
-        float4 acc[U];
-        size_t e[U];
+    const size_t pe = p.partial_elems;
+    bool cok[CPL];
+    int dcol[CPL];
+    size_t dbase[CPL];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = base + u * NUM_WORKER_WARPS * 32;
-            if (idx < total) {
-                const int r = idx / vpr, cv = idx - r * vpr;
-                e[u] = static_cast<size_t>(mb * BM + r) * p.N + nb * BN + cv * 4;
-                acc[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + e[u]));
-            }
-        }
-        for (int s = 1; s < p.W; ++s) {
-            const float* ps = p.partials + static_cast<size_t>(s) * p.partial_elems;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = base + u * NUM_WORKER_WARPS * 32;
-                if (idx < total) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + e[u]));
-                    acc[u].x = acc[u].x + v.x;
-                    acc[u].y = acc[u].y + v.y;
-                    acc[u].z = acc[u].z + v.z;
-                    acc[u].w = acc[u].w + v.w;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = base + u * NUM_WORKER_WARPS * 32;
-            if (idx >= total) continue;
-            uint2 o;
-            o.x = pack2(acc[u].x, acc[u].y, p.bf16);
-            o.y = pack2(acc[u].z, acc[u].w, p.bf16);
-            const size_t i = e[u] / p.N;
-            const int j = static_cast<int>(e[u] - i * p.N);
-            if (p.op == OP_MM_RS) {
-                const int rr = j / p.N_local, jl = j - rr * p.N_local;
-                *reinterpret_cast<uint2*>(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_out +
-                                          (i * p.N_local + jl) * 2) = o;
-            } else {
-                const size_t off = p.off_out + e[u] * 2;
-                const int nreg = p.replicate ? p.W : 1;
-                for (int rg = 0; rg < nreg; ++rg)
-                    *reinterpret_cast<uint2*>(p.heap + static_cast<size_t>(rg) * p.rank_stride + off) = o;
-            }
+    for (int k = 0; k < CPL; ++k) {
+        const int c4 = wc.lane + 32 * k;
+        cok[k] = c4 * 4 < cols;
+        const int j = nb * BN + c4 * 4;
+        if (p.op == OP_MM_RS) {
+            const int rr = cok[k] ? j / p.N_local : 0;
+            dcol[k] = j - rr * p.N_local;
+            dbase[k] = static_cast<size_t>(rr) * p.rank_stride + p.off_out;
+        } else {
+            dcol[k] = j;
+            dbase[k] = p.off_out;
         }
     }
-    return true;
+    const int ldo = (p.op == OP_MM_RS) ? p.N_local : p.N;
+    const int nreg = (p.op == OP_MM_AR && p.replicate) ? p.W : 1;
+    for (int r = wc.w; r < rows; r += NUM_WORKER_WARPS) {
+        float4 acc[CPL];
+        const float* src0 = p.partials + static_cast<size_t>(mb * BM + r) * p.N + nb * BN;
+        for (int s0 = 0; s0 < p.W; s0 += SC) {
+            float4 v[SC][CPL];
+#pragma unroll
+            for (int ds = 0; ds < SC; ++ds)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+                    if (s0 + ds < p.W && cok[k])
+                        v[ds][k] = __ldcg(reinterpret_cast<const float4*>(src0 + static_cast<size_t>(s0 + ds) * pe) +
+                                          wc.lane + 32 * k);
+#pragma unroll
+            for (int ds = 0; ds < SC; ++ds)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                    if (s0 + ds == 0) {
+                        acc[k] = v[0][k];
+                    } else if (s0 + ds < p.W) {
+                        acc[k].x = acc[k].x + v[ds][k].x;
+                        acc[k].y = acc[k].y + v[ds][k].y;
+                        acc[k].z = acc[k].z + v[ds][k].z;
+                        acc[k].w = acc[k].w + v[ds][k].w;
+                    }
+                }
+        }
+        const size_t orow = static_cast<size_t>(mb * BM + r) * ldo;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            if (!cok[k]) continue;
+            uint2 o;
+            o.x = pack2(acc[k].x, acc[k].y, p.bf16);
+            o.y = pack2(acc[k].z, acc[k].w, p.bf16);
+            for (int rg = 0; rg < nreg; ++rg)
+                *reinterpret_cast<uint2*>(p.heap + static_cast<size_t>(rg) * p.rank_stride + dbase[k] +
+                                          (orow + dcol[k]) * 2) = o;
+        }
+    }
 }
 
 // concurrent-mode collective tile over the W heap regions
-__device__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& wc) {
+__device__ __noinline__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& wc) {
     const int tid = wc.w * 32 + wc.lane;
     constexpr int NT = NUM_WORKER_WARPS * 32;
     if (p.coll == COLL_AG) {
@@ -733,6 +889,13 @@ __device__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& wc) {
     const long long e1 = min(p.count, e0 + p.comm_block);
     const long long nv = (e1 - e0) / 4;
     const long long cw = p.count / p.W;  // reduce-scatter chunk per rank
+    int rs_rank = 0;
+    long long rs_bound = cw;             // first element past rs_rank's chunk
+    if (p.coll == COLL_RS) {
+        const long long first = e0 + static_cast<long long>(tid) * 4;
+        rs_rank = static_cast<int>(first / cw);
+        rs_bound = static_cast<long long>(rs_rank + 1) * cw;
+    }
     constexpr int U = 2;
     for (long long base = tid; base < nv; base += NT * U) {
         float4 acc[U];
@@ -760,13 +923,19 @@ __device__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& wc) {
                     if (base + u * NT < nv) dst[e0 / 4 + base + u * NT] = acc[u];
             }
         } else {
+            // elements of one thread increase monotonically, so the owning
+            // rank only ever moves forward: advance it by comparison
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (base + u * NT < nv) {
                     const long long e = e0 + (base + u * NT) * 4;
-                    const int r = static_cast<int>(e / cw);
-                    float4* dst = reinterpret_cast<float4*>(p.heap + static_cast<size_t>(r) * p.rank_stride + p.off_cout);
-                    dst[(e - r * cw) / 4] = acc[u];
+                    while (e >= rs_bound) {
+                        ++rs_rank;
+                        rs_bound += cw;
+                    }
+                    float4* dst = reinterpret_cast<float4*>(p.heap + static_cast<size_t>(rs_rank) * p.rank_stride +
+                                                            p.off_cout);
+                    dst[(e - (rs_bound - cw)) / 4] = acc[u];
                 }
         }
     }
@@ -776,10 +945,12 @@ template <int BN, int STAGES>
 __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem,
                             int warp, int lane) {
     WorkerCtx wc;
-    wc.w = warp - 2;
+    wc.w = warp - FIRST_WORKER_WARP;
     wc.lane = lane;
     wc.q = warp & 3;
-    wc.h = (warp - 2) >> 2;
+    wc.h = (warp - FIRST_WORKER_WARP) >> 2;
+    Tracer tr;
+    if (wc.w == 0 && lane == 0) tr.init(p, TR_WORK);
     wc.wphase = 0;
     uint32_t ring_n = 0, acc_i = 0;
     while (true) {
@@ -792,17 +963,20 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
         if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
         ++ring_n;
         if (item == ITEM_END) break;
+        tr.rec(EV_BEGIN, item);
         if (item & ITEM_COMM) {
             const uint32_t c = item & ~ITEM_COMM;
             if (p.op == OP_AG_MM) ok = gather_tile(p, ctl, sm, c, wc);
             else if (p.op == OP_CONC) coll_tile(p, c, wc);
             else ok = reduce_tile<BN, STAGES>(p, ctl, c, wc);
         } else {
-            ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc);
+            ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc, tr);
             ++acc_i;
         }
+        tr.rec(EV_END, item);
         if (!ok) break;
     }
+    tr.finish();
 }
 
 // ============================================================ kernel
@@ -825,7 +999,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         }
         for (int i = 0; i < RING; ++i) {
             mbar_init(&sm.item_full[i], 1);
-            mbar_init(&sm.item_empty[i], 1 + NUM_WORKER_WARPS);
+            mbar_init(&sm.item_empty[i], 2 + NUM_WORKER_WARPS);  // MMA + TMA + workers
         }
         mbar_init(sm.wbar, NUM_WORKER_WARPS);
         mbar_init(sm.final_bar, 1);
@@ -846,7 +1020,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
     const Ctl ctl{p.ws, *sm.epoch_slot, p.wait_ns};
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES>(p, ctl, sm);
+        if (lane == 0) run_scheduler<BN, STAGES>(p, ctl, sm);
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0) run_tma<BN, STAGES>(p, ctl, sm);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) run_mma<BN, STAGES>(p, ctl, sm, tmem);

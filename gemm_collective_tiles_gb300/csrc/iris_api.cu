@@ -80,6 +80,10 @@ struct Cfg {
     int tile_n, group_m, gemm_ctas, comm_block, replicate, bias_on_m, grid;
     unsigned long long wait_ns;
     uint32_t debug_skip;
+    unsigned long long* trace;
+    int trace_cap;
+    int reduce_mode;
+    int rank_inner;
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -108,6 +112,12 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     out.wait_ns = c->wait_ns ? c->wait_ns : DEFAULT_WAIT_NS;
     if (c->debug_skip_flag < 0) return IRIS_EINVAL;
     out.debug_skip = static_cast<uint32_t>(c->debug_skip_flag);
+    if (c->trace_buf && (c->trace_cap < 2 || (c->trace_buf & 7))) return IRIS_EINVAL;
+    out.trace = reinterpret_cast<unsigned long long*>(c->trace_buf);
+    out.trace_cap = c->trace_buf ? c->trace_cap : 0;
+    if (c->reduce_mode < 0 || c->reduce_mode > 1) return IRIS_EINVAL;
+    out.reduce_mode = c->reduce_mode;
+    out.rank_inner = c->rank_inner ? 1 : 0;
     return IRIS_OK;
 }
 
@@ -123,7 +133,7 @@ WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n) {
     if (op == IRIS_OP_ALL_GATHER_MATMUL)
         L.n_flags = static_cast<size_t>(W) * mb;
     else if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
-        L.n_flags = static_cast<size_t>(W) * mb * nb;
+        L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte arrival counters
     L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
     if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
         L.partial_elems = static_cast<size_t>(M) * N;
@@ -177,6 +187,10 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.bias_on_m = c.bias_on_m;
     p.wait_ns = c.wait_ns;
     p.debug_skip = c.debug_skip;
+    p.trace = c.trace;
+    p.trace_cap = c.trace_cap;
+    p.reduce_mode = c.reduce_mode;
+    p.rank_inner = c.rank_inner;
 }
 
 int launch(Params& p, const Cfg& c, cudaStream_t stream) {
@@ -339,7 +353,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     const uint64_t tiles = (M > 0 && N > 0) ? uint64_t(p.n_tiles) : 0;
     if (tiles * W >= 0x7FFFFFFFull) return IRIS_EINVAL;
     p.n_gemm = static_cast<uint32_t>(tiles * W);
-    p.n_comm = static_cast<uint32_t>(tiles);
+    p.n_comm = c.reduce_mode == 1 ? static_cast<uint32_t>(tiles) : 0u;
     if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;

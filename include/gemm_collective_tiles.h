@@ -110,6 +110,19 @@ typedef struct {
                               release ready-flag k-1, so the tile waiting on it
                               runs into its bounded wait (IRIS_ETIMEOUT from
                               query_status).  Never set it in production. */
+    unsigned long long trace_buf; /* optional device buffer (as an address) for a
+                              per-CTA timeline: 4 streams per CTA (scheduler, MMA,
+                              TMA, workers) of trace_cap (event, ns) u64 pairs,
+                              pair 0 holding the count; 0 = off */
+    int trace_cap;         /* pairs per stream (>= 2 when trace_buf is set) */
+    int reduce_mode;       /* matmul_reduce_scatter / matmul_all_reduce: 0 = the rank
+                              whose partial completes an output tile reduces it right
+                              away (epoch-tagged arrival counter per tile; default);
+                              1 = reduce tiles go through the comm queue and wait on
+                              per-partial ready-flags (the gemm_ctas split applies) */
+    int rank_inner;        /* reduce ops: 1 = order GEMM tiles with the rank index
+                              fastest; 0 (default) = rank by rank inside each GROUP_M
+                              group, so one rank's operands share the L2 at a time */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

@@ -135,12 +135,14 @@ def test_ag_mm_bias_on_m_random():
 # ------------------------------------------------------------------ reduce ops
 
 @pytest.mark.parametrize("W,M,N,K,dt", [(4, 256, 512, 128, "f16"), (4, 200, 160, 72, "bf16"),
-                                         (2, 128, 256, 64, "f16"), (8, 384, 1024, 256, "bf16")])
+                                         (2, 128, 256, 64, "f16"), (8, 384, 1024, 256, "bf16"),
+                                         (1, 136, 264, 64, "bf16")])
 @pytest.mark.parametrize("exact", [True, False])
-def test_mm_reduce_scatter(W, M, N, K, dt, exact):
+@pytest.mark.parametrize("reduce_mode", [0, 1])
+def test_mm_reduce_scatter(W, M, N, K, dt, exact, reduce_mode):
     kw = dict(dist="int", scale=2, bias_scale=3) if exact else dict(dist="uniform", scale=1.0)
     x = synthetic.make_fused_inputs("mm_rs", W, M, N, K, dt, seed=31 + W + M, bias=True, **kw)
-    prob, outs = run_fused(x)
+    prob, outs = run_fused(x, config={"reduce_mode": reduce_mode})
     want = oracle.matmul_reduce_scatter(x.A, x.B, x.bias)
     for r in range(W):
         if exact:
@@ -151,10 +153,11 @@ def test_mm_reduce_scatter(W, M, N, K, dt, exact):
 
 @pytest.mark.parametrize("W,M,N,K,dt", [(8, 256, 256, 128, "bf16"), (3, 200, 136, 72, "f16")])
 @pytest.mark.parametrize("replicate", [0, 1])
-def test_mm_all_reduce_exact_integer(W, M, N, K, dt, replicate):
+@pytest.mark.parametrize("reduce_mode", [0, 1])
+def test_mm_all_reduce_exact_integer(W, M, N, K, dt, replicate, reduce_mode):
     x = synthetic.make_fused_inputs("mm_ar", W, M, N, K, dt, seed=41 + W, dist="int", scale=2,
                                     bias=True, bias_scale=3)
-    prob, outs = run_fused(x, config={"replicate_outputs": replicate})
+    prob, outs = run_fused(x, config={"replicate_outputs": replicate, "reduce_mode": reduce_mode})
     want = oracle.matmul_all_reduce(x.A, x.B, x.bias)
     assert_exact(bits(outs["out"][0]), want)
     if replicate:
@@ -274,7 +277,9 @@ def test_workspace_reuse_and_schedule_invariance(op):
             ref = cur
         for a, b in zip(ref, cur):
             assert_exact(a, b)
-    for cfg in ({"gemm_ctas": 20}, {"grid": 7}, {"group_m": 1}, {"tile_n": 128}, {"gemm_ctas": -1}):
+    for cfg in ({"gemm_ctas": 20}, {"grid": 7}, {"group_m": 1}, {"tile_n": 128}, {"gemm_ctas": -1},
+                {"reduce_mode": 1}, {"reduce_mode": 1, "gemm_ctas": 30}, {"rank_inner": 1},
+                {"rank_inner": 1, "reduce_mode": 1}, {"group_m": 3, "reduce_mode": 1}):
         p2 = FusedProblem(op, W, M, N, K, "bf16", bias=True, config=cfg)
         p2.upload(x.A, x.B, x.bias)
         p2.poison_outputs()
@@ -298,7 +303,9 @@ def test_missing_flag_times_out_and_context_survives(op, skip):
     from gemm_collective_tiles_gb300 import query_status, _native
     W, M, N, K = 4, 256, 512, 256
     x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=81, dist="int", scale=2)
-    bad = FusedProblem(op, W, M, N, K, "bf16", config={"debug_skip_flag": skip, "wait_ns": 50_000_000})
+    # the reduce op's flag waits belong to its comm-queue schedule
+    bad = FusedProblem(op, W, M, N, K, "bf16", config={"debug_skip_flag": skip, "wait_ns": 50_000_000,
+                                                       "reduce_mode": 1 if op == "mm_rs" else 0})
     bad.upload(x.A, x.B, x.bias)
     bad.run()
     rc, status, where, index = query_status(bad.ws)
