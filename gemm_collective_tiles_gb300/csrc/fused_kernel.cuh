@@ -4,7 +4,7 @@
 // swizzle, explicit GEMM/comm CTA split; iris docs "Fused Communication and
 // Compute Operations" for the four dependent ops).
 //
-// CTA layout (352 threads, one CTA per SM):
+// CTA layout (224 threads, one CTA per SM):
 //   warp 0      scheduler (lane 0): claims work items from the two global
 //               queues with atomics and publishes them into a small
 //               shared-memory item ring, ahead of the warps that run them.
@@ -12,7 +12,8 @@
 //               steps, fp32 accumulators in TMEM, double-buffered).
 //   warp 2      TMA producer (lane 0): for GEMM items streams the A/B K-blocks
 //               into a STAGES-deep shared-memory pipeline.
-//   warps 3..10 workers: GEMM epilogue (tcgen05.ld -> +bias -> fp16/bf16 or
+//   warps 3..6  workers, one per tensor-memory lane quadrant: GEMM epilogue
+//               (tcgen05.ld -> +bias -> fp16/bf16 or
 //               fp32 partial -> global) and comm tiles (128-bit vector copy /
 //               rank-order fp32 reduce), so the comm tiles of one SM run
 //               while its tensor cores work on the next GEMM tile.
@@ -33,7 +34,7 @@ enum : int { COLL_AG = 0, COLL_AR = 1, COLL_RS = 2 };
 constexpr int BM = 128;           // tile rows (tcgen05 M for cta_group::1)
 constexpr int BK = 64;            // K per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int NUM_WORKER_WARPS = 8;
+constexpr int NUM_WORKER_WARPS = 4;  // one per tensor-memory lane quadrant (or a multiple of 4)
 constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
 constexpr int NUM_THREADS = 32 * (FIRST_WORKER_WARP + NUM_WORKER_WARPS);
 constexpr int RING = 8;           // work-item ring depth
@@ -56,6 +57,9 @@ enum : int {
     WAIT_TEARDOWN_TMA = 11,
     WAIT_TEARDOWN_MMA = 12,
     WAIT_ITEM_FULL_TMA = 13,
+    WAIT_REDUCE_PARTS = 14,
+    WAIT_CHAIN = 15,
+    WAIT_CHAIN_LOAD = 16,
 };
 
 // First 256 bytes of the workspace.
@@ -68,18 +72,23 @@ struct WsHeader {
     uint32_t abort_epoch;  // == current epoch while the launch is aborting
     int err_where;
     int err_index;
-    uint32_t pad[56];
+    uint32_t part_ctr;     // next reduce part to claim (distributed reduce schedule)
+    uint32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 struct Params {
     CUtensorMap tmA;  // 3-D {k, row, rank}, box {64, 128, 1}, 128-byte swizzle
     CUtensorMap tmB;  // 3-D {n, k, rank},   box {64, 64, 1},  128-byte swizzle
+    CUtensorMap tmC;  // 4-D {n, row, row block, region} output, box {32, 32, 1, 1}:
+                      // fp32 partials (128-byte swizzle) or 16-bit outputs (64-byte swizzle)
+    CUtensorMap tmS;  // chained reduce: the fp32 running-sum tile buffer, box {32, 32, 1, 1}
     int op, W, bf16, coll;
     int M;            // rows of one GEMM (M_local for matmul_all_gather)
     int N, K;
     int m_blocks, mb_per_rank, n_blocks, k_blocks, group_m, n_tiles;
     uint32_t n_gemm, n_comm;
+    uint32_t n_parts;    // reduce ops, distributed parts schedule: output tiles x W row parts
     int gemm_ctas;    // CTAs preferring GEMM; < 0 = balanced
     uint32_t lookahead;
     char* heap;
@@ -97,7 +106,7 @@ struct Params {
     int elem_bytes;
     unsigned long long wait_ns;
     uint32_t debug_skip;               // flag index + 1 that is never released (0 = none)
-    int reduce_mode;                   // reduce ops: 0 = last arriving rank reduces, 1 = comm queue
+    int reduce_mode;                   // reduce ops: 1 = comm queue, 2 = distributed parts, 3 = chained
     int rank_inner;                    // reduce ops: 1 = rank index fastest in the GEMM item order
     unsigned long long* trace;         // optional per-CTA event trace (nullptr = off)
     int trace_cap;                     // events per (CTA, role)
@@ -299,11 +308,14 @@ struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2;
-    static constexpr uint32_t BYTES = 1024 /*align slack*/ + TILES_BYTES + NUM_BARS * 8 +
-                                      (RING + 4) * 4;
+    static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + 2 * NUM_WORKER_WARPS;
+    static constexpr uint32_t BYTES = 1024 /*align slack*/ + TILES_BYTES +
+                                      NUM_WORKER_WARPS * STAGE_OUT_BYTES + NUM_BARS * 8 + (RING + 4) * 4;
     uint8_t* tiles;
+    uint8_t* stage_out;
     uint64_t *full, *empty, *acc_full, *acc_empty, *item_full, *item_empty, *wbar, *final_bar;
+    uint64_t* sbar;  // per worker warp: 2 barriers for running-sum chunk loads
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
@@ -313,7 +325,8 @@ struct Smem {
         uintptr_t a = reinterpret_cast<uintptr_t>(raw);
         a = (a + 1023) & ~static_cast<uintptr_t>(1023);
         tiles = reinterpret_cast<uint8_t*>(a);
-        uint64_t* b = reinterpret_cast<uint64_t*>(tiles + TILES_BYTES);
+        stage_out = tiles + TILES_BYTES;  // 1024-aligned: TILES_BYTES is a multiple of 1024
+        uint64_t* b = reinterpret_cast<uint64_t*>(stage_out + NUM_WORKER_WARPS * STAGE_OUT_BYTES);
         full = b;
         empty = full + STAGES;
         acc_full = empty + STAGES;
@@ -322,11 +335,13 @@ struct Smem {
         item_empty = item_full + RING;
         wbar = item_empty + RING;
         final_bar = wbar + 1;
-        uint32_t* u = reinterpret_cast<uint32_t*>(final_bar + 1);
+        sbar = final_bar + 1;
+        uint32_t* u = reinterpret_cast<uint32_t*>(sbar + 2 * NUM_WORKER_WARPS);
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
         bcast = u + RING + 2;
+
     }
     __device__ uint8_t* a_tile(uint32_t s) const { return tiles + s * STAGE_BYTES; }
     __device__ uint8_t* b_tile(uint32_t s) const { return tiles + s * STAGE_BYTES + A_BYTES; }
@@ -579,17 +594,175 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
 
 // ============================================================ workers
 struct WorkerCtx {
-    int w;      // worker warp 0..7
+    int w;      // worker warp index
     int lane;
     int q;      // TMEM lane quarter of this warp (warp id % 4)
-    int h;      // column half of the accumulator this warp drains
+    int h;      // column slice of the accumulator this warp drains
     uint32_t wphase;
+    uint32_t sphase;  // parity bits of this warp's two running-sum load barriers
 };
 
 template <int BN, int STAGES>
 __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx& wc);
 
-// barrier over the 8 worker warps built on an mbarrier (bounded, abortable)
+// Distributed reduce (reduce ops, reduce_mode 2).  Output tile t is cut into W
+// row parts (part s = rows [s*rows/W, (s+1)*rows/W)); part i = t*W + s sits in
+// one global queue.  A worker warp with nothing else to do takes the next part
+// (fetch-and-add), and reduces its rows one at a time once tile t's arrival
+// counter shows all W partials; until then it keeps doing its own GEMM work.
+// No warp ever waits on work that another warp holds, and the reduce spreads
+// over every SM with idle workers.
+struct PartState {
+    uint32_t cur;   // claimed part, or NO_PART
+    int row;        // next row of it
+    bool ready;     // its tile has all W partials
+};
+constexpr uint32_t NO_PART = 0xFFFFFFFFu;
+
+// Output row r (inside tile mb, nb) of the rank-order reduce: the loads of
+// up to SC ranks are issued before their adds.
+template <int BN>
+__device__ __forceinline__ void reduce_row(const Params& p, int mb, int nb, int r, int rows, WorkerCtx& wc) {
+    constexpr int CPL = BN / 4 / 32;
+    constexpr int SC = 4;
+    constexpr int RU = 1;
+    const int cols = min(BN, p.N - nb * BN);
+    const size_t pe = p.partial_elems;
+    const float* src0 = p.partials + static_cast<size_t>(mb * BM + r) * p.N + nb * BN;
+    float4 acc[RU][CPL];
+    for (int s0 = 0; s0 < p.W; s0 += SC) {
+        float4 v[SC][RU][CPL];
+#pragma unroll
+        for (int ds = 0; ds < SC; ++ds)
+#pragma unroll
+            for (int u = 0; u < RU; ++u)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+                    if (s0 + ds < p.W && r + u * NUM_WORKER_WARPS < rows && (wc.lane + 32 * k) * 4 < cols)
+                        v[ds][u][k] = __ldcg(reinterpret_cast<const float4*>(
+                                                 src0 + static_cast<size_t>(s0 + ds) * pe +
+                                                 static_cast<size_t>(u * NUM_WORKER_WARPS) * p.N) +
+                                             wc.lane + 32 * k);
+#pragma unroll
+        for (int ds = 0; ds < SC; ++ds)
+#pragma unroll
+            for (int u = 0; u < RU; ++u)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                    if (s0 + ds == 0) {
+                        acc[u][k] = v[0][u][k];
+                    } else if (s0 + ds < p.W) {
+                        acc[u][k].x = acc[u][k].x + v[ds][u][k].x;
+                        acc[u][k].y = acc[u][k].y + v[ds][u][k].y;
+                        acc[u][k].z = acc[u][k].z + v[ds][u][k].z;
+                        acc[u][k].w = acc[u][k].w + v[ds][u][k].w;
+                    }
+                }
+    }
+    const int nreg = (p.op == OP_MM_AR && p.replicate) ? p.W : 1;
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+        const int rr_row = r + u * NUM_WORKER_WARPS;
+        if (rr_row >= rows) continue;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int c4 = wc.lane + 32 * k;
+            if (c4 * 4 >= cols) continue;
+            const int j = nb * BN + c4 * 4;
+            size_t off;
+            if (p.op == OP_MM_RS) {
+                const int rr = j / p.N_local;
+                off = static_cast<size_t>(rr) * p.rank_stride + p.off_out +
+                      (static_cast<size_t>(mb * BM + rr_row) * p.N_local + (j - rr * p.N_local)) * 2;
+            } else {
+                off = p.off_out + (static_cast<size_t>(mb * BM + rr_row) * p.N + j) * 2;
+            }
+            uint2 o;
+            o.x = pack2(acc[u][k].x, acc[u][k].y, p.bf16);
+            o.y = pack2(acc[u][k].z, acc[u][k].w, p.bf16);
+            for (int rg = 0; rg < nreg; ++rg)
+                *reinterpret_cast<uint2*>(p.heap + static_cast<size_t>(rg) * p.rank_stride + off) = o;
+        }
+    }
+}
+
+__device__ __forceinline__ bool tile_ready(const Params& p, uint32_t epoch, uint32_t t) {
+    const unsigned long long v =
+        *reinterpret_cast<volatile unsigned long long*>(reinterpret_cast<unsigned long long*>(p.flags) + t);
+    return v == ((static_cast<unsigned long long>(epoch) << 32) | static_cast<uint32_t>(p.W));
+}
+
+// One row of reduce work for this warp: continue the claimed part, or claim
+// the head part if its tile is complete.  false = nothing to do right now.
+template <int BN>
+__device__ __noinline__ bool part_step(const Params& p, uint32_t epoch, PartState& ps, WorkerCtx& wc) {
+    if (p.n_parts == 0) return false;
+    if (ps.cur == NO_PART) {
+        uint32_t got = NO_PART;
+        if (wc.lane == 0 && ld_relaxed_gpu(&p.ws->part_ctr) < p.n_parts) {
+            const uint32_t i = atomicAdd(&p.ws->part_ctr, 1u);
+            if (i < p.n_parts) got = i;
+        }
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (got == NO_PART) return false;
+        ps.cur = got;
+        ps.row = 0;
+        ps.ready = false;
+    }
+    if (!ps.ready) {
+        int rdy = 0;
+        if (wc.lane == 0) rdy = tile_ready(p, epoch, ps.cur / p.W) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, rdy, 0)) return false;
+        __threadfence();  // acquire side of the arrival-counter protocol
+        ps.ready = true;
+    }
+    const uint32_t t = ps.cur / p.W;
+    const int part = static_cast<int>(ps.cur % p.W);
+    int mb, nb;
+    swizzle_tile(p, t, mb, nb);
+    const int rows = min(BM, p.M - mb * BM);
+    const int lo = part * rows / p.W, hi = (part + 1) * rows / p.W;
+    if (lo + ps.row < hi) reduce_row<BN>(p, mb, nb, lo + ps.row, hi, wc);
+    ps.row += 1;
+    if (lo + ps.row >= hi) ps.cur = NO_PART;
+    return true;
+}
+
+// true once every part has been claimed and this warp holds none
+__device__ __forceinline__ bool parts_done(const Params& p, const PartState& ps) {
+    return ps.cur == NO_PART && ld_relaxed_gpu(&p.ws->part_ctr) >= p.n_parts;
+}
+
+// Bounded wait on an mbarrier phase that does reduce rows while the phase is
+// not complete (warp-uniform: lane 0 polls).
+template <int BN>
+__device__ bool wait_bar_working(const Params& p, const Ctl& c, uint64_t* bar, uint32_t parity, int where,
+                                 PartState& ps, WorkerCtx& wc) {
+    uint64_t t0 = 0;
+    bool timing = false;
+    for (uint32_t i = 0;; ++i) {
+        int ready = 0;
+        if (wc.lane == 0) ready = mbar_try_wait(bar, parity) ? 1 : 0;
+        if (__shfl_sync(0xFFFFFFFFu, ready, 0)) return true;
+        if (part_step<BN>(p, c.epoch, ps, wc)) {
+            timing = false;  // progress: restart the idle clock
+            continue;
+        }
+        if (!timing) {
+            t0 = global_timer_ns();
+            timing = true;
+        }
+        if ((i & 15) == 0) {
+            if (launch_aborted(c)) return false;
+            if (global_timer_ns() - t0 > c.limit) {
+                if (wc.lane == 0) raise_timeout(c, where, -1);
+                return false;
+            }
+        }
+    }
+}
+
+// barrier over the worker warps built on an mbarrier (bounded, abortable)
 template <int BN, int STAGES>
 __device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES>& sm, WorkerCtx& wc) {
     __syncwarp();
@@ -605,11 +778,9 @@ __device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES>& sm
 // GEMM epilogue of one tile: TMEM -> registers -> (+bias) -> global.
 template <int BN, int STAGES>
 __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem,
-                         uint32_t g, uint32_t acc_i, WorkerCtx& wc, Tracer& tr) {
+                         uint32_t g, uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
-    bool ok = true;
-    if (wc.lane == 0) ok = wait_bar(ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL);
-    if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return false;
+    if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
     tr.rec(EV_READY, g);
 
@@ -639,9 +810,28 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     if (p.has_bias && p.bias_on_m && row_ok)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[bias_row], p.bf16);
 
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * (BN / 2);
+    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;  // accumulator columns this warp drains
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
+    // Each 32 x 32 chunk (the warp's 32 rows, one per lane) goes registers ->
+    // swizzled shared-memory staging -> TMA tensor store, so global memory
+    // sees whole 128-byte lines instead of 16-byte pieces of 32 rows.
+    uint8_t* stg = sm.stage_out + wc.w * Smem<BN, STAGES>::STAGE_OUT_BYTES;
+    // TMA coordinates of the warp's 32-row slab
+    int c_row, c_blk, c_reg_lo = 0, c_reg_hi = 1;
+    if (reduce_op) {
+        c_row = gc.mb * BM + wc.q * 32;
+        c_blk = gc.rank;
+    } else if (p.op == OP_MM_AG) {
+        c_row = (gc.mb % p.mb_per_rank) * BM + wc.q * 32;
+        c_blk = gc.rank;
+        if (p.replicate) c_reg_hi = p.W;
+    } else {
+        c_row = gc.mb * BM + wc.q * 32;
+        c_blk = 0;
+        if (p.replicate && p.op == OP_AG_MM) c_reg_hi = p.W;
+    }
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 2; cc += 32) {
+    for (int cc = 0; cc < COLS; cc += 32) {
         uint32_t r[32];
         if (p.k_blocks > 0) {
             tmem_ld_32x32b_x32(tbase + cc, r);
@@ -650,12 +840,13 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        const int col0 = gc.nb * BN + wc.h * (BN / 2) + cc;
-        if (!row_ok) continue;
+        const int col0 = gc.nb * BN + wc.h * COLS + cc;
+        if (col0 >= p.N) continue;  // whole chunk right of the matrix (warp-uniform)
+        // the previous chunk's store must have read the staging buffer
+        if (wc.lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int col = col0 + v * 8;
-            if (col >= p.N) break;
+        for (int v = 0; v < 4; ++v) {  // 8 columns at a time: +bias, then into the staging row
             float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(r[v * 8 + i]);
@@ -663,8 +854,8 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
                 if (p.bias_on_m) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = x[i] + row_bias;
-                } else {
-                    const uint4 bb = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(col) * 2);
+                } else if (col0 + v * 8 < p.N) {
+                    const uint4 bb = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(col0 + v * 8) * 2);
                     const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -674,26 +865,27 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
                 }
             }
             if (reduce_op) {
-                float* dst = p.partials + static_cast<size_t>(gc.rank) * p.partial_elems +
-                             static_cast<size_t>(row) * p.N + col;
-                reinterpret_cast<float4*>(dst)[0] = make_float4(x[0], x[1], x[2], x[3]);
-                reinterpret_cast<float4*>(dst)[1] = make_float4(x[4], x[5], x[6], x[7]);
+                // fp32 row = 8 chunks of 16 B; chunk index XOR (row % 8) (128-byte swizzle)
+                const int c0 = 2 * v, c1 = 2 * v + 1;
+                *reinterpret_cast<float4*>(stg + wc.lane * 128 + ((c0 ^ (wc.lane & 7)) << 4)) =
+                    make_float4(x[0], x[1], x[2], x[3]);
+                *reinterpret_cast<float4*>(stg + wc.lane * 128 + ((c1 ^ (wc.lane & 7)) << 4)) =
+                    make_float4(x[4], x[5], x[6], x[7]);
             } else {
+                // 16-bit row = 4 chunks of 16 B; chunk index XOR ((row / 2) % 4) (64-byte swizzle)
                 uint4 o;
                 o.x = pack2(x[0], x[1], p.bf16);
                 o.y = pack2(x[2], x[3], p.bf16);
                 o.z = pack2(x[4], x[5], p.bf16);
                 o.w = pack2(x[6], x[7], p.bf16);
-                if (p.op == OP_CONC) {
-                    *reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.C) +
-                                              (static_cast<size_t>(row) * p.N + col) * 2) = o;
-                } else {
-                    const size_t off = p.off_out + (static_cast<size_t>(row) * p.N + col) * 2;
-                    const int nreg = p.replicate ? p.W : 1;
-                    for (int rg = 0; rg < nreg; ++rg)
-                        *reinterpret_cast<uint4*>(p.heap + static_cast<size_t>(rg) * p.rank_stride + off) = o;
-                }
+                *reinterpret_cast<uint4*>(stg + wc.lane * 64 + ((v ^ ((wc.lane >> 1) & 3)) << 4)) = o;
             }
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (wc.lane == 0) {
+            for (int rg = c_reg_lo; rg < c_reg_hi; ++rg) tma_store_4d(&p.tmC, stg, col0, c_row, c_blk, rg);
+            bulk_commit();
         }
     }
     tc_fence_before();
@@ -701,28 +893,196 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     if (wc.lane == 0) mbar_arrive(&sm.acc_empty[buf]);
 
     if (reduce_op) {
-        // publish this rank's partial tile: all 8 warps' stores, then the flag
+        // publish this rank's partial tile: all worker warps' stores complete and
+        // visible to generic-proxy readers, then the flag / arrival
+        if (wc.lane == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+        }
+        __syncwarp();
         __threadfence();
         if (!worker_sync(ctl, sm, wc)) return false;
-        if (p.reduce_mode == 0) {
-            // the rank whose partial completes the tile reduces it now, while
-            // the other partials are still in L2
-            if (wc.w == 0 && wc.lane == 0) {
-                uint32_t last = 0;
-                if (p.debug_skip != g + 1)
-                    last = arrive_count(reinterpret_cast<unsigned long long*>(p.flags) + gc.tile, ctl.epoch) ==
-                           static_cast<uint32_t>(p.W);
+        if (p.reduce_mode == 2) {
+            // count this partial in; the tile's reduce parts become claimable
+            // once all W are in
+            if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1) {
                 __threadfence();
-                *sm.bcast = last;
-            }
-            if (!worker_sync(ctl, sm, wc)) return false;
-            if (*reinterpret_cast<volatile uint32_t*>(sm.bcast)) {
-                __threadfence();
-                reduce_body<BN, STAGES>(p, gc.tile, wc);
+                arrive_count(reinterpret_cast<unsigned long long*>(p.flags) + gc.tile, ctl.epoch);
             }
         } else if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1) {
             st_release_gpu(&p.flags[g], ctl.epoch);
         }
+    }
+    return true;
+}
+
+// Bounded wait for a 64-bit counter to hold `want` (acquire).
+__device__ __forceinline__ bool wait_count(const Ctl& c, const unsigned long long* ctr, unsigned long long want,
+                                           int where, int index) {
+    if (ld_acquire_gpu_u64(ctr) == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu_u64(ctr) == want) return true;
+        if ((i & 7) == 0) {
+            if (launch_aborted(c)) return false;
+            if (global_timer_ns() - t0 > c.limit) {
+                raise_timeout(c, where, index);
+                return false;
+            }
+        }
+    }
+}
+
+// Chained reduce epilogue (reduce ops, reduce_mode 3): rank s of output tile t
+// waits until ranks 0..s-1 have folded their partials into the fp32 running
+// sum S[t] (tile counter = s), loads S[t] chunk by chunk with TMA, adds its own
+// partial (acc + bias_s) -- so S = ((P_0 + P_1) + P_2) + ... in rank order --
+// and stores S[t] back (s < W-1) or rounds it to the 16-bit output (s = W-1),
+// then advances the counter.  This is a ring reduce-scatter/all-reduce done
+// per tile inside the GEMM epilogues; each wait is on a GEMM item with a
+// smaller index, which was claimed earlier and never waits on this one.
+template <int BN, int STAGES>
+__device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem, uint32_t g,
+                               uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
+    const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
+    if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
+    tc_fence_after();
+    tr.rec(EV_READY, g);
+    const GemmCoord gc = decode_gemm(p, g);
+    const int s = gc.rank;
+    const bool last = (s == p.W - 1);
+    const int row = gc.mb * BM + wc.q * 32 + wc.lane;
+    const char* bias_base =
+        p.has_bias ? p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_bias : nullptr;
+    float row_bias = 0.f;
+    if (p.has_bias && p.bias_on_m && row < p.M)
+        row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
+    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.flags) + gc.tile;
+    const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
+    if (s > 0) {
+        int ok = 1;
+        if (wc.lane == 0) ok = wait_count(ctl, ctr, tag | static_cast<uint32_t>(s), WAIT_CHAIN, static_cast<int>(g));
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+        if (wc.lane == 0) fence_proxy_async_global();  // S[t] was written by the TMA of another SM
+    }
+    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
+    constexpr int NCH = COLS / 32;
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
+    uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES>::STAGE_OUT_BYTES;
+    uint64_t* lbar = sm.sbar + 2 * wc.w;
+    const int c_row = gc.mb * BM + wc.q * 32;
+    const int colbase = gc.nb * BN + wc.h * COLS;
+    // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
+    const int nch = max(0, min(NCH, (p.N - colbase) / 32));
+    auto issue_load = [&](int ci) {
+        // the staging half must be free: earlier stores have read it
+        bulk_wait_read_all();
+        mbar_arrive_expect_tx(&lbar[ci & 1], 32 * 32 * 4);
+        tma_load_4d(stg_base + (ci & 1) * 4096, &p.tmS, colbase + ci * 32, c_row, 0, 0, &lbar[ci & 1]);
+    };
+    if (s > 0 && nch > 0 && wc.lane == 0) issue_load(0);
+#pragma unroll 1
+    for (int ci = 0; ci < nch; ++ci) {
+        uint8_t* stg = stg_base + (ci & 1) * 4096;
+        uint32_t r[32];
+        if (p.k_blocks > 0) {
+            tmem_ld_32x32b_x32(tbase + ci * 32, r);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        const int col0 = colbase + ci * 32;
+        if (s > 0 && ci + 1 < nch && wc.lane == 0) issue_load(ci + 1);
+        // P_s = acc + bias_s (fp32)
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+        if (p.has_bias) {
+            if (p.bias_on_m) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = x[i] + row_bias;
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 bb = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(col0 + v * 8) * 2);
+                    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[v * 8 + 2 * i] = x[v * 8 + 2 * i] + bits16_to_float(bw[i] & 0xFFFFu, p.bf16);
+                        x[v * 8 + 2 * i + 1] = x[v * 8 + 2 * i + 1] + bits16_to_float(bw[i] >> 16, p.bf16);
+                    }
+                }
+            }
+        }
+        if (s > 0) {
+            // S_new = S_old + P_s (S_old holds ranks 0..s-1 in order)
+            int ok = 1;
+            if (wc.lane == 0) {
+                const uint32_t par = (wc.sphase >> (ci & 1)) & 1u;
+                ok = wait_bar(ctl, &lbar[ci & 1], par, WAIT_CHAIN_LOAD) ? 1 : 0;
+            }
+            wc.sphase ^= 1u << (ci & 1);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 o = *reinterpret_cast<const float4*>(stg + wc.lane * 128 + ((c ^ (wc.lane & 7)) << 4));
+                x[4 * c + 0] = o.x + x[4 * c + 0];
+                x[4 * c + 1] = o.y + x[4 * c + 1];
+                x[4 * c + 2] = o.z + x[4 * c + 2];
+                x[4 * c + 3] = o.w + x[4 * c + 3];
+            }
+            __syncwarp();  // every lane has read its row before the buffer is rewritten
+        } else {
+            if (wc.lane == 0) bulk_wait_read_all();
+            __syncwarp();
+        }
+        if (!last) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(stg + wc.lane * 128 + ((c ^ (wc.lane & 7)) << 4)) =
+                    make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                uint4 o;
+                o.x = pack2(x[8 * v + 0], x[8 * v + 1], p.bf16);
+                o.y = pack2(x[8 * v + 2], x[8 * v + 3], p.bf16);
+                o.z = pack2(x[8 * v + 4], x[8 * v + 5], p.bf16);
+                o.w = pack2(x[8 * v + 6], x[8 * v + 7], p.bf16);
+                *reinterpret_cast<uint4*>(stg + wc.lane * 64 + ((v ^ ((wc.lane >> 1) & 3)) << 4)) = o;
+            }
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (wc.lane == 0) {
+            if (!last) {
+                tma_store_4d(&p.tmS, stg, col0, c_row, 0, 0);
+            } else if (p.op == OP_MM_RS) {
+                const int rr = col0 / p.N_local;
+                tma_store_4d(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0);
+            } else {
+                const int nreg = p.replicate ? p.W : 1;
+                for (int rg = 0; rg < nreg; ++rg) tma_store_4d(&p.tmC, stg, col0, c_row, 0, rg);
+            }
+            bulk_commit();
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (wc.lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+    if (!last) {
+        // S[t] complete and visible, then hand the tile to rank s+1
+        if (wc.lane == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+        }
+        __syncwarp();
+        __threadfence();
+        if (!worker_sync(ctl, sm, wc)) return false;
+        if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1)
+            st_release_gpu_u64(ctr, tag | static_cast<uint32_t>(s + 1));
     }
     return true;
 }
@@ -869,7 +1229,7 @@ __device__ __noinline__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& w
         const long long nv = (min(bytes_per_rank, b0 + chunk_bytes) - b0) / 16;
         const uint4* src = reinterpret_cast<const uint4*>(p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_in + b0);
         const size_t dst_off = p.off_cout + static_cast<size_t>(s) * bytes_per_rank + b0;
-        constexpr int U = 4;
+        constexpr int U = 8;
         for (long long base = tid; base < nv; base += NT * U) {
             uint4 v[U];
 #pragma unroll
@@ -952,12 +1312,17 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
     Tracer tr;
     if (wc.w == 0 && lane == 0) tr.init(p, TR_WORK);
     wc.wphase = 0;
+    wc.sphase = 0;
+    PartState ps;
+    ps.cur = NO_PART;
+    ps.row = 0;
+    ps.ready = false;
     uint32_t ring_n = 0, acc_i = 0;
+    bool ok = true;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
-        bool ok = true;
-        if (lane == 0) ok = wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_WORKER);
-        if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+        ok = wait_bar_working<BN>(p, ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_WORKER, ps, wc);
+        if (!ok) break;
         const uint32_t item = sm.ring[slot];
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
@@ -970,13 +1335,44 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
             else if (p.op == OP_CONC) coll_tile(p, c, wc);
             else ok = reduce_tile<BN, STAGES>(p, ctl, c, wc);
         } else {
-            ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc, tr);
+            if (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR))
+                ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
+            else
+                ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
             ++acc_i;
         }
         tr.rec(EV_END, item);
         if (!ok) break;
     }
+    // help with the reduce parts left: their tiles' GEMM items are all
+    // claimed and run without waiting on parts, so they complete (bounded)
+    if (ok && p.n_parts > 0) {
+        uint64_t t0 = 0;
+        bool timing = false;
+        for (uint32_t i = 0; !parts_done(p, ps); ++i) {
+            if (part_step<BN>(p, ctl.epoch, ps, wc)) {
+                timing = false;
+                continue;
+            }
+            if (!timing) {
+                t0 = global_timer_ns();
+                timing = true;
+            }
+            __nanosleep(128);
+            if ((i & 15) == 0) {
+                if (launch_aborted(ctl)) break;
+                if (global_timer_ns() - t0 > ctl.limit) {
+                    if (lane == 0) raise_timeout(ctl, WAIT_REDUCE_PARTS, -1);
+                    break;
+                }
+            }
+        }
+    }
+    tr.rec(EV_END, 0x7FFFFFFEu);  // workers done (after the reduce parts)
     tr.finish();
+    // the staging buffer must outlive every store that reads it
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
 }
 
 // ============================================================ kernel
@@ -1003,6 +1399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         }
         mbar_init(sm.wbar, NUM_WORKER_WARPS);
         mbar_init(sm.final_bar, 1);
+        for (int i = 0; i < 2 * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
         fence_mbar_init();
         uint32_t e = *reinterpret_cast<volatile uint32_t*>(&p.ws->epoch) + 1u;
         if (e == 0u) e = 1u;
@@ -1011,6 +1408,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
             tma_prefetch_desc(&p.tmA);
             tma_prefetch_desc(&p.tmB);
         }
+        if (p.n_gemm > 0) tma_prefetch_desc(&p.tmC);
+        if (p.n_gemm > 0 && p.reduce_mode == 3) tma_prefetch_desc(&p.tmS);
     }
     if (warp == 1) tmem_alloc<TMEM_COLS>(sm.tmem_slot);
     tc_fence_before();
@@ -1046,6 +1445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
             // this workspace and publish the epoch
             atomicExch(&p.ws->gemm_ctr, 0u);
             atomicExch(&p.ws->comm_ctr, 0u);
+            atomicExch(&p.ws->part_ctr, 0u);
             atomicExch(&p.ws->done_ctr, 0u);
             __threadfence();
             atomicExch(&p.ws->epoch, ctl.epoch);

@@ -6,6 +6,8 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -28,6 +30,20 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
+
+// IRIS_B200_DEBUG=1 in the environment prints the failing step of an
+// IRIS_ECUDA return to stderr.
+bool debug_on() {
+    static const bool on = [] {
+        const char* e = std::getenv("IRIS_B200_DEBUG");
+        return e && e[0] && e[0] != '0';
+    }();
+    return on;
+}
+int cuda_fail(const char* what, int code) {
+    if (debug_on()) std::fprintf(stderr, "[iris_b200] %s failed: %d\n", what, code);
+    return IRIS_ECUDA;
+}
 bool g_attr_done[64] = {false};
 
 EncodeTiledFn encoder() {
@@ -53,14 +69,14 @@ int ensure_attrs(int dev) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (dev < 0 || dev >= 64) return IRIS_ECUDA;
     if (g_attr_done[dev]) return IRIS_OK;
-    if (cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>,
+    cudaError_t e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<BN_WIDE, STAGES_WIDE>()));
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_n 256)", static_cast<int>(e));
+    e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN_WIDE, STAGES_WIDE>())) != cudaSuccess)
-        return IRIS_ECUDA;
-    if (cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN_NARROW, STAGES_NARROW>())) != cudaSuccess)
-        return IRIS_ECUDA;
+                             static_cast<int>(smem_bytes<BN_NARROW, STAGES_NARROW>()));
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_n 128)", static_cast<int>(e));
     g_attr_done[dev] = true;
     return IRIS_OK;
 }
@@ -82,7 +98,7 @@ struct Cfg {
     uint32_t debug_skip;
     unsigned long long* trace;
     int trace_cap;
-    int reduce_mode;
+    int reduce_mode;  // resolved by the reduce ops (resolve_reduce_mode)
     int rank_inner;
 };
 
@@ -95,7 +111,10 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256) return IRIS_EINVAL;
     out.tile_n = c->tile_n ? c->tile_n : (N <= 128 ? 128 : 256);
     if (c->group_m < 0) return IRIS_EINVAL;
-    out.group_m = c->group_m ? c->group_m : 8;
+    // reduce ops: a wide swizzle group keeps one rank's operands in L2 per
+    // group phase and spaces a tile's W ranks several waves apart
+    const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
+    out.group_m = c->group_m ? c->group_m : (reduce_op ? 32 : 8);
     out.comm_block = c->comm_block ? c->comm_block : 65536;
     if (out.comm_block < 0 || out.comm_block % 8 != 0) return IRIS_EINVAL;
     out.replicate = c->replicate_outputs ? 1 : 0;
@@ -115,10 +134,24 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->trace_buf && (c->trace_cap < 2 || (c->trace_buf & 7))) return IRIS_EINVAL;
     out.trace = reinterpret_cast<unsigned long long*>(c->trace_buf);
     out.trace_cap = c->trace_buf ? c->trace_cap : 0;
-    if (c->reduce_mode < 0 || c->reduce_mode > 1) return IRIS_EINVAL;
+    if (c->reduce_mode < 0 || c->reduce_mode > 3) return IRIS_EINVAL;
     out.reduce_mode = c->reduce_mode;
     out.rank_inner = c->rank_inner ? 1 : 0;
     return IRIS_OK;
+}
+
+// Reduce schedule of matmul_reduce_scatter / matmul_all_reduce: 1 = comm
+// queue, 2 = distributed parts, 3 = chained through the epilogues (needs every
+// rank's output slice in whole 32-column chunks).  0 (auto) picks 3 when it
+// applies, else 2.  Returns -1 for an invalid request.
+int resolve_reduce_mode(const iris_b200_config* c, iris_op op, int64_t N, int W) {
+    const int req = c ? c->reduce_mode : 0;
+    const int64_t slice = (op == IRIS_OP_MATMUL_REDUCE_SCATTER && W > 0) ? N / W : N;
+    const bool chain_ok = N % 32 == 0 && slice % 32 == 0;
+    if (req == 0) return chain_ok ? 3 : 2;
+    if (req == 1 || req == 2) return req;
+    if (req == 3) return chain_ok ? 3 : -1;
+    return -1;
 }
 
 // Sizes of the workspace pieces for one call.
@@ -126,18 +159,20 @@ struct WsLayout {
     size_t flags_off, n_flags, partial_off, partial_elems, total;
 };
 
-WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n) {
+WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n, int reduce_mode) {
     WsLayout L{};
     L.flags_off = WS_HEADER;
     const int64_t mb = cdiv(M, BM), nb = cdiv(N, tile_n);
+    const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
     if (op == IRIS_OP_ALL_GATHER_MATMUL)
         L.n_flags = static_cast<size_t>(W) * mb;
-    else if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
-        L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte arrival counters
+    else if (reduce_op)
+        L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte tile counters
     L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
-    if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE)
-        L.partial_elems = static_cast<size_t>(M) * N;
-    L.total = round_up(L.partial_off + L.partial_elems * 4 * (L.partial_elems ? W : 0), 256);
+    if (reduce_op) L.partial_elems = static_cast<size_t>(M) * N;
+    // one fp32 running sum (chained) or one fp32 partial per rank
+    const size_t copies = L.partial_elems ? (reduce_mode == 3 ? 1 : W) : 0;
+    L.total = round_up(L.partial_off + L.partial_elems * 4 * copies, 256);
     return L;
 }
 
@@ -169,7 +204,28 @@ int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t d0, uint64_t d
                      const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? IRIS_OK : IRIS_ECUDA;
+    return r == CUDA_SUCCESS ? IRIS_OK : cuda_fail("cuTensorMapEncodeTiled (operand)", static_cast<int>(r));
+}
+
+// Output map: 4-D {n, row, row block, region} with a 32 x 32 box, written by
+// the epilogue's TMA stores.  fp32 (partials) use the 128-byte swizzle (one
+// 128-byte staging row), 16-bit outputs the 64-byte swizzle.
+int make_out_map(CUtensorMap* m, const void* base, int kind /*0 f16, 1 bf16, 2 f32*/, uint64_t n,
+                 uint64_t rows, uint64_t blocks, uint64_t regions, uint64_t row_pitch, uint64_t block_pitch,
+                 uint64_t region_pitch) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    cuuint64_t dims[4] = {n, rows, blocks, regions};
+    cuuint64_t strides[3] = {row_pitch, block_pitch, region_pitch};
+    cuuint32_t box[4] = {32, 32, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = kind == 2   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : kind == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     kind == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? IRIS_OK : cuda_fail("cuTensorMapEncodeTiled (output)", static_cast<int>(r));
 }
 
 void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks, const Cfg& c) {
@@ -205,7 +261,8 @@ int launch(Params& p, const Cfg& c, cudaStream_t stream) {
         fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>
             <<<c.grid, NUM_THREADS, smem_bytes<BN_NARROW, STAGES_NARROW>(), stream>>>(p);
     }
-    return cudaGetLastError() == cudaSuccess ? IRIS_OK : IRIS_ECUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? IRIS_OK : cuda_fail("kernel launch", static_cast<int>(e));
 }
 
 bool dims_ok(int64_t M, int64_t N, int64_t K) {
@@ -215,7 +272,7 @@ bool dims_ok(int64_t M, int64_t N, int64_t K) {
 
 int prepare_ws(Params& p, void* ws, size_t ws_bytes, iris_op op, int64_t M, int64_t N, int W,
                const Cfg& c) {
-    const WsLayout L = ws_layout(op, M, N, W, c.tile_n);
+    const WsLayout L = ws_layout(op, M, N, W, c.tile_n, c.reduce_mode);
     if (!ws || ws_bytes < L.total) return IRIS_ENOWS;
     if (!aligned16(reinterpret_cast<uintptr_t>(ws))) return IRIS_EALIGN;
     p.ws = reinterpret_cast<WsHeader*>(ws);
@@ -261,7 +318,12 @@ int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int wo
     }
     int64_t Mrows = M;
     if (op == IRIS_OP_MATMUL_ALL_GATHER) Mrows = 0;  // no flags or partials
-    *bytes = ws_layout(op, Mrows, N, world, tile_n).total;
+    int mode = 0;
+    if (op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE) {
+        mode = resolve_reduce_mode(cfg, op, N, world);
+        if (mode < 0) return IRIS_EINVAL;
+    }
+    *bytes = ws_layout(op, Mrows, N, world, tile_n, mode).total;
     return IRIS_OK;
 }
 
@@ -310,6 +372,9 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
             return rc;
     }
+    if (p.n_gemm > 0 &&
+        (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M, 1, W, N * 2, size_t(M) * N * 2, heap->rank_stride)))
+        return rc;
     return launch(p, c, stream);
 }
 
@@ -329,6 +394,8 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if (K % 8 != 0 || N % 8 != 0 || N_l % 8 != 0) return IRIS_EALIGN;
     Cfg c;
     if ((rc = resolve_cfg(cfg, op, N, c))) return rc;
+    c.reduce_mode = resolve_reduce_mode(cfg, op, N, W);
+    if (c.reduce_mode < 0) return IRIS_EINVAL;
     if ((rc = check_region(heap, off_A, size_t(M) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N_l * 2))) return rc;
@@ -354,10 +421,28 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if (tiles * W >= 0x7FFFFFFFull) return IRIS_EINVAL;
     p.n_gemm = static_cast<uint32_t>(tiles * W);
     p.n_comm = c.reduce_mode == 1 ? static_cast<uint32_t>(tiles) : 0u;
+    p.n_parts = c.reduce_mode == 2 ? static_cast<uint32_t>(tiles * W) : 0u;
     if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64, BK))) return rc;
+    }
+    if (p.n_gemm > 0) {
+        if (c.reduce_mode == 3) {
+            // running sum (fp32) and the 16-bit output written by the last rank
+            if ((rc = make_out_map(&p.tmS, p.partials, 2, N, M, 1, 1, N * 4, size_t(M) * N * 4, size_t(M) * N * 4)))
+                return rc;
+            if (op == IRIS_OP_MATMUL_REDUCE_SCATTER)
+                rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N_l, M, W, 1, N_l * 2, heap->rank_stride,
+                                  heap->rank_stride * W);
+            else
+                rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M, 1, W, N * 2, size_t(M) * N * 2,
+                                  heap->rank_stride);
+            if (rc) return rc;
+        } else if ((rc = make_out_map(&p.tmC, p.partials, 2, N, M, W, 1, N * 4, size_t(M) * N * 4,
+                                      size_t(W) * M * N * 4))) {
+            return rc;
+        }
     }
     return launch(p, c, stream);
 }
@@ -419,6 +504,9 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
             return rc;
     }
+    if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M_l, W, W, N * 2,
+                                           size_t(M_l) * N * 2, heap->rank_stride)))
+        return rc;
     return launch(p, c, stream);
 }
 
@@ -498,6 +586,9 @@ int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, 
         if ((rc = make_map(&p.tmA, A, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK))) return rc;
     }
+    if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, C, p.bf16, N, M, 1, 1, N * 2, size_t(M) * N * 2,
+                                           size_t(M) * N * 2)))
+        return rc;
     return launch(p, c, stream);
 }
 

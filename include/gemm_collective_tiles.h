@@ -115,11 +115,20 @@ typedef struct {
                               TMA, workers) of trace_cap (event, ns) u64 pairs,
                               pair 0 holding the count; 0 = off */
     int trace_cap;         /* pairs per stream (>= 2 when trace_buf is set) */
-    int reduce_mode;       /* matmul_reduce_scatter / matmul_all_reduce: 0 = the rank
-                              whose partial completes an output tile reduces it right
-                              away (epoch-tagged arrival counter per tile; default);
-                              1 = reduce tiles go through the comm queue and wait on
-                              per-partial ready-flags (the gemm_ctas split applies) */
+    int reduce_mode;       /* matmul_reduce_scatter / matmul_all_reduce reduce schedule:
+                              0 = auto (3 when every rank's output slice is whole
+                                  32-column chunks, else 2);
+                              1 = comm queue: reduce tiles claimed like GEMM tiles,
+                                  waiting on per-partial ready-flags (the gemm_ctas
+                                  split applies);
+                              2 = distributed parts: each output tile's rows split in
+                                  W parts that idle worker warps claim once all W
+                                  partials are in (epoch-tagged tile counters);
+                              3 = chained: rank s adds its partial to the running fp32
+                                  sum of ranks 0..s-1 in its GEMM epilogue and hands the
+                                  tile on; the last rank writes the rounded output
+                                  (a per-tile ring reduction; workspace holds one M x N
+                                  fp32 sum instead of W partials) */
     int rank_inner;        /* reduce ops: 1 = order GEMM tiles with the rank index
                               fastest; 0 (default) = rank by rank inside each GROUP_M
                               group, so one rank's operands share the L2 at a time */

@@ -44,15 +44,29 @@ def test_workspace_size_layout():
     assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 4096, 14336, 4096, 8, N.IRIS_BF16,
                                         None, ctypes.byref(out)) == 0
     assert out.value == 256 + ((8 * 32 * 4 + 255) // 256) * 256
-    # reduce-scatter: flags per (rank, tile) + W fp32 partials of M x N
+    # reduce-scatter, default (chained) schedule: flags / tile counters + one
+    # fp32 running sum of M x N
     assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 4096, 4096, 4096, 4, N.IRIS_F16,
                                         None, ctypes.byref(out)) == 0
     flags = 4 * 32 * 16 * 4
-    assert out.value == 256 + flags + 4 * 4096 * 4096 * 4
+    assert out.value == 256 + flags + 4096 * 4096 * 4
+    # queue and parts schedules keep one fp32 partial per rank
+    for mode in (1, 2):
+        cfg = gct.make_config(reduce_mode=mode)
+        assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 4096, 4096, 4096, 4, N.IRIS_F16,
+                                            ctypes.byref(cfg), ctypes.byref(out)) == 0
+        assert out.value == 256 + flags + 4 * 4096 * 4096 * 4
+    # chained needs whole 32-column slices: N/W = 8 does not qualify -> parts
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 64, 32, 64, 4, N.IRIS_F16,
+                                        None, ctypes.byref(out)) == 0
+    assert out.value == 256 + 256 + 4 * 64 * 32 * 4
+    cfg = gct.make_config(reduce_mode=3)
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 64, 32, 64, 4, N.IRIS_F16,
+                                        ctypes.byref(cfg), ctypes.byref(out)) == N.IRIS_EINVAL
     cfg = gct.make_config(tile_n=128)
     assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_ALL_REDUCE, 256, 256, 64, 2, N.IRIS_F16,
                                         ctypes.byref(cfg), ctypes.byref(out)) == 0
-    assert out.value == 256 + 256 + 2 * 256 * 256 * 4
+    assert out.value == 256 + 256 + 256 * 256 * 4
     assert lib.iris_b200_workspace_size(N.IRIS_OP_CONCURRENT, 8192, 8192, 8192, 8, N.IRIS_BF16,
                                         None, ctypes.byref(out)) == 0
     assert out.value == 256

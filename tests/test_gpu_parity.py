@@ -138,7 +138,7 @@ def test_ag_mm_bias_on_m_random():
                                          (2, 128, 256, 64, "f16"), (8, 384, 1024, 256, "bf16"),
                                          (1, 136, 264, 64, "bf16")])
 @pytest.mark.parametrize("exact", [True, False])
-@pytest.mark.parametrize("reduce_mode", [0, 1])
+@pytest.mark.parametrize("reduce_mode", [0, 1, 2])
 def test_mm_reduce_scatter(W, M, N, K, dt, exact, reduce_mode):
     kw = dict(dist="int", scale=2, bias_scale=3) if exact else dict(dist="uniform", scale=1.0)
     x = synthetic.make_fused_inputs("mm_rs", W, M, N, K, dt, seed=31 + W + M, bias=True, **kw)
@@ -153,7 +153,7 @@ def test_mm_reduce_scatter(W, M, N, K, dt, exact, reduce_mode):
 
 @pytest.mark.parametrize("W,M,N,K,dt", [(8, 256, 256, 128, "bf16"), (3, 200, 136, 72, "f16")])
 @pytest.mark.parametrize("replicate", [0, 1])
-@pytest.mark.parametrize("reduce_mode", [0, 1])
+@pytest.mark.parametrize("reduce_mode", [0, 1, 2])
 def test_mm_all_reduce_exact_integer(W, M, N, K, dt, replicate, reduce_mode):
     x = synthetic.make_fused_inputs("mm_ar", W, M, N, K, dt, seed=41 + W, dist="int", scale=2,
                                     bias=True, bias_scale=3)
@@ -279,7 +279,8 @@ def test_workspace_reuse_and_schedule_invariance(op):
             assert_exact(a, b)
     for cfg in ({"gemm_ctas": 20}, {"grid": 7}, {"group_m": 1}, {"tile_n": 128}, {"gemm_ctas": -1},
                 {"reduce_mode": 1}, {"reduce_mode": 1, "gemm_ctas": 30}, {"rank_inner": 1},
-                {"rank_inner": 1, "reduce_mode": 1}, {"group_m": 3, "reduce_mode": 1}):
+                {"rank_inner": 1, "reduce_mode": 1}, {"group_m": 3, "reduce_mode": 1}, {"reduce_mode": 2},
+                {"reduce_mode": 2, "grid": 5}, {"reduce_mode": 3, "grid": 3}, {"reduce_mode": 3, "rank_inner": 1}):
         p2 = FusedProblem(op, W, M, N, K, "bf16", bias=True, config=cfg)
         p2.upload(x.A, x.B, x.bias)
         p2.poison_outputs()
