@@ -274,20 +274,118 @@ def workload_config(wl, name, cfg):
     return d
 
 
+def run_concurrent(args, cfg):
+    """Independent GEMM (bf16 8192^3, normal(0,1), seed 3) sharing the SMs with
+    an all-reduce of W=8 fp32 buffers of 64Mi elements (uniform[-1,1], seed 4).
+    value = GEMM TFLOP/s over the whole step; the roofline is
+    max(GEMM flop / tensor peak, collective bytes / HBM bandwidth).  The
+    all-reduce writes a separate output (the same bytes as in place, and the
+    inputs stay unchanged across steps)."""
+    from gemm_collective_tiles_gb300 import query_status
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem
+    cw = synthetic.CONCURRENT_WORKLOAD
+    torch.cuda.set_device(0)
+    A, B = synthetic.make_gemm_inputs(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], cw["gemm_seed"],
+                                      dist="normal", scale=1.0)
+    X = synthetic.make_coll_inputs(cw["W"], cw["count"], cw["coll_dtype"], cw["coll_seed"])
+    peaks, peak_kind = measured_peaks()
+
+    def make(conf, gemm=True, coll=True):
+        pr = ConcurrentProblem(cw["M"] if gemm else 0, cw["N"] if gemm else 0, cw["K"] if gemm else 0,
+                               cw["gemm_dtype"], "all_reduce", cw["W"], cw["count"] if coll else 0,
+                               coll_dtype=cw["coll_dtype"], config=conf or None)
+        pr.upload(A if gemm else None, B if gemm else None, X if coll else None)
+        return pr
+
+    def timeit(probs, steps, warm):
+        stream = torch.cuda.current_stream()
+        for _ in range(warm):
+            for pr in probs:
+                pr.run(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for pr in probs:
+                pr.run(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        for pr in probs:
+            rc = query_status(pr.ws, stream)
+            if rc[0] != 0:
+                raise RuntimeError(f"device status {rc}")
+        return e0.elapsed_time(e1) / steps
+
+    flops = 2.0 * cw["M"] * cw["N"] * cw["K"]
+    coll_bytes = 2.0 * cw["W"] * cw["count"] * 4
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), coll_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    steps = max(3, min(args.steps, 200))
+    warm = max(3, args.warmup)
+    fused = make(cfg)
+    sampler = ClockSampler(0)
+    sampler.start()
+    ms = timeit([fused], steps, warm)
+    clocks = sampler.stop()
+    del fused
+    g_only = make(cfg, coll=False)
+    c_only = make(cfg, gemm=False)
+    ms_g = timeit([g_only], steps, warm)
+    ms_c = timeit([c_only], steps, warm)
+    del g_only, c_only
+    line = {"metric": "concurrent GEMM + all-reduce step: GEMM TFLOPS over the step; % of max(tensor, HBM) roofline",
+            "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warm,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "concurrent: bf16 GEMM 8192^3 || all_reduce W=8 x 64Mi fp32 (concurrent_ar_w8)",
+                       **cfg},
+            "roofline": {"bound": "hbm" if coll_bytes / peaks["hbm_gbs"] > flops / peaks["bf16_tflops"] / 1e3 else "tensor",
+                         "roofline_ms": t_roof, "frac": t_roof / ms, "peak_source": peak_kind},
+            "sequential": {"gemm_ms": ms_g, "all_reduce_ms": ms_c, "sum_ms": ms_g + ms_c,
+                           "speedup_concurrent_vs_sequential": (ms_g + ms_c) / ms,
+                           "gemm_tflops_alone": flops / (ms_g * 1e-3) / 1e12,
+                           "all_reduce_gbs_alone": coll_bytes / (ms_c * 1e-3) / 1e9},
+            "gpu_launches": steps, "clocks": clocks}
+    if args.sweep:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        sweep = []
+        for frac in (0.25, 0.35, 0.45, 0.55, 0.65, 0.75, 0.85, 0.9):
+            conf = dict(cfg)
+            conf["gemm_ctas"] = max(1, int(round(frac * sms)))
+            pr = make(conf)
+            t = timeit([pr], max(3, steps // 4), 2)
+            sweep.append({"gemm_ctas": conf["gemm_ctas"], "ms": t})
+            del pr
+        conf = dict(cfg)
+        conf["gemm_ctas"] = -1
+        pr = make(conf)
+        sweep.append({"gemm_ctas": "balanced", "ms": timeit([pr], max(3, steps // 4), 2)})
+        line["gemm_ctas_sweep"] = sweep
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(synthetic.WORKLOADS) + ["concurrent_ar_w8"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="concurrent workload: also time gemm_ctas from 25%% to 90%% of the SMs")
     ap.add_argument("--config", default="{}", help="JSON dict of iris_b200_config fields")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    wl = dict(synthetic.WORKLOADS[args.workload])
     cfg = json.loads(args.config)
+    if args.workload == "concurrent_ar_w8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the fused-op workloads"}))
+            return 0
+        return run_concurrent(args, cfg)
+    wl = dict(synthetic.WORKLOADS[args.workload])
 
     if args.impl == "reference":
         return run_reference(args, wl, args.workload)

@@ -38,6 +38,7 @@ constexpr int NUM_WORKER_WARPS = 4;  // one per tensor-memory lane quadrant (or 
 constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
 constexpr int NUM_THREADS = 32 * (FIRST_WORKER_WARP + NUM_WORKER_WARPS);
 constexpr int RING = 8;           // work-item ring depth
+constexpr int GATHER_AHEAD = 2;   // all_gather_matmul: look-ahead gathers claimed per GEMM item
 constexpr uint32_t ITEM_END = 0xFFFFFFFFu;
 constexpr uint32_t ITEM_COMM = 0x80000000u;
 constexpr int DEV_TIMEOUT = 1;
@@ -60,6 +61,10 @@ enum : int {
     WAIT_REDUCE_PARTS = 14,
     WAIT_CHAIN = 15,
     WAIT_CHAIN_LOAD = 16,
+    WAIT_LEASE = 17,
+    WAIT_LEASE_DONE = 18,
+    WAIT_COLL_LOAD = 19,
+    WAIT_DRAIN = 20,
 };
 
 // First 256 bytes of the workspace.
@@ -279,13 +284,18 @@ __device__ __forceinline__ uint32_t gemm_index(const Params& p, uint32_t t, int 
     return sg * T * p.W + static_cast<uint32_t>(s) * Tsg + (t - sg * T);
 }
 
-// all_gather_matmul: number of gather items that must be claimed before GEMM
-// item x may be published (all shards of every m-block of x's swizzle group).
+// all_gather_matmul: number of gather items (ordered m-block by m-block, W
+// shards each) that must be claimed before GEMM item x may be published: all
+// shards of every m-block up to x's own.  Inside a swizzle group the first
+// items visit the group's m-blocks in order, so the need grows one m-block per
+// item there and stays at the whole group afterwards (monotonic in x).
 __device__ __forceinline__ uint32_t gather_need(const Params& p, uint32_t x) {
     const uint32_t group_size = static_cast<uint32_t>(p.group_m) * p.n_blocks;
-    const int first_m = static_cast<int>(x / group_size) * p.group_m;
+    const uint32_t group = x / group_size;
+    const int first_m = static_cast<int>(group) * p.group_m;
     const int gsz = min(p.m_blocks - first_m, p.group_m);
-    return static_cast<uint32_t>(first_m + gsz) * p.W;
+    const int local = static_cast<int>(x - group * group_size);
+    return static_cast<uint32_t>(first_m + min(local, gsz - 1) + 1) * p.W;
 }
 
 __device__ __forceinline__ float bits16_to_float(uint32_t b, int bf16) {
@@ -309,17 +319,22 @@ struct Smem {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + 2 * NUM_WORKER_WARPS;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + 2 * NUM_WORKER_WARPS + 2;
+    static constexpr int READY_BITS = 4096;  // all_gather_matmul: m-blocks whose gathers this CTA has seen complete
     static constexpr uint32_t BYTES = 1024 /*align slack*/ + TILES_BYTES +
-                                      NUM_WORKER_WARPS * STAGE_OUT_BYTES + NUM_BARS * 8 + (RING + 4) * 4;
+                                      NUM_WORKER_WARPS * STAGE_OUT_BYTES + NUM_BARS * 8 + (RING + 4) * 4 +
+                                      READY_BITS / 8;
     uint8_t* tiles;
     uint8_t* stage_out;
     uint64_t *full, *empty, *acc_full, *acc_empty, *item_full, *item_empty, *wbar, *final_bar;
-    uint64_t* sbar;  // per worker warp: 2 barriers for running-sum chunk loads
+    uint64_t* sbar;  // per worker warp: 2 barriers for running-sum / collective chunk loads
+    uint64_t* lease;       // TMA producer -> workers: pipeline stages lent for a collective tile
+    uint64_t* lease_done;  // workers -> TMA producer: stages returned
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
     uint32_t* bcast;
+    uint32_t* ready_bits;
 
     __device__ void carve(uint8_t* raw) {
         uintptr_t a = reinterpret_cast<uintptr_t>(raw);
@@ -336,11 +351,14 @@ struct Smem {
         wbar = item_empty + RING;
         final_bar = wbar + 1;
         sbar = final_bar + 1;
-        uint32_t* u = reinterpret_cast<uint32_t*>(sbar + 2 * NUM_WORKER_WARPS);
+        lease = sbar + 2 * NUM_WORKER_WARPS;
+        lease_done = lease + 1;
+        uint32_t* u = reinterpret_cast<uint32_t*>(lease_done + 1);
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
         bcast = u + RING + 2;
+        ready_bits = u + RING + 4;
 
     }
     __device__ uint8_t* a_tile(uint32_t s) const { return tiles + s * STAGE_BYTES; }
@@ -382,14 +400,21 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
             return true;
         }
         if (p.op == OP_AG_MM) {
-            const uint32_t la = min(g + p.lookahead, p.n_gemm - 1);
-            const uint32_t need = gather_need(p, la);
-            while (!comm_dry && ld_relaxed_gpu(&p.ws->comm_ctr) < need) {
+            // gathers g itself needs are claimed before g (mandatory); gathers
+            // for items up to `lookahead` ahead are claimed at most
+            // GATHER_AHEAD per GEMM item, so they spread over many CTAs
+            const uint32_t need = gather_need(p, g);
+            const uint32_t need_ahead = gather_need(p, min(g + p.lookahead, p.n_gemm - 1));
+            int ahead = 0;
+            while (!comm_dry) {
+                const uint32_t head = ld_relaxed_gpu(&p.ws->comm_ctr);
+                if (head >= need && (head >= need_ahead || ahead >= GATHER_AHEAD)) break;
                 const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
                 if (c >= p.n_comm) {
                     comm_dry = true;
                     break;
                 }
+                if (c >= need) ++ahead;
                 if (!publish(ITEM_COMM | c)) return false;
             }
         }
@@ -487,8 +512,25 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
         }
         const int b_rank = reduce_op ? gc.rank : 0;
         int acquired = 0;  // all_gather_matmul: shards whose flags are held
+        if (p.op == OP_AG_MM) {
+            // an m-block seen complete before needs no flag traffic; else check
+            // all W shard flags at once and take the per-shard waits below
+            // only for the shards still missing
+            const bool cacheable = gc.mb < Smem<BN, STAGES>::READY_BITS;
+            if (cacheable && (sm.ready_bits[gc.mb >> 5] >> (gc.mb & 31) & 1u)) {
+                acquired = p.W;
+            } else {
+                uint32_t seen = 0;
+                for (int s = 0; s < p.W; ++s) seen += ld_acquire_gpu(&p.flags[gc.mb * p.W + s]) == ctl.epoch ? 1u : 0u;
+                if (seen == static_cast<uint32_t>(p.W)) {
+                    acquired = p.W;
+                    fence_proxy_async_global();
+                    if (cacheable) sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
+                }
+            }
+        }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (p.op == OP_AG_MM) {
+            if (p.op == OP_AG_MM && acquired < p.W) {
                 const int s_hi = min(p.W - 1, (kb * BK + BK - 1) / p.K_local);
                 if (s_hi >= acquired) {
                     for (int s = acquired; s <= s_hi; ++s) {
@@ -497,6 +539,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
                     }
                     acquired = s_hi + 1;
                     fence_proxy_async_global();
+                    if (acquired == p.W && gc.mb < Smem<BN, STAGES>::READY_BITS)
+                        sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
                 }
             }
             if (!wait_bar(ctl, &sm.empty[stage], phase ^ 1, WAIT_SMEM_EMPTY)) return false;
@@ -516,6 +560,7 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
         return true;
     };
 
+    uint32_t leases = 0;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
         if (!wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_TMA)) break;
@@ -523,7 +568,19 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
         mbar_arrive(&sm.item_empty[slot]);
         ++ring_n;
         if (item == ITEM_END) break;
-        if (item & ITEM_COMM) continue;
+        if (item & ITEM_COMM) {
+            if (p.op != OP_CONC) continue;
+            // lend the pipeline stages to the workers for this collective
+            // tile: every load issued so far must have been consumed first
+            bool ok = true;
+            for (int s = 0; s < STAGES && ok; ++s)
+                if (used_mask & (1u << s)) ok = wait_bar(ctl, &sm.empty[s], issued_phase[s], WAIT_DRAIN);
+            if (!ok) break;
+            mbar_arrive(sm.lease);
+            if (!wait_bar(ctl, sm.lease_done, leases & 1, WAIT_LEASE_DONE)) break;
+            ++leases;
+            continue;
+        }
         tr.rec(EV_BEGIN, item);
         if (!load_gemm(item)) break;
         tr.rec(EV_END, item);
@@ -1214,91 +1271,107 @@ __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx&
     }
 }
 
-// concurrent-mode collective tile over the W heap regions
-__device__ __noinline__ void coll_tile(const Params& p, uint32_t c, WorkerCtx& wc) {
-    const int tid = wc.w * 32 + wc.lane;
-    constexpr int NT = NUM_WORKER_WARPS * 32;
+// Concurrent-mode collective tile through the TMA engine, run while the TMA
+// producer lends the CTA's pipeline stages (STAGES x STAGE_BYTES bytes of
+// shared memory) to the workers.  Worker warp w owns 1/4 of that space as two
+// buffers; for each sub-chunk of its slice of tile c it bulk-loads the sources
+// (all W ranks for all-reduce / reduce-scatter, rank s for all-gather) into one
+// buffer while the other is summed in rank order (fp32) and bulk-stored to the
+// destinations.  Bytes in flight per SM: about half the stage area.
+template <int BN, int STAGES>
+__device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t c, WorkerCtx& wc) {
+    constexpr uint32_t AREA = STAGES * Smem<BN, STAGES>::STAGE_BYTES / NUM_WORKER_WARPS;
+    constexpr uint32_t HALF = AREA / 2;
+    uint8_t* area = sm.tiles + wc.w * AREA;
+    uint64_t* bar = sm.sbar + 2 * wc.w;
+    const size_t esz = static_cast<size_t>(p.elem_bytes);
+    // this tile's byte range, per source rank, and the sources / destinations
+    size_t b0, b1;
+    int src_lo, src_n;
+    size_t dst_off_base;  // AG: where rank s's block goes in every output
     if (p.coll == COLL_AG) {
-        // item c = (source rank s, chunk k) of comm_block elements
-        const long long bytes_per_rank = p.count * p.elem_bytes;
-        const long long chunk_bytes = static_cast<long long>(p.comm_block) * p.elem_bytes;
-        const long long chunks = (bytes_per_rank + chunk_bytes - 1) / chunk_bytes;
+        const size_t bytes_per_rank = static_cast<size_t>(p.count) * esz;
+        const size_t chunk = static_cast<size_t>(p.comm_block) * esz;
+        const size_t chunks = (bytes_per_rank + chunk - 1) / chunk;
         const int s = static_cast<int>(c / chunks);
-        const long long k = c - static_cast<long long>(s) * chunks;
-        const long long b0 = k * chunk_bytes;
-        const long long nv = (min(bytes_per_rank, b0 + chunk_bytes) - b0) / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_in + b0);
-        const size_t dst_off = p.off_cout + static_cast<size_t>(s) * bytes_per_rank + b0;
-        constexpr int U = 8;
-        for (long long base = tid; base < nv; base += NT * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (base + u * NT < nv) v[u] = __ldcs(src + base + u * NT);
-            for (int r = 0; r < p.W; ++r) {
-                uint4* dst = reinterpret_cast<uint4*>(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_off);
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (base + u * NT < nv) dst[base + u * NT] = v[u];
-            }
-        }
-        return;
+        b0 = (c - s * chunks) * chunk;
+        b1 = min(bytes_per_rank, b0 + chunk);
+        src_lo = s;
+        src_n = 1;
+        dst_off_base = static_cast<size_t>(s) * bytes_per_rank;
+    } else {
+        b0 = static_cast<size_t>(c) * p.comm_block * 4;
+        b1 = min(static_cast<size_t>(p.count) * 4, b0 + static_cast<size_t>(p.comm_block) * 4);
+        src_lo = 0;
+        src_n = p.W;
+        dst_off_base = 0;
     }
-    // all-reduce / reduce-scatter: chunk c of the element index space
-    const long long e0 = static_cast<long long>(c) * p.comm_block;
-    const long long e1 = min(p.count, e0 + p.comm_block);
-    const long long nv = (e1 - e0) / 4;
-    const long long cw = p.count / p.W;  // reduce-scatter chunk per rank
-    int rs_rank = 0;
-    long long rs_bound = cw;             // first element past rs_rank's chunk
-    if (p.coll == COLL_RS) {
-        const long long first = e0 + static_cast<long long>(tid) * 4;
-        rs_rank = static_cast<int>(first / cw);
-        rs_bound = static_cast<long long>(rs_rank + 1) * cw;
-    }
-    constexpr int U = 2;
-    for (long long base = tid; base < nv; base += NT * U) {
-        float4 acc[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (base + u * NT < nv)
-                acc[u] = __ldcs(reinterpret_cast<const float4*>(p.heap + p.off_in) + e0 / 4 + base + u * NT);
-        for (int s = 1; s < p.W; ++s) {
-            const float4* xs = reinterpret_cast<const float4*>(p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_in);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (base + u * NT < nv) {
-                    const float4 v = __ldcs(xs + e0 / 4 + base + u * NT);
-                    acc[u].x = acc[u].x + v.x;
-                    acc[u].y = acc[u].y + v.y;
-                    acc[u].z = acc[u].z + v.z;
-                    acc[u].w = acc[u].w + v.w;
+    // the warp's contiguous slice (16-byte granules)
+    const size_t g_tot = (b1 - b0) / 16;
+    const size_t g_lo = g_tot * wc.w / NUM_WORKER_WARPS, g_hi = g_tot * (wc.w + 1) / NUM_WORKER_WARPS;
+    const uint32_t sub = (HALF / src_n) & ~15u;  // bytes per source per sub-chunk
+    const size_t s_lo = b0 + g_lo * 16, s_hi = b0 + g_hi * 16;
+    const int nsub = static_cast<int>((s_hi - s_lo + sub - 1) / sub);
+    const size_t cw_bytes = static_cast<size_t>(p.count / p.W) * 4;  // reduce-scatter slice per rank
+    auto issue = [&](int i) {
+        const size_t o = s_lo + static_cast<size_t>(i) * sub;
+        const uint32_t n = static_cast<uint32_t>(min(static_cast<size_t>(sub), s_hi - o));
+        uint8_t* buf = area + (i & 1) * HALF;
+        bulk_wait_read_all();  // earlier stores have read this buffer
+        mbar_arrive_expect_tx(&bar[i & 1], n * src_n);
+        for (int r = 0; r < src_n; ++r)
+            bulk_load(buf + r * sub, p.heap + static_cast<size_t>(src_lo + r) * p.rank_stride + p.off_in + o, n,
+                      &bar[i & 1]);
+    };
+    if (nsub > 0 && wc.lane == 0) issue(0);
+    for (int i = 0; i < nsub; ++i) {
+        if (i + 1 < nsub && wc.lane == 0) issue(i + 1);
+        int ok = 1;
+        if (wc.lane == 0) ok = wait_bar(ctl, &bar[i & 1], (wc.sphase >> (i & 1)) & 1u, WAIT_COLL_LOAD) ? 1 : 0;
+        wc.sphase ^= 1u << (i & 1);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+        const size_t o = s_lo + static_cast<size_t>(i) * sub;
+        const uint32_t n = static_cast<uint32_t>(min(static_cast<size_t>(sub), s_hi - o));
+        uint8_t* buf = area + (i & 1) * HALF;
+        if (src_n > 1) {
+            // rank-order fp32 sum into the rank-0 slot
+            for (uint32_t q = wc.lane; q < n / 16; q += 32) {
+                float4 a = *reinterpret_cast<const float4*>(buf + q * 16);
+                for (int r = 1; r < src_n; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(buf + r * sub + q * 16);
+                    a.x = a.x + v.x;
+                    a.y = a.y + v.y;
+                    a.z = a.z + v.z;
+                    a.w = a.w + v.w;
                 }
-        }
-        if (p.coll == COLL_AR) {
-            for (int r = 0; r < p.W; ++r) {
-                float4* dst = reinterpret_cast<float4*>(p.heap + static_cast<size_t>(r) * p.rank_stride + p.off_cout);
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (base + u * NT < nv) dst[e0 / 4 + base + u * NT] = acc[u];
+                *reinterpret_cast<float4*>(buf + q * 16) = a;
             }
-        } else {
-            // elements of one thread increase monotonically, so the owning
-            // rank only ever moves forward: advance it by comparison
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (base + u * NT < nv) {
-                    const long long e = e0 + (base + u * NT) * 4;
-                    while (e >= rs_bound) {
-                        ++rs_rank;
-                        rs_bound += cw;
-                    }
-                    float4* dst = reinterpret_cast<float4*>(p.heap + static_cast<size_t>(rs_rank) * p.rank_stride +
-                                                            p.off_cout);
-                    dst[(e - (rs_bound - cw)) / 4] = acc[u];
+            fence_proxy_async_shared();
+        }
+        __syncwarp();
+        if (wc.lane == 0) {
+            if (p.coll == COLL_RS) {
+                // o..o+n may cross a rank boundary: split the store there
+                size_t done = 0;
+                while (done < n) {
+                    const size_t e = o + done;
+                    const int rr = static_cast<int>(e / cw_bytes);
+                    const size_t piece = min(static_cast<size_t>(n) - done, (rr + 1) * cw_bytes - e);
+                    bulk_store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
+                               buf + done, static_cast<uint32_t>(piece));
+                    done += piece;
                 }
+            } else {
+                for (int r = 0; r < p.W; ++r)
+                    bulk_store(p.heap + static_cast<size_t>(r) * p.rank_stride + p.off_cout + dst_off_base + o, buf, n);
+            }
+            bulk_commit();
         }
     }
+    // the stages go back to the TMA producer once every store has read them
+    if (wc.lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    return true;
 }
 
 template <int BN, int STAGES>
@@ -1313,6 +1386,7 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
     if (wc.w == 0 && lane == 0) tr.init(p, TR_WORK);
     wc.wphase = 0;
     wc.sphase = 0;
+    uint32_t leases = 0;
     PartState ps;
     ps.cur = NO_PART;
     ps.row = 0;
@@ -1331,9 +1405,18 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
         tr.rec(EV_BEGIN, item);
         if (item & ITEM_COMM) {
             const uint32_t c = item & ~ITEM_COMM;
-            if (p.op == OP_AG_MM) ok = gather_tile(p, ctl, sm, c, wc);
-            else if (p.op == OP_CONC) coll_tile(p, c, wc);
-            else ok = reduce_tile<BN, STAGES>(p, ctl, c, wc);
+            if (p.op == OP_AG_MM) {
+                ok = gather_tile(p, ctl, sm, c, wc);
+            } else if (p.op == OP_CONC) {
+                int got = 1;
+                if (lane == 0) got = wait_bar(ctl, sm.lease, leases & 1, WAIT_LEASE) ? 1 : 0;
+                ++leases;
+                ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0 && coll_tile_tma<BN, STAGES>(p, ctl, sm, c, wc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.lease_done);
+            } else {
+                ok = reduce_tile<BN, STAGES>(p, ctl, c, wc);
+            }
         } else {
             if (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR))
                 ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
@@ -1400,6 +1483,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         mbar_init(sm.wbar, NUM_WORKER_WARPS);
         mbar_init(sm.final_bar, 1);
         for (int i = 0; i < 2 * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
+        mbar_init(sm.lease, 1);
+        mbar_init(sm.lease_done, NUM_WORKER_WARPS);
+        for (int i = 0; i < Smem<BN, STAGES>::READY_BITS / 32; ++i) sm.ready_bits[i] = 0u;
         fence_mbar_init();
         uint32_t e = *reinterpret_cast<volatile uint32_t*>(&p.ws->epoch) + 1u;
         if (e == 0u) e = 1u;

@@ -111,10 +111,10 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256) return IRIS_EINVAL;
     out.tile_n = c->tile_n ? c->tile_n : (N <= 128 ? 128 : 256);
     if (c->group_m < 0) return IRIS_EINVAL;
-    // reduce ops: a wide swizzle group keeps one rank's operands in L2 per
-    // group phase and spaces a tile's W ranks several waves apart
-    const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
-    out.group_m = c->group_m ? c->group_m : (reduce_op ? 32 : 8);
+    // 32 m-blocks per swizzle group (measured best on the reduce ops, where it
+    // also keeps one rank's operands in L2 per group phase and spaces a
+    // tile's W ranks several waves apart, and on all_gather_matmul)
+    out.group_m = c->group_m ? c->group_m : 32;
     out.comm_block = c->comm_block ? c->comm_block : 65536;
     if (out.comm_block < 0 || out.comm_block % 8 != 0) return IRIS_EINVAL;
     out.replicate = c->replicate_outputs ? 1 : 0;
