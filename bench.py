@@ -171,6 +171,23 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def max_over_ranks(x: float, pg) -> float:
+    """The largest value of x over all ranks (identity without a process
+    group); the tensor lives on the device the backend works on."""
+    if pg is None:
+        return float(x)
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank processes flops_per_step per step, the
+    job takes the slowest rank's time."""
+    return flops_per_step * steps * world / (total_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ CPU side
 
 def oracle_rows(wl: dict, x, rows: int):
@@ -437,13 +454,9 @@ def main():
     if rc[0] != 0:
         raise RuntimeError(f"device status after timed steps: {rc}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), pg)
     flops = prob.flops()
-    value = flops * K * world / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, K, total_ms)
     ms_per_step = total_ms / K
 
     # roofline of the one kernel per step
@@ -478,11 +491,7 @@ def main():
             h.copy_(v, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / E
-    if pg:
-        t = torch.tensor([e2e_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, pg)
     e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     rc = query_status(prob.ws, stream)

@@ -125,6 +125,19 @@ def make_config(**kw) -> iris_b200_config:
     return c
 
 
+def _resolve(cfg, op: str, W: int, M: int, N: int, K: int, dtype: torch.dtype):
+    """config="auto": the measured winner cached for this device and shape
+    (see tuning.py), else the static default."""
+    if isinstance(cfg, str):
+        if cfg != "auto":
+            raise ValueError(f"unknown config {cfg!r}")
+        from . import tuning
+        name = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[dtype]
+        hit = tuning.select(tuning.device_arch(), tuning.shape_key(op, W, M, N, K, name))
+        return hit or None
+    return cfg
+
+
 def _cfgp(cfg):
     if cfg is None:
         return None
@@ -177,6 +190,7 @@ def all_gather_matmul(heap: SymmetricHeap, A: HeapTensor, B: HeapTensor, out: He
     B (K, N), bias and outputs in region 0).  Returns the workspace."""
     M, K_l = A.shape
     K, N = B.shape
+    config = _resolve(config, "all_gather_matmul", heap.world, M, N, K, B.dtype)
     ws = _ws(workspace, workspace_size("all_gather_matmul", M, N, K, heap.world, B.dtype, config),
              heap.buf.device)
     _native.check("iris_b200_all_gather_matmul", _native.load().iris_b200_all_gather_matmul(
@@ -186,6 +200,7 @@ def all_gather_matmul(heap: SymmetricHeap, A: HeapTensor, B: HeapTensor, out: He
 
 
 def _mm_coll(name, heap, A, B, out, bias, config, workspace, stream, M, N, K):
+    config = _resolve(config, name, heap.world, M, N, K, B.dtype)
     ws = _ws(workspace, workspace_size(name, M, N, K, heap.world, B.dtype, config), heap.buf.device)
     fn = getattr(_native.load(), "iris_b200_" + name)
     _native.check("iris_b200_" + name, fn(
@@ -240,6 +255,7 @@ def concurrent_gemm_collective(A: Optional[torch.Tensor], B: Optional[torch.Tens
         dev = heap.buf.device
     W = heap.world if heap is not None else 1
     count = x_in.nbytes // torch.empty((), dtype=x_in.dtype).element_size() if x_in is not None else 0
+    config = _resolve(config, "concurrent", W, M, N, K, gdt)
     ws = _ws(workspace, workspace_size("concurrent", M, N, K, W, gdt, config), dev)
     hp = ctypes.byref(heap.c_heap()) if heap is not None else None
     _native.check("iris_b200_concurrent_gemm_collective",

@@ -1,0 +1,176 @@
+"""Config selection for the fused ops: explicit config, else a measured
+winner cached in a JSON file, else the library's static default.
+
+The shape of this subsystem follows ROCm/iris PR #544 ("Add iris.concurrent",
+the autotune commit) and PR #506 (auto-config selection): candidates are ranked,
+the top ones are benchmarked together with the static default, and the winner
+is cached per (architecture, op, world size, shape, dtype).  Because the
+default is always measured, tuning never ends worse than the default.  The
+cache is written atomically (a per-process temporary file, then a rename).
+The MI300X tables and rules on those pages do not carry over; every value
+here is measured on the running GPU.
+"""
+from __future__ import annotations
+
+import json
+import os
+from typing import Callable, Dict, Iterable, List, Optional, Sequence
+
+ENV_CACHE = "IRIS_B200_CACHE"
+
+# knobs a cached entry may set (the rest stay at their defaults)
+TUNABLE = ("tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block")
+
+
+def cache_path() -> str:
+    p = os.environ.get(ENV_CACHE)
+    if p:
+        return p
+    return os.path.join(os.path.expanduser("~"), ".cache", "gemm_collective_tiles", "tuning.json")
+
+
+def arch_key(device_name: str, sm_count: int, capability=(10, 3)) -> str:
+    """Stable cache key of the device: name, compute capability, SM count."""
+    return f"{device_name.strip()}|sm_{capability[0]}{capability[1]}|{int(sm_count)}sm"
+
+
+def shape_key(op: str, W: int, M: int, N: int, K: int, dtype: str) -> str:
+    return f"{op}|W{int(W)}|{int(M)}x{int(N)}x{int(K)}|{dtype}"
+
+
+def load_db(path: Optional[str] = None) -> Dict[str, Dict[str, dict]]:
+    path = path or cache_path()
+    try:
+        with open(path) as f:
+            db = json.load(f)
+        return db if isinstance(db, dict) else {}
+    except (OSError, ValueError):
+        return {}
+
+
+def save_db(db: Dict[str, Dict[str, dict]], path: Optional[str] = None) -> bool:
+    """Atomic write: a per-process temporary file renamed over the cache, so a
+    concurrent reader sees the old or the new file, never a torn one."""
+    path = path or cache_path()
+    try:
+        os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+        tmp = f"{path}.{os.getpid()}.tmp"
+        with open(tmp, "w") as f:
+            json.dump(db, f, indent=1, sort_keys=True)
+        os.replace(tmp, path)
+        return True
+    except OSError:
+        return False
+
+
+def lookup(arch: str, key: str, path: Optional[str] = None) -> Optional[dict]:
+    entry = load_db(path).get(arch, {}).get(key)
+    if not entry:
+        return None
+    return {k: v for k, v in entry.get("config", {}).items() if k in TUNABLE}
+
+
+def record(arch: str, key: str, config: dict, ms: float, default_ms: float, path: Optional[str] = None) -> bool:
+    db = load_db(path)
+    db.setdefault(arch, {})[key] = {"config": {k: v for k, v in config.items() if k in TUNABLE},
+                                    "ms": ms, "default_ms": default_ms}
+    return save_db(db, path)
+
+
+def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: int = 8) -> List[dict]:
+    """Ranked candidate configs (the static default, {}, is always first).
+
+    Ranking rule (from the measurements behind the defaults): the swizzle
+    group width matters most for operand reuse in L2, then the tile width for
+    small N, then -- per op -- the reduce schedule or the concurrent CTA
+    split.  The list is truncated to top_k."""
+    out: List[dict] = [{}]
+    for gm in (32, 16, 64, 8):
+        out.append({"group_m": gm})
+    if N <= 4096:
+        out.append({"tile_n": 128})
+    if op in ("matmul_reduce_scatter", "matmul_all_reduce"):
+        out += [{"reduce_mode": 2}, {"reduce_mode": 1}, {"group_m": 64, "reduce_mode": 3}]
+    if op == "concurrent":
+        for frac in (0.55, 0.45, 0.65, 0.35, 0.75):
+            out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
+    # drop duplicates, keep order
+    seen, uniq = set(), []
+    for c in out:
+        k = json.dumps(c, sort_keys=True)
+        if k not in seen:
+            seen.add(k)
+            uniq.append(c)
+    return uniq[:max(1, top_k)]
+
+
+def tune(measure: Callable[[dict], float], cands: Sequence[dict], arch: str, key: str,
+         path: Optional[str] = None) -> dict:
+    """Benchmark every candidate with ``measure(config) -> ms`` (the static
+    default {} is added if missing), cache and return the fastest.  A
+    candidate the library rejects (``measure`` raises) is skipped."""
+    cands = list(cands)
+    if {} not in cands:
+        cands.insert(0, {})
+    results = []
+    default_ms = None
+    for c in cands:
+        try:
+            ms = float(measure(dict(c)))
+        except Exception:  # noqa: BLE001 -- an invalid candidate for this shape
+            continue
+        results.append((ms, c))
+        if c == {}:
+            default_ms = ms
+    if not results:
+        raise RuntimeError("no candidate config could run")
+    best_ms, best = min(results, key=lambda t: t[0])
+    if default_ms is not None and best_ms > default_ms:   # cannot happen; kept explicit
+        best_ms, best = default_ms, {}
+    record(arch, key, best, best_ms, default_ms if default_ms is not None else best_ms, path)
+    return {"config": best, "ms": best_ms, "default_ms": default_ms, "tried": len(results)}
+
+
+def select(arch: str, key: str, explicit: Optional[dict] = None, path: Optional[str] = None) -> dict:
+    """Explicit config, else the cached winner, else {} (the static default)."""
+    if explicit:
+        return dict(explicit)
+    hit = lookup(arch, key, path)
+    return hit if hit is not None else {}
+
+
+def device_arch() -> str:
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return arch_key(props.name, props.multi_processor_count, (props.major, props.minor))
+
+
+def tune_fused(op: str, W: int, M: int, N: int, K: int, dtype: str, seed: int = 0, top_k: int = 8,
+               reps: int = 10, path: Optional[str] = None) -> dict:
+    """Measure the candidates of a fused op (runner.FusedProblem) on the
+    current GPU with CUDA events and cache the winner."""
+    import torch
+
+    from .runner import FusedProblem
+    short = {"all_gather_matmul": "ag_mm", "matmul_reduce_scatter": "mm_rs",
+             "matmul_all_gather": "mm_ag", "matmul_all_reduce": "mm_ar"}[op]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+    def measure(cfg):
+        prob = FusedProblem(short, W, M, N, K, dtype, config=cfg)
+        for r in range(W):
+            prob.heap.view(prob.A, r).normal_(0, 0.02)
+            prob.heap.view(prob.B, r if prob.per_rank_b() else 0).normal_(0, 0.02)
+        for _ in range(2):
+            prob.run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            prob.run()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    return tune(measure, candidates(op, W, M, N, K, sms, top_k), device_arch(),
+                shape_key(op, W, M, N, K, dtype), path)

@@ -1,0 +1,75 @@
+"""Config selection: JSON cache round trip, atomic writes, stable keys, and
+tuning that always measures the static default and never ends worse.  CPU."""
+import json
+import os
+
+import pytest
+
+from gemm_collective_tiles_gb300 import tuning
+
+
+def test_keys_are_stable_strings():
+    a = tuning.arch_key("NVIDIA GB300 ", 152, (10, 3))
+    assert a == "NVIDIA GB300|sm_103|152sm"
+    assert tuning.shape_key("matmul_reduce_scatter", 4, 4096, 4096, 4096, "f16") == \
+        "matmul_reduce_scatter|W4|4096x4096x4096|f16"
+
+
+def test_cache_round_trip_and_atomic_write(tmp_path):
+    path = str(tmp_path / "sub" / "tuning.json")
+    assert tuning.lookup("a", "k", path) is None
+    assert tuning.record("a", "k", {"group_m": 16, "not_a_knob": 1}, 1.0, 2.0, path)
+    assert tuning.lookup("a", "k", path) == {"group_m": 16}
+    # no temporary files left behind, valid JSON on disk
+    assert sorted(os.listdir(tmp_path / "sub")) == ["tuning.json"]
+    json.load(open(path))
+    # a second key keeps the first
+    tuning.record("a", "k2", {"tile_n": 128}, 1.0, 1.0, path)
+    assert tuning.lookup("a", "k", path) == {"group_m": 16}
+    assert tuning.lookup("b", "k", path) is None
+
+
+def test_corrupt_cache_reads_as_empty(tmp_path):
+    path = tmp_path / "tuning.json"
+    path.write_text("{not json")
+    assert tuning.load_db(str(path)) == {}
+    assert tuning.select("a", "k", None, str(path)) == {}
+
+
+def test_tune_measures_default_and_never_loses(tmp_path):
+    path = str(tmp_path / "t.json")
+    times = {json.dumps({}): 5.0, json.dumps({"group_m": 16}): 4.0, json.dumps({"tile_n": 128}): 6.0}
+    seen = []
+
+    def measure(cfg):
+        seen.append(cfg)
+        if cfg == {"group_m": 64}:
+            raise RuntimeError("rejected by the library")
+        return times[json.dumps(cfg, sort_keys=True)]
+
+    res = tuning.tune(measure, [{"group_m": 16}, {"tile_n": 128}, {"group_m": 64}], "a", "k", path)
+    assert {} in seen                       # the static default is always measured
+    assert res["config"] == {"group_m": 16} and res["ms"] == 4.0 and res["default_ms"] == 5.0
+    assert res["tried"] == 3
+    assert tuning.select("a", "k", None, path) == {"group_m": 16}
+    # when nothing beats the default, the default wins
+    res = tuning.tune(lambda c: 1.0 if c == {} else 2.0, [{"group_m": 8}], "a", "k3", path)
+    assert res["config"] == {} and tuning.select("a", "k3", None, path) == {}
+    # explicit configs win over the cache
+    assert tuning.select("a", "k", {"tile_n": 128}, path) == {"tile_n": 128}
+
+
+def test_candidates():
+    c = tuning.candidates("concurrent", 8, 8192, 8192, 8192, 152, top_k=50)
+    assert c[0] == {}
+    assert any("gemm_ctas" in x for x in c)
+    assert len({json.dumps(x, sort_keys=True) for x in c}) == len(c)
+    r = tuning.candidates("matmul_reduce_scatter", 4, 4096, 4096, 4096, 152, top_k=50)
+    assert {"reduce_mode": 1} in r and {"reduce_mode": 2} in r
+    assert len(tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)) == 3
+
+
+def test_all_tuned_knobs_exist_in_the_config_struct():
+    from gemm_collective_tiles_gb300 import _native
+    names = {f[0] for f in _native.iris_b200_config._fields_}
+    assert set(tuning.TUNABLE) <= names
