@@ -344,6 +344,26 @@ def run_concurrent(args, cfg):
     ms = timeit([fused], steps, warm)
     clocks = sampler.stop()
     del fused
+    # the two-stream mode: GEMM kernel and collective kernel side by side
+    two = make(cfg)
+    s_g, s_c = torch.cuda.Stream(), torch.cuda.Stream()
+    sms_all = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def time_two(gemm_ctas):
+        conf = dict(cfg)
+        conf["gemm_ctas"] = gemm_ctas
+        from gemm_collective_tiles_gb300 import make_config
+        two.config = make_config(**conf)
+        for _ in range(2):
+            two.run_two_stream(s_g, s_c)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            two.run_two_stream(s_g, s_c)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) * 1e3 / steps
+    two_stream = {str(g): time_two(g) for g in (sms_all // 2, int(sms_all * 0.55), int(sms_all * 0.45))}
+    del two
     g_only = make(cfg, coll=False)
     c_only = make(cfg, gemm=False)
     ms_g = timeit([g_only], steps, warm)
@@ -361,6 +381,7 @@ def run_concurrent(args, cfg):
                            "speedup_concurrent_vs_sequential": (ms_g + ms_c) / ms,
                            "gemm_tflops_alone": flops / (ms_g * 1e-3) / 1e12,
                            "all_reduce_gbs_alone": coll_bytes / (ms_c * 1e-3) / 1e9},
+            "two_stream_ms_by_gemm_ctas": two_stream,
             "gpu_launches": steps, "clocks": clocks}
     if args.sweep:
         sms = torch.cuda.get_device_properties(0).multi_processor_count

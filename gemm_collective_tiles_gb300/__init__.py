@@ -46,7 +46,7 @@ from ._native import (  # noqa: F401  (same-name C ABI wrappers)
 __all__ = [
     "SymmetricHeap", "HeapTensor", "Workspace", "make_config", "workspace_size",
     "all_gather_matmul", "matmul_reduce_scatter", "matmul_all_gather", "matmul_all_reduce",
-    "concurrent_gemm_collective", "query_status", "num_sms", "IrisError",
+    "concurrent_gemm_collective", "concurrent_two_stream", "query_status", "num_sms", "IrisError",
 ]
 
 _DT = {torch.float16: _native.IRIS_F16, torch.bfloat16: _native.IRIS_BF16,
@@ -59,7 +59,8 @@ _OPS = {
     "concurrent": _native.IRIS_OP_CONCURRENT,
 }
 _COLL = {"all_gather": _native.IRIS_COLL_ALL_GATHER, "all_reduce": _native.IRIS_COLL_ALL_REDUCE,
-         "reduce_scatter": _native.IRIS_COLL_REDUCE_SCATTER}
+         "reduce_scatter": _native.IRIS_COLL_REDUCE_SCATTER, "all_to_all": _native.IRIS_COLL_ALL_TO_ALL,
+         "broadcast": _native.IRIS_COLL_BROADCAST}
 
 
 def _round_up(x: int, a: int) -> int:
@@ -266,6 +267,30 @@ def concurrent_gemm_collective(A: Optional[torch.Tensor], B: Optional[torch.Tens
                       _DT[x_in.dtype] if x_in is not None else _native.IRIS_F32,
                       _cfgp(config), ws.ptr, ws.nbytes, _stream(stream)))
     return ws
+
+
+def concurrent_two_stream(A, B, C, coll: str, heap, x_in, x_out, gemm_workspace: Workspace,
+                          comm_workspace: Workspace, gemm_stream, comm_stream, config=None):
+    """The two-stream concurrent mode: the GEMM and the collective as two
+    persistent kernels on two streams (disjoint SM sets; cfg gemm_ctas CTAs
+    for the GEMM).  Workspaces are required (one per launch)."""
+    if C is not None:
+        M, N = C.shape
+        K = A.shape[1]
+        gdt = C.dtype
+        a_ptr, b_ptr, c_ptr = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    else:
+        M = N = K = 0
+        gdt = torch.bfloat16
+        a_ptr = b_ptr = c_ptr = None
+    count = x_in.nbytes // torch.empty((), dtype=x_in.dtype).element_size() if x_in is not None else 0
+    hp = ctypes.byref(heap.c_heap()) if heap is not None else None
+    _native.check("iris_b200_concurrent_two_stream", _native.load().iris_b200_concurrent_two_stream(
+        a_ptr, b_ptr, c_ptr, M, N, K, _DT[gdt], _COLL[coll], hp,
+        x_in.offset if x_in is not None else 0, x_out.offset if x_out is not None else 0, count,
+        _DT[x_in.dtype] if x_in is not None else _native.IRIS_F32, _cfgp(config),
+        gemm_workspace.ptr, gemm_workspace.nbytes, comm_workspace.ptr, comm_workspace.nbytes,
+        _stream(gemm_stream), _stream(comm_stream)))
 
 
 def query_status(workspace: Workspace, stream=None):

@@ -26,6 +26,7 @@ IRIS_NOALLOC_SCRATCH_BYTES = 256 + 4 * IRIS_NOALLOC_MAX_FLAGS
 
 IRIS_F16, IRIS_BF16, IRIS_F32 = 0, 1, 2
 IRIS_COLL_ALL_GATHER, IRIS_COLL_ALL_REDUCE, IRIS_COLL_REDUCE_SCATTER = 0, 1, 2
+IRIS_COLL_ALL_TO_ALL, IRIS_COLL_BROADCAST = 3, 4
 (IRIS_OP_ALL_GATHER_MATMUL, IRIS_OP_MATMUL_REDUCE_SCATTER, IRIS_OP_MATMUL_ALL_GATHER,
  IRIS_OP_MATMUL_ALL_REDUCE, IRIS_OP_CONCURRENT) = range(5)
 
@@ -38,6 +39,7 @@ EXPORTS = (
     "iris_b200_matmul_all_gather",
     "iris_b200_matmul_all_reduce",
     "iris_b200_concurrent_gemm_collective",
+    "iris_b200_concurrent_two_stream",
     "iris_b200_query_status",
     "iris_b200_strerror",
     "iris_b200_num_sms",
@@ -61,6 +63,7 @@ class iris_b200_config(ctypes.Structure):
         ("trace_buf", ctypes.c_ulonglong),
         ("trace_cap", ctypes.c_int),
         ("reduce_mode", ctypes.c_int),
+        ("root", ctypes.c_int),
         ("rank_inner", ctypes.c_int),
     ]
 
@@ -89,6 +92,8 @@ def _declare(lib):
         "iris_b200_matmul_all_reduce": (ci, [heapp, sz, sz, sz, sz, i64, i64, i64, ci, cfgp, vp, sz, vp]),
         "iris_b200_concurrent_gemm_collective": (
             ci, [vp, vp, vp, i64, i64, i64, ci, ci, heapp, sz, sz, i64, ci, cfgp, vp, sz, vp]),
+        "iris_b200_concurrent_two_stream": (
+            ci, [vp, vp, vp, i64, i64, i64, ci, ci, heapp, sz, sz, i64, ci, cfgp, vp, sz, vp, sz, vp, vp]),
         "iris_b200_query_status": (ci, [vp, vp, P(ci), P(ci), P(ci)]),
         "iris_b200_strerror": (ctypes.c_char_p, [ci]),
         "iris_b200_num_sms": (ci, [P(ci)]),
@@ -159,6 +164,10 @@ def iris_b200_matmul_all_reduce(*args):
 
 def iris_b200_concurrent_gemm_collective(*args):
     return load().iris_b200_concurrent_gemm_collective(*args)
+
+
+def iris_b200_concurrent_two_stream(*args):
+    return load().iris_b200_concurrent_two_stream(*args)
 
 
 def iris_b200_query_status(*args):

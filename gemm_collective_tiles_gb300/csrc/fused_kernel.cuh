@@ -29,7 +29,7 @@
 namespace gct {
 
 enum : int { OP_AG_MM = 0, OP_MM_RS = 1, OP_MM_AG = 2, OP_MM_AR = 3, OP_CONC = 4 };
-enum : int { COLL_AG = 0, COLL_AR = 1, COLL_RS = 2 };
+enum : int { COLL_AG = 0, COLL_AR = 1, COLL_RS = 2, COLL_A2A = 3, COLL_BC = 4 };
 
 constexpr int BM = 128;           // tile rows (tcgen05 M for cta_group::1)
 constexpr int BK = 64;            // K per stage: 64 x 16-bit = one 128-byte swizzle row
@@ -108,6 +108,7 @@ struct Params {
     void* C;                           // concurrent GEMM output
     long long count;                   // concurrent collective elements per rank
     int comm_block;                    // concurrent elements per comm tile
+    int root;                          // broadcast root rank
     int elem_bytes;
     unsigned long long wait_ns;
     uint32_t debug_skip;               // flag index + 1 that is never released (0 = none)
@@ -1285,32 +1286,59 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
     uint8_t* area = sm.tiles + wc.w * AREA;
     uint64_t* bar = sm.sbar + 2 * wc.w;
     const size_t esz = static_cast<size_t>(p.elem_bytes);
-    // this tile's byte range, per source rank, and the sources / destinations
-    size_t b0, b1;
-    int src_lo, src_n;
-    size_t dst_off_base;  // AG: where rank s's block goes in every output
+    const size_t bytes_per_rank = static_cast<size_t>(p.count) * esz;
+    const size_t chunk = static_cast<size_t>(p.comm_block) * esz;
+    // Item c covers bytes [b0, b1) of a source range.  Sources: src_n regions
+    // starting at src_lo, at src_base + (b - b0).  Destinations: every region
+    // (dst_all), the owning rank's slice (reduce-scatter), or one region.
+    size_t b0, b1, src_base, dst_base;
+    int src_lo, src_n, dst_region = -1;
+    bool dst_all = false;
     if (p.coll == COLL_AG) {
-        const size_t bytes_per_rank = static_cast<size_t>(p.count) * esz;
-        const size_t chunk = static_cast<size_t>(p.comm_block) * esz;
         const size_t chunks = (bytes_per_rank + chunk - 1) / chunk;
         const int s = static_cast<int>(c / chunks);
         b0 = (c - s * chunks) * chunk;
         b1 = min(bytes_per_rank, b0 + chunk);
         src_lo = s;
         src_n = 1;
-        dst_off_base = static_cast<size_t>(s) * bytes_per_rank;
-    } else {
+        src_base = p.off_in + b0;
+        dst_base = p.off_cout + static_cast<size_t>(s) * bytes_per_rank + b0;
+        dst_all = true;
+    } else if (p.coll == COLL_A2A) {
+        // pair (r receives from s): rank s's slice r -> rank r's slot s
+        const size_t sb = bytes_per_rank / p.W;
+        const size_t chunks = (sb + chunk - 1) / chunk;
+        const uint32_t pair = static_cast<uint32_t>(c / chunks);
+        const int r = static_cast<int>(pair / p.W), s = static_cast<int>(pair % p.W);
+        b0 = (c - pair * chunks) * chunk;
+        b1 = min(sb, b0 + chunk);
+        src_lo = s;
+        src_n = 1;
+        src_base = p.off_in + static_cast<size_t>(r) * sb + b0;
+        dst_base = p.off_cout + static_cast<size_t>(s) * sb + b0;
+        dst_region = r;
+    } else if (p.coll == COLL_BC) {
+        b0 = static_cast<size_t>(c) * chunk;
+        b1 = min(bytes_per_rank, b0 + chunk);
+        src_lo = p.root;
+        src_n = 1;
+        src_base = p.off_in + b0;
+        dst_base = p.off_cout + b0;
+        dst_all = true;
+    } else {  // all-reduce, reduce-scatter: fp32 sum over all W sources
         b0 = static_cast<size_t>(c) * p.comm_block * 4;
         b1 = min(static_cast<size_t>(p.count) * 4, b0 + static_cast<size_t>(p.comm_block) * 4);
         src_lo = 0;
         src_n = p.W;
-        dst_off_base = 0;
+        src_base = p.off_in + b0;
+        dst_base = p.off_cout + b0;
+        dst_all = (p.coll == COLL_AR);
     }
-    // the warp's contiguous slice (16-byte granules)
+    // the warp's contiguous slice (16-byte granules) of [b0, b1), as offsets from b0
     const size_t g_tot = (b1 - b0) / 16;
     const size_t g_lo = g_tot * wc.w / NUM_WORKER_WARPS, g_hi = g_tot * (wc.w + 1) / NUM_WORKER_WARPS;
     const uint32_t sub = (HALF / src_n) & ~15u;  // bytes per source per sub-chunk
-    const size_t s_lo = b0 + g_lo * 16, s_hi = b0 + g_hi * 16;
+    const size_t s_lo = g_lo * 16, s_hi = g_hi * 16;
     const int nsub = static_cast<int>((s_hi - s_lo + sub - 1) / sub);
     const size_t cw_bytes = static_cast<size_t>(p.count / p.W) * 4;  // reduce-scatter slice per rank
     auto issue = [&](int i) {
@@ -1320,7 +1348,7 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
         bulk_wait_read_all();  // earlier stores have read this buffer
         mbar_arrive_expect_tx(&bar[i & 1], n * src_n);
         for (int r = 0; r < src_n; ++r)
-            bulk_load(buf + r * sub, p.heap + static_cast<size_t>(src_lo + r) * p.rank_stride + p.off_in + o, n,
+            bulk_load(buf + r * sub, p.heap + static_cast<size_t>(src_lo + r) * p.rank_stride + src_base + o, n,
                       &bar[i & 1]);
     };
     if (nsub > 0 && wc.lane == 0) issue(0);
@@ -1351,19 +1379,21 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
         __syncwarp();
         if (wc.lane == 0) {
             if (p.coll == COLL_RS) {
-                // o..o+n may cross a rank boundary: split the store there
+                // the item may cross a rank boundary: split the store there
                 size_t done = 0;
                 while (done < n) {
-                    const size_t e = o + done;
+                    const size_t e = b0 + o + done;  // byte index into the summed vector
                     const int rr = static_cast<int>(e / cw_bytes);
                     const size_t piece = min(static_cast<size_t>(n) - done, (rr + 1) * cw_bytes - e);
                     bulk_store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
                                buf + done, static_cast<uint32_t>(piece));
                     done += piece;
                 }
-            } else {
+            } else if (dst_all) {
                 for (int r = 0; r < p.W; ++r)
-                    bulk_store(p.heap + static_cast<size_t>(r) * p.rank_stride + p.off_cout + dst_off_base + o, buf, n);
+                    bulk_store(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + o, buf, n);
+            } else {
+                bulk_store(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base + o, buf, n);
             }
             bulk_commit();
         }

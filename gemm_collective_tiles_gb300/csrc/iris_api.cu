@@ -96,6 +96,7 @@ struct Cfg {
     int tile_n, group_m, gemm_ctas, comm_block, replicate, bias_on_m, grid;
     unsigned long long wait_ns;
     uint32_t debug_skip;
+    int root;
     unsigned long long* trace;
     int trace_cap;
     int reduce_mode;  // resolved by the reduce ops (resolve_reduce_mode)
@@ -126,11 +127,13 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->gemm_ctas < -1 || c->gemm_ctas > out.grid) return IRIS_EINVAL;
     if (c->gemm_ctas != 0)
         out.gemm_ctas = c->gemm_ctas;
-    else
-        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? -1 : out.grid;
+    else  // concurrent: 55% of the CTAs prefer the GEMM (measured best split); others: all
+        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? std::max(1, (out.grid * 55 + 50) / 100) : out.grid;
     out.wait_ns = c->wait_ns ? c->wait_ns : DEFAULT_WAIT_NS;
     if (c->debug_skip_flag < 0) return IRIS_EINVAL;
     out.debug_skip = static_cast<uint32_t>(c->debug_skip_flag);
+    if (c->root < 0 || c->root >= IRIS_MAX_WORLD) return IRIS_EINVAL;
+    out.root = c->root;
     if (c->trace_buf && (c->trace_cap < 2 || (c->trace_buf & 7))) return IRIS_EINVAL;
     out.trace = reinterpret_cast<unsigned long long*>(c->trace_buf);
     out.trace_cap = c->trace_buf ? c->trace_cap : 0;
@@ -510,11 +513,12 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     return launch(p, c, stream);
 }
 
-int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                                         iris_dtype gemm_dtype, iris_coll coll, const iris_b200_heap* heap,
-                                         size_t off_in, size_t off_out, int64_t count, iris_dtype coll_dtype,
-                                         const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
-                                         cudaStream_t stream) {
+// part: 0 = GEMM and collective in one launch; 1 = the GEMM alone on `grid`
+// CTAs; 2 = the collective alone on `grid` CTAs (two-stream mode).
+static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                           iris_dtype gemm_dtype, iris_coll coll, const iris_b200_heap* heap, size_t off_in,
+                           size_t off_out, int64_t count, iris_dtype coll_dtype, const iris_b200_config* cfg,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream, int part, int grid) {
     if (!dims_ok(M, N, K) || count < 0) return IRIS_EINVAL;
     if (gemm_dtype != IRIS_F16 && gemm_dtype != IRIS_BF16) return IRIS_EINVAL;
     const bool has_gemm = M > 0 && N > 0;
@@ -531,25 +535,32 @@ int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, 
     if (count > 0) {
         if ((rc = check_heap(heap))) return rc;
         W = heap->world;
-        if (coll != IRIS_COLL_ALL_GATHER && coll != IRIS_COLL_ALL_REDUCE && coll != IRIS_COLL_REDUCE_SCATTER)
-            return IRIS_EINVAL;
-        if (coll == IRIS_COLL_ALL_GATHER) {
+        if (coll < IRIS_COLL_ALL_GATHER || coll > IRIS_COLL_BROADCAST) return IRIS_EINVAL;
+        const bool sums = (coll == IRIS_COLL_ALL_REDUCE || coll == IRIS_COLL_REDUCE_SCATTER);
+        if (sums) {
+            if (coll_dtype != IRIS_F32) return IRIS_EUNSUPPORTED;
+        } else {
+            // pure data movement: any element type, moved as bytes
             esz = (coll_dtype == IRIS_F32) ? 4 : (coll_dtype == IRIS_F16 || coll_dtype == IRIS_BF16) ? 2 : 0;
             if (!esz) return IRIS_EINVAL;
-        } else if (coll_dtype != IRIS_F32) {
-            return IRIS_EUNSUPPORTED;
         }
         if ((count * esz) % 16 != 0) return IRIS_EALIGN;
         if (coll == IRIS_COLL_REDUCE_SCATTER && count % (4 * W) != 0) return IRIS_EALIGN;
+        if (coll == IRIS_COLL_ALL_TO_ALL && (count % W != 0 || ((count / W) * esz) % 16 != 0)) return IRIS_EALIGN;
     }
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_CONCURRENT, N, c))) return rc;
+    if (part != 0) {
+        c.grid = grid;
+        c.gemm_ctas = part == 1 ? grid : 0;
+    }
     if (count > 0) {
         if (size_t(c.comm_block) * esz % 16 != 0) return IRIS_EALIGN;
         const size_t in_bytes = size_t(count) * esz;
-        const size_t out_bytes = coll == IRIS_COLL_ALL_GATHER   ? in_bytes * W
-                                 : coll == IRIS_COLL_ALL_REDUCE ? in_bytes
-                                                                : in_bytes / W;
+        const size_t out_bytes = coll == IRIS_COLL_ALL_GATHER      ? in_bytes * W
+                                 : coll == IRIS_COLL_REDUCE_SCATTER ? in_bytes / W
+                                                                    : in_bytes;
+        if (coll == IRIS_COLL_BROADCAST && c.root >= W) return IRIS_EINVAL;
         if ((rc = check_region(heap, off_in, in_bytes))) return rc;
         if ((rc = check_region(heap, off_out, out_bytes))) return rc;
         // an in-place collective must use the same offsets exactly; partial overlap is refused
@@ -562,13 +573,18 @@ int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, 
     p.op = OP_CONC;
     p.W = W;
     p.bf16 = gemm_dtype == IRIS_BF16;
-    p.coll = coll == IRIS_COLL_ALL_GATHER ? COLL_AG : coll == IRIS_COLL_ALL_REDUCE ? COLL_AR : COLL_RS;
+    p.coll = coll == IRIS_COLL_ALL_GATHER      ? COLL_AG
+             : coll == IRIS_COLL_ALL_REDUCE    ? COLL_AR
+             : coll == IRIS_COLL_REDUCE_SCATTER ? COLL_RS
+             : coll == IRIS_COLL_ALL_TO_ALL    ? COLL_A2A
+                                               : COLL_BC;
+    p.root = c.root;
     const int mblocks = static_cast<int>(cdiv(M, BM));
     fill_geometry(p, M, N, K, mblocks, c);
     p.mb_per_rank = mblocks;
     p.C = C;
-    p.n_gemm = has_gemm ? static_cast<uint32_t>(p.n_tiles) : 0u;
-    if (count > 0) {
+    p.n_gemm = (has_gemm && part != 2) ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    if (count > 0 && part != 1) {
         p.heap = static_cast<char*>(heap->base);
         p.rank_stride = heap->rank_stride;
         p.off_in = off_in;
@@ -577,7 +593,9 @@ int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, 
         p.comm_block = c.comm_block;
         p.elem_bytes = esz;
         const int64_t chunks = cdiv(count, c.comm_block);
-        const int64_t items = (coll == IRIS_COLL_ALL_GATHER) ? chunks * W : chunks;
+        const int64_t items = coll == IRIS_COLL_ALL_GATHER  ? chunks * W
+                              : coll == IRIS_COLL_ALL_TO_ALL ? int64_t(W) * W * cdiv(count / W, c.comm_block)
+                                                              : chunks;
         if (items >= 0x7FFFFFFF) return IRIS_EINVAL;
         p.n_comm = static_cast<uint32_t>(items);
     }
@@ -590,6 +608,44 @@ int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, 
                                            size_t(M) * N * 2)))
         return rc;
     return launch(p, c, stream);
+}
+
+int iris_b200_concurrent_gemm_collective(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                         iris_dtype gemm_dtype, iris_coll coll, const iris_b200_heap* heap,
+                                         size_t off_in, size_t off_out, int64_t count, iris_dtype coll_dtype,
+                                         const iris_b200_config* cfg, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    return concurrent_impl(A, B, C, M, N, K, gemm_dtype, coll, heap, off_in, off_out, count, coll_dtype, cfg,
+                           workspace, workspace_bytes, stream, 0, 0);
+}
+
+int iris_b200_concurrent_two_stream(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                    iris_dtype gemm_dtype, iris_coll coll, const iris_b200_heap* heap,
+                                    size_t off_in, size_t off_out, int64_t count, iris_dtype coll_dtype,
+                                    const iris_b200_config* cfg, void* gemm_workspace, size_t gemm_workspace_bytes,
+                                    void* comm_workspace, size_t comm_workspace_bytes, cudaStream_t gemm_stream,
+                                    cudaStream_t comm_stream) {
+    int sms = 0;
+    if (num_sms_current(&sms) != IRIS_OK) return IRIS_ECUDA;
+    const int total = (cfg && cfg->grid) ? cfg->grid : sms;
+    if (total < 2 || total > sms) return IRIS_EINVAL;
+    int gemm_grid = (cfg && cfg->gemm_ctas > 0) ? cfg->gemm_ctas : total / 2;
+    if (gemm_grid >= total) return IRIS_EINVAL;
+    const bool has_gemm = M > 0 && N > 0, has_coll = count > 0;
+    if (!has_gemm) gemm_grid = 0;
+    if (!has_coll) gemm_grid = total;
+    if (gemm_workspace == comm_workspace && has_gemm && has_coll) return IRIS_EINVAL;  // each launch owns its queues
+    int rc = IRIS_OK;
+    if (has_gemm) {
+        rc = concurrent_impl(A, B, C, M, N, K, gemm_dtype, coll, heap, off_in, off_out, 0, coll_dtype, cfg,
+                             gemm_workspace, gemm_workspace_bytes, gemm_stream, 1, gemm_grid);
+        if (rc) return rc;
+    }
+    if (has_coll)
+        rc = concurrent_impl(nullptr, nullptr, nullptr, 0, 0, 0, gemm_dtype, coll, heap, off_in, off_out, count,
+                             coll_dtype, cfg, comm_workspace, comm_workspace_bytes, comm_stream, 2,
+                             total - gemm_grid);
+    return rc;
 }
 
 int iris_b200_query_status(void* workspace, cudaStream_t stream, int* device_status, int* where, int* index) {

@@ -10,8 +10,8 @@ from typing import Dict, List, Optional
 import torch
 
 from . import (HeapTensor, SymmetricHeap, Workspace, all_gather_matmul, concurrent_gemm_collective,
-               make_config, matmul_all_gather, matmul_all_reduce, matmul_reduce_scatter,
-               workspace_size)
+               concurrent_two_stream, make_config, matmul_all_gather, matmul_all_reduce,
+               matmul_reduce_scatter, workspace_size)
 
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 OPS = ("ag_mm", "mm_rs", "mm_ag", "mm_ar")
@@ -179,6 +179,14 @@ class ConcurrentProblem:
     def run(self, stream=None):
         concurrent_gemm_collective(self.A, self.B, self.C, self.coll, self.heap, self.x_in, self.x_out,
                                    self.config, self.ws, stream)
+
+    def run_two_stream(self, gemm_stream, comm_stream):
+        """The two-kernel mode: GEMM on gemm_stream, the collective on
+        comm_stream (config gemm_ctas CTAs for the GEMM)."""
+        if not hasattr(self, "ws2"):
+            self.ws2 = Workspace(self.ws.nbytes, self.ws.buf.device)
+        concurrent_two_stream(self.A, self.B, self.C, self.coll, self.heap, self.x_in, self.x_out,
+                              self.ws, self.ws2, gemm_stream, comm_stream, self.config)
 
     def outputs(self):
         res = {}

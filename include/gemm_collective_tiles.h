@@ -77,7 +77,9 @@ typedef enum { IRIS_F16 = 0, IRIS_BF16 = 1, IRIS_F32 = 2 } iris_dtype;
 typedef enum {
     IRIS_COLL_ALL_GATHER = 0,
     IRIS_COLL_ALL_REDUCE = 1,
-    IRIS_COLL_REDUCE_SCATTER = 2
+    IRIS_COLL_REDUCE_SCATTER = 2,
+    IRIS_COLL_ALL_TO_ALL = 3,
+    IRIS_COLL_BROADCAST = 4
 } iris_coll;
 
 typedef enum {
@@ -93,12 +95,13 @@ typedef struct {
     int tile_m;            /* GEMM tile rows: 128 (only value) */
     int tile_n;            /* GEMM tile columns: 128 or 256 (default 256) */
     int tile_k;            /* K step per pipeline stage: 64 (only value) */
-    int group_m;           /* GROUP_M tile swizzle width in M blocks (default 8) */
+    int group_m;           /* GROUP_M tile swizzle width in M blocks (default 32) */
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
-                              other queue when its own runs dry.  0 = op default;
-                              -1 = balanced (every CTA draws from both queues so
-                              that both finish together). */
+                              other queue when its own runs dry.  0 = op default
+                              (concurrent: 55% of the grid; the dependent ops: all
+                              CTAs); -1 = balanced (every CTA draws from both queues
+                              so that both finish together). */
     int stages;            /* reserved: pipeline depth is fixed per tile_n */
     int comm_block;        /* concurrent mode: elements per comm tile (default 65536) */
     int replicate_outputs; /* 1: also write the W-1 identical copies of replicated
@@ -129,6 +132,7 @@ typedef struct {
                                   tile on; the last rank writes the rounded output
                                   (a per-tile ring reduction; workspace holds one M x N
                                   fp32 sum instead of W partials) */
+    int root;              /* concurrent broadcast: source rank (default 0) */
     int rank_inner;        /* reduce ops: 1 = order GEMM tiles with the rank index
                               fastest; 0 (default) = rank by rank inside each GROUP_M
                               group, so one rank's operands share the L2 at a time */
@@ -236,6 +240,9 @@ IRIS_API int iris_b200_matmul_all_reduce(const iris_b200_heap* heap, size_t off_
  *     IRIS_COLL_REDUCE_SCATTER (IRIS_F32)  out_r[i] = (sum_s in_s)[r*count/W + i];
  *                              count % (4W) == 0.
  *     IRIS_COLL_ALL_GATHER     (any type)  out_r[s*count + i] = in_s[i] for every r.
+ *     IRIS_COLL_ALL_TO_ALL     (any type)  each buffer is W chunks of count/W elements:
+ *                              out_r[s*count/W + i] = in_s[r*count/W + i]; count % W == 0.
+ *     IRIS_COLL_BROADCAST      (any type)  out_r[i] = in_root[i] for every r (cfg->root).
  *   count      elements per rank's input (0 runs the GEMM alone); count *
  *              element size must be a multiple of 16 bytes.
  */
@@ -246,6 +253,25 @@ IRIS_API int iris_b200_concurrent_gemm_collective(const void* A, const void* B, 
                                          iris_dtype coll_dtype, const iris_b200_config* cfg,
                                          void* workspace, size_t workspace_bytes,
                                          cudaStream_t stream);
+
+/*
+ * Two-stream concurrent mode -- ROCm/iris PR #544 (mode="concurrent": the
+ * GEMM and the collective as separate persistent kernels on different
+ * streams).  Same operands and semantics as iris_b200_concurrent_gemm_collective;
+ * the GEMM kernel runs on cfg->gemm_ctas CTAs (default half of cfg->grid or of
+ * the SMs) on `gemm_stream`, the collective kernel on the remaining CTAs on
+ * `comm_stream`.  Each kernel holds one CTA per SM, so the two run side by
+ * side on disjoint SMs.  Each launch needs its own workspace (of
+ * iris_b200_workspace_size(IRIS_OP_CONCURRENT, ...) bytes); the caller orders
+ * later work after both streams.
+ */
+IRIS_API int iris_b200_concurrent_two_stream(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                             int64_t K, iris_dtype gemm_dtype, iris_coll coll,
+                                             const iris_b200_heap* heap, size_t off_in, size_t off_out,
+                                             int64_t count, iris_dtype coll_dtype, const iris_b200_config* cfg,
+                                             void* gemm_workspace, size_t gemm_workspace_bytes,
+                                             void* comm_workspace, size_t comm_workspace_bytes,
+                                             cudaStream_t gemm_stream, cudaStream_t comm_stream);
 
 /*
  * all_gather_matmul without a caller-provided workspace.  This entry point

@@ -49,4 +49,6 @@ from .reference import (  # noqa: F401
     all_reduce,
     all_gather,
     reduce_scatter,
+    all_to_all,
+    broadcast,
 )

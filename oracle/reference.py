@@ -283,6 +283,7 @@ def matmul_all_reduce_at(A_ranks, B_ranks, bias, ii, jj, bias_on_m: bool = False
 
 # --------------------------------------------------------------------------
 # Concurrent mode (ROCm/iris PR #544): an independent GEMM and a collective
+# (all_gather / all_reduce / reduce_scatter / all_to_all / broadcast)
 # --------------------------------------------------------------------------
 
 def gemm(A: torch.Tensor, B: torch.Tensor) -> np.ndarray:
@@ -316,6 +317,30 @@ def all_gather(X: Sequence[torch.Tensor]) -> np.ndarray:
         out[off:off + p.size] = p
         off += p.size
     return out
+
+
+def all_to_all(X: Sequence[torch.Tensor]) -> List[np.ndarray]:
+    """all_to_all of W buffers of ``count`` elements (count divisible by W):
+    each buffer is W contiguous chunks; rank r receives chunk r of every rank,
+    rank s's chunk at position s: out_r[s*c + i] = X_s[r*c + i].  Returned as
+    raw bytes of the element type."""
+    W = len(X)
+    parts = [x.detach().contiguous().view(torch.uint8).numpy() for x in X]
+    cb = parts[0].size // W
+    outs = []
+    for r in range(W):
+        o = np.empty(W * cb, dtype=np.uint8)
+        for s in range(W):
+            o[s * cb:(s + 1) * cb] = parts[s][r * cb:(r + 1) * cb]
+        outs.append(o)
+    return outs
+
+
+def broadcast(X: Sequence[torch.Tensor], root: int = 0) -> List[np.ndarray]:
+    """broadcast of rank ``root``'s buffer: every rank receives a copy of it.
+    Returned as raw bytes of the element type."""
+    src = X[root].detach().contiguous().view(torch.uint8).numpy()
+    return [src.copy() for _ in X]
 
 
 def reduce_scatter(X: Sequence[torch.Tensor]) -> List[np.ndarray]:

@@ -126,3 +126,31 @@ def test_config_builder_rejects_unknown_keys():
     assert c.tile_n == 128 and c.gemm_ctas == -1 and c.wait_ns == 10**6
     with pytest.raises(KeyError):
         gct.make_config(bogus=1)
+
+
+def test_ctypes_structs_match_the_c_header(tmp_path):
+    """Compile a probe against the header with the host C compiler and compare
+    every field offset and the struct sizes with the ctypes mirrors."""
+    fields = [f[0] for f in N.iris_b200_config._fields_]
+    src = ['#include <stdio.h>', '#include <stddef.h>', '#include "gemm_collective_tiles.h"', 'int main(void) {',
+           'printf("cfg %zu\\n", sizeof(iris_b200_config));', 'printf("heap %zu\\n", sizeof(iris_b200_heap));']
+    for f in fields:
+        src.append(f'printf("{f} %zu\\n", offsetof(iris_b200_config, {f}));')
+    for f in ("base", "rank_stride", "world"):
+        src.append(f'printf("heap.{f} %zu\\n", offsetof(iris_b200_heap, {f}));')
+    src.append("return 0; }")
+    c = tmp_path / "probe.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "probe"
+    cuda_inc = "/usr/local/cuda/include"
+    r = subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(c), "-o", str(exe)],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("no host C compiler with the CUDA headers: " + r.stderr[:200])
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    assert int(out["cfg"]) == ctypes.sizeof(N.iris_b200_config)
+    assert int(out["heap"]) == ctypes.sizeof(N.iris_b200_heap)
+    for f in fields:
+        assert int(out[f]) == getattr(N.iris_b200_config, f).offset, f
+    for f in ("base", "rank_stride", "world"):
+        assert int(out["heap." + f]) == getattr(N.iris_b200_heap, f).offset, f

@@ -230,6 +230,65 @@ def test_concurrent_collective_bit_exact(coll, gemm_ctas):
             assert np.array_equal(out["x"][r].contiguous().view(torch.uint8).numpy(), want)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_concurrent_all_to_all_and_broadcast_bit_exact(dt):
+    W = 8
+    count = W * (3 * 4096 + 512)     # per-rank slices of 12800 elements
+    M, N, K = 256, 384, 192
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=65, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, dt, seed=66)
+    want_a2a = oracle.all_to_all(X)
+    prob = ConcurrentProblem(M, N, K, "bf16", "all_to_all", W, count, coll_dtype=dt,
+                             config={"comm_block": 4096, "gemm_ctas": 60})
+    prob.upload(A, B, X)
+    prob.poison_outputs()
+    prob.run()
+    torch.cuda.synchronize()
+    out = prob.outputs()
+    assert_exact(bits(out["C"]), oracle.gemm(A, B))
+    for r in range(W):
+        assert np.array_equal(out["x"][r].contiguous().view(torch.uint8).numpy(), want_a2a[r]), r
+    for root in (0, 5):
+        prob = ConcurrentProblem(0, 0, 0, "bf16", "broadcast", W, count, coll_dtype=dt,
+                                 config={"comm_block": 8192, "root": root})
+        prob.upload(X=X)
+        prob.poison_outputs()
+        prob.run()
+        torch.cuda.synchronize()
+        want = oracle.broadcast(X, root)
+        for r in range(W):
+            assert np.array_equal(prob.outputs()["x"][r].contiguous().view(torch.uint8).numpy(), want[r])
+
+
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter", "all_gather", "all_to_all", "broadcast"])
+def test_two_stream_mode_bit_exact(coll):
+    """The GEMM and the collective as two kernels on two streams."""
+    W, count = 8, 8 * 16384
+    M, N, K = 384, 512, 256
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=67, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=68)
+    prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count, config={"comm_block": 8192, "gemm_ctas": 40})
+    prob.upload(A, B, X)
+    prob.poison_outputs()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    prob.run_two_stream(s1, s2)
+    torch.cuda.synchronize()
+    from gemm_collective_tiles_gb300 import query_status
+    assert query_status(prob.ws)[0] == 0 and query_status(prob.ws2)[0] == 0
+    out = prob.outputs()
+    assert_exact(bits(out["C"]), oracle.gemm(A, B))
+    want = {"all_reduce": lambda: [oracle.all_reduce(X)] * W,
+            "reduce_scatter": lambda: oracle.reduce_scatter(X),
+            "all_gather": lambda: [oracle.all_gather(X)] * W,
+            "all_to_all": lambda: oracle.all_to_all(X),
+            "broadcast": lambda: oracle.broadcast(X, 0)}[coll]()
+    for r in range(W):
+        got = out["x"][r].contiguous().view(torch.uint8).numpy()
+        w = want[r] if want[r].dtype == np.uint8 else want[r].view(np.uint8)
+        assert np.array_equal(got, w), r
+
+
 def test_concurrent_all_reduce_in_place_and_alone():
     W, count = 4, 100000
     X = synthetic.make_coll_inputs(W, count, "f32", seed=63)

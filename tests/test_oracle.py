@@ -376,3 +376,28 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     monkeypatch.setattr(ref, "round_bf16_bits", away)
     assert fails(test_rne16_golden_cases)
     monkeypatch.undo()
+
+
+def test_all_to_all_golden_and_involution():
+    g = _load("all_to_all_small.json")
+    X = [torch.tensor(b, dtype=torch.float32) for b in g["buffers"]]
+    outs = oracle.all_to_all(X)
+    for o, want in zip(outs, g["expected"]):
+        assert o.view(np.float32).tolist() == [float(v) for v in want]
+    # applying all_to_all twice gives the inputs back (a block transpose)
+    Y = synthetic.make_coll_inputs(4, 64, "bf16", seed=91)
+    once = [torch.from_numpy(o.copy()).view(torch.bfloat16) for o in oracle.all_to_all(Y)]
+    twice = oracle.all_to_all(once)
+    for a, b in zip(twice, Y):
+        assert np.array_equal(a, b.view(torch.uint8).numpy())
+
+
+def test_broadcast_matches_gather_block():
+    W, count = 4, 40
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=92)
+    for root in range(W):
+        outs = oracle.broadcast(X, root)
+        ag = oracle.all_gather(X)
+        blk = ag[root * count * 4:(root + 1) * count * 4]
+        for o in outs:
+            assert np.array_equal(o, blk)
