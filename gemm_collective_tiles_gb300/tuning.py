@@ -77,7 +77,8 @@ def record(arch: str, key: str, config: dict, ms: float, default_ms: float, path
     return save_db(db, path)
 
 
-def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: int = 8) -> List[dict]:
+def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: int = 8,
+               coll: str = "all_reduce", count: int = 0) -> List[dict]:
     """Ranked candidate configs (the static default, {}, is always first).
 
     Ranking rule (from the measurements behind the defaults): the swizzle
@@ -92,8 +93,15 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     if op in ("matmul_reduce_scatter", "matmul_all_reduce"):
         out += [{"reduce_mode": 2}, {"reduce_mode": 1}, {"group_m": 64, "reduce_mode": 3}]
     if op == "concurrent":
-        for frac in (0.55, 0.45, 0.65, 0.35, 0.75):
-            out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
+        if count > 0:
+            # splits ranked by the work-stealing makespan model
+            from . import predictor
+            wl = predictor.Workload(M=M, N=N, K=K, coll=coll, W=W, count=count)
+            for d in predictor.predict_split(wl, m=predictor.Machine(sms=sm_count), top_k=4):
+                out.insert(1, {"gemm_ctas": d["gemm_ctas"]})
+        else:
+            for frac in (0.55, 0.45, 0.65, 0.35, 0.75):
+                out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
     # drop duplicates, keep order
     seen, uniq = set(), []
     for c in out:

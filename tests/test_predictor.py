@@ -1,0 +1,67 @@
+"""The concurrent-mode split predictor: cost model and work-stealing makespan
+simulator against closed forms and invariants.  CPU."""
+import math
+
+import pytest
+
+from gemm_collective_tiles_gb300 import predictor as P
+from gemm_collective_tiles_gb300 import tuning
+
+
+def test_gemm_only_makespan_is_waves_times_tile_time():
+    m = P.Machine(sms=10, tile_overhead_us=0.0)
+    wl = P.Workload(M=128 * 5, N=256 * 7, K=1024, count=0)           # 35 tiles
+    t_tile = 2 * 128 * 256 * 1024 / (m.gemm_tflops_per_sm * 1e12) * 1e6
+    assert P.simulate(wl, gemm_ctas=10, m=m) == pytest.approx(math.ceil(35 / 10) * t_tile)
+    # a CTA split does not matter without collective work (everyone spills)
+    assert P.simulate(wl, gemm_ctas=3, m=m) == pytest.approx(math.ceil(35 / 10) * t_tile)
+
+
+def test_comm_only_makespan_is_bandwidth_bound():
+    m = P.Machine(sms=152, tile_overhead_us=0.0)
+    wl = P.Workload(M=0, N=0, K=0, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    total = wl.comm_tiles() * wl.comm_tile_bytes()
+    assert total == pytest.approx(2 * 8 * 64 * 1024 * 1024 * 4)
+    bound = total / (min(m.hbm_gbs, m.sms * m.comm_gbs_per_sm) * 1e9) * 1e6
+    t = P.simulate(wl, gemm_ctas=0, m=m)
+    assert bound <= t <= bound * 1.1
+
+
+def test_tile_bytes_per_collective():
+    wl = P.Workload(M=0, N=0, K=0, W=4, count=1 << 20, comm_block=1024, elem_bytes=4)
+    for coll, want in (("all_reduce", 2 * 4 * 1024 * 4), ("reduce_scatter", 5 * 1024 * 4),
+                       ("all_gather", 5 * 1024 * 4), ("broadcast", 5 * 1024 * 4), ("all_to_all", 2 * 1024 * 4)):
+        wl.coll = coll
+        assert wl.comm_tile_bytes() == want, coll
+    wl.coll = "all_gather"
+    assert wl.comm_tiles() == 4 * 1024
+    wl.coll = "all_to_all"
+    assert wl.comm_tiles() == 16 * 256
+
+
+def test_best_split_beats_sequential_and_respects_the_floor():
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    ranked = P.predict_split(wl, top_k=10)
+    assert ranked == sorted(ranked, key=lambda d: d["us"])
+    assert ranked[0]["us"] < P.sequential_us(wl)
+    floor = P.comm_floor("all_reduce")
+    assert floor == 16 and P.comm_floor("all_gather") == 1
+    assert all(152 - d["gemm_ctas"] >= floor for d in ranked)
+
+
+def test_calibration_close_to_measurements():
+    """GB300 measurements of this library: GEMM 8192^3 alone 0.69-0.70 ms,
+    all-reduce 8 x 64Mi fp32 alone 0.72-0.75 ms."""
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    g = P.simulate(P.Workload(M=8192, N=8192, K=8192, count=0), 152)
+    c = P.simulate(P.Workload(M=0, N=0, K=0, coll="all_reduce", W=8, count=64 * 1024 * 1024), 0)
+    assert 0.6e3 < g < 0.9e3
+    assert 0.6e3 < c < 0.9e3
+    assert P.sequential_us(wl) == pytest.approx(g + c)
+
+
+def test_tuning_candidates_use_the_predictor():
+    c = tuning.candidates("concurrent", 8, 8192, 8192, 8192, 152, top_k=6, coll="all_reduce",
+                          count=64 * 1024 * 1024)
+    assert c[0] == {}
+    assert sum("gemm_ctas" in x for x in c) >= 3
