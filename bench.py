@@ -402,6 +402,91 @@ def run_concurrent(args, cfg):
     return 0
 
 
+def run_shape_sweep(args, cfg):
+    """all_gather_matmul at W=8 over the PR #506 shape list (bf16, N(0, 0.02)
+    drawn on the device, seed 7 + shape index), each against the sequential
+    path it replaces: the gather as one torch.cat of the W K-shards, then a
+    cuBLAS matmul.  Prints one JSON row per shape, then a summary line.
+    Both arms write into the same region-0 buffers; the fused output of a
+    sampled row block is compared with cuBLAS's before the latter overwrites it."""
+    from gemm_collective_tiles_gb300 import query_status
+    from gemm_collective_tiles_gb300.runner import FusedProblem
+    torch.cuda.set_device(0)
+    W = 8
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    only = set(args.shapes.split(",")) if args.shapes else None
+    rows = []
+
+    def timed(fn, reps, warm=2):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    for idx, (label, M, N, K) in enumerate(synthetic.AG_MM_SHAPES):
+        if only and label not in only:
+            continue
+        per_region = (M * (K // W) + K * N + M * N + M * K) * 2
+        free, _total = torch.cuda.mem_get_info()
+        if W * per_region > 0.92 * free:
+            rows.append({"shape": label, "M": M, "N": N, "K": K, "skipped": f"needs {W * per_region / 1e9:.1f} GB"})
+            print(json.dumps(rows[-1]), flush=True)
+            continue
+        prob = FusedProblem("ag_mm", W, M, N, K, "bf16", config=cfg)
+        for r in range(W):
+            synthetic.fill_device_(prob.heap.view(prob.A, r), 7 + idx * 16 + r)
+        synthetic.fill_device_(prob.heap.view(prob.B, 0), 7 + idx * 16 + W)
+        flops = 2.0 * M * N * K
+        reps = max(3, min(20, int(2e16 / flops)))
+        t0 = time.perf_counter()
+        ms_fused = timed(lambda: prob.run(stream), reps)
+        rc = query_status(prob.ws, stream)
+        if rc[0] != 0:
+            raise RuntimeError(f"{label}: device status {rc}")
+        out0 = prob.heap.view(prob.out, 0)
+        gath0 = prob.heap.view(prob.gathered, 0)
+        r0 = (M // 2) // 128 * 128
+        fused_rows = out0[r0:r0 + 128].float().cpu()
+        shards = [prob.heap.view(prob.A, r) for r in range(W)]
+        B0 = prob.heap.view(prob.B, 0)
+
+        def seq():
+            torch.cat(shards, dim=1, out=gath0)
+            torch.matmul(gath0, B0, out=out0)
+        ms_seq = timed(seq, reps)
+        ref_rows = out0[r0:r0 + 128].float().cpu()
+        rel = float((fused_rows - ref_rows).abs().max() / ref_rows.abs().max().clamp_min(1e-30))
+        tf = flops / (ms_fused * 1e-3) / 1e12
+        rows.append({"shape": label, "M": M, "N": N, "K": K, "ms": ms_fused, "tflops": tf,
+                     "frac_of_peak": tf / peak, "cat_cublas_ms": ms_seq,
+                     "cat_cublas_tflops": flops / (ms_seq * 1e-3) / 1e12, "speedup": ms_seq / ms_fused,
+                     "max_rel_diff_vs_cublas": rel, "reps": reps, "wall_s": time.perf_counter() - t0})
+        print(json.dumps(rows[-1]), flush=True)
+        del prob, shards, B0, out0, gath0
+        torch.cuda.empty_cache()
+    done = [r for r in rows if "tflops" in r]
+    print(json.dumps({"metric": "all_gather_matmul W=8 shape sweep (bf16): TFLOP/s and speedup vs torch.cat + cuBLAS",
+                      "unit": "TFLOP/s", "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+                      "peak": peak, "peak_source": f"{peak_kind} bf16 burst",
+                      "config": {"workload": "ag_mm_shape_sweep", **cfg},
+                      "shapes": len(done), "winners": sum(1 for r in done if r["speedup"] > 1.0),
+                      "geomean_speedup": statistics.geometric_mean([r["speedup"] for r in done]) if done else None}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,7 +494,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(synthetic.WORKLOADS) + ["concurrent_ar_w8"])
+                    choices=sorted(synthetic.WORKLOADS) + ["concurrent_ar_w8", "ag_mm_shape_sweep"])
+    ap.add_argument("--shapes", default="", help="ag_mm_shape_sweep: comma-separated labels (default all)")
     ap.add_argument("--sweep", action="store_true",
                     help="concurrent workload: also time gemm_ctas from 25%% to 90%% of the SMs")
     ap.add_argument("--config", default="{}", help="JSON dict of iris_b200_config fields")
@@ -423,6 +509,11 @@ def main():
             print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the fused-op workloads"}))
             return 0
         return run_concurrent(args, cfg)
+    if args.workload == "ag_mm_shape_sweep":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the shape sweep compares against cuBLAS, not the oracle"}))
+            return 0
+        return run_shape_sweep(args, cfg)
     wl = dict(synthetic.WORKLOADS[args.workload])
 
     if args.impl == "reference":
@@ -490,31 +581,60 @@ def main():
                 "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json) x 1.0 fp16/bf16 nominal ratio",
                 "kernel": KERNEL_NAME, "median_ms": statistics.median(step_ms)}
 
-    # end to end: pinned host inputs -> heap, fused op, outputs -> pinned host
+    # end to end: pinned host inputs -> heap, fused op, outputs -> pinned host,
+    # every step.  Two problem instances alternate so that step i's uploads
+    # (copy stream) overlap step i-1's kernel and step i-2's download, the
+    # way a serving loop double-buffers its inputs.
     pin_A = [a.pin_memory() for a in x.A]
     pin_B = [b.pin_memory() for b in x.B]
     pin_bias = x.bias.pin_memory() if x.bias is not None else None
-    out_views = [prob.heap.view(prob.out, r) for r in range(wl["W"])] if wl["op"] == "mm_rs" else \
-        [prob.heap.view(prob.out, 0)]
-    host_out = [torch.empty(v.shape, dtype=v.dtype).pin_memory() for v in out_views]
+    prob2 = FusedProblem(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"], wl["dtype"], bias=wl.get("bias", False),
+                         config=cfg)
+    probs = [prob, prob2]
+
+    def out_views(p):
+        return [p.heap.view(p.out, r) for r in range(wl["W"])] if wl["op"] == "mm_rs" else [p.heap.view(p.out, 0)]
+    host_out = [[torch.empty(v.shape, dtype=v.dtype).pin_memory() for v in out_views(p)] for p in probs]
     h2d = prob.input_bytes()
-    d2h = sum(v.numel() * v.element_size() for v in out_views)
+    d2h = sum(v.numel() * v.element_size() for v in out_views(prob))
+    up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in probs]
+    ev_run = [torch.cuda.Event() for _ in probs]
+    ev_down = [torch.cuda.Event() for _ in probs]
+    for e in ev_run + ev_down:
+        e.record(stream)
     E = max(3, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     for i in range(3 + E):
         if i == 3:
             torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        prob.upload(pin_A, pin_B, pin_bias, non_blocking=True)
-        prob.run(stream)
-        for h, v in zip(host_out, out_views):
-            h.copy_(v, non_blocking=True)
-    e1.record(stream)
+            e0.record(up_s)
+        j = i % 2
+        p = probs[j]
+        up_s.wait_event(ev_run[j])            # the kernel that read these inputs is done
+        with torch.cuda.stream(up_s):
+            p.upload(pin_A, pin_B, pin_bias, non_blocking=True)
+        ev_up[j].record(up_s)
+        stream.wait_event(ev_up[j])
+        stream.wait_event(ev_down[j])         # the previous download of this output is done
+        p.run(stream)
+        ev_run[j].record(stream)
+        down_s.wait_event(ev_run[j])
+        with torch.cuda.stream(down_s):
+            for h, v in zip(host_out[j], out_views(p)):
+                h.copy_(v, non_blocking=True)
+        ev_down[j].record(down_s)
+    e1.record(down_s)                         # after the last step's download
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, pg)
     e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "pipelining": "two buffers; uploads, kernel and downloads on three streams"}
+    rc2 = query_status(prob2.ws, stream)
+    if rc2[0] != 0:
+        raise RuntimeError(f"device status after e2e steps: {rc2}")
+    del prob2
     rc = query_status(prob.ws, stream)
     if rc[0] != 0:
         raise RuntimeError(f"device status after e2e steps: {rc}")

@@ -180,3 +180,34 @@ WORKLOADS = {
 CONCURRENT_WORKLOAD = dict(M=8192, N=8192, K=8192, gemm_dtype="bf16", gemm_seed=3,
                            coll="all_reduce", W=8, count=64 * 1024 * 1024, coll_dtype="f32",
                            coll_seed=4)
+
+# The world-size-8 all_gather_matmul shape list of the ROCm/iris PR #506
+# performance table (label, M, N, K; bf16).  Timing workloads only: their
+# inputs are drawn on the device by ``fill_device_`` and never reach the oracle.
+AG_MM_SHAPES = [
+    ("g2", 131072, 16384, 16384),
+    ("g14", 147456, 28672, 4096),
+    ("g15", 327680, 28672, 4096),
+    ("g16", 229376, 28672, 4096),
+    ("g5", 8192, 8192, 262144),
+    ("g6", 262144, 8192, 8192),
+    ("g1", 16384, 16384, 131072),
+    ("g8", 262144, 28672, 8192),
+    ("g9", 196608, 18432, 16384),
+    ("mixtral_gate", 4096, 14336, 4096),
+    ("llama7b_gate", 4096, 11008, 4096),
+    ("pow2_4k", 4096, 4096, 4096),
+]
+
+
+def fill_device_(t: torch.Tensor, seed: int, dist: str = "normal", scale: float = 0.02) -> torch.Tensor:
+    """Fill a device tensor in place from ``torch.Generator(device).manual_seed(seed)``
+    ('normal' with std ``scale`` or 'uniform' in [-scale, scale]), drawn in
+    the tensor's own dtype.  For multi-GB timing inputs that would take
+    minutes to draw on the host; parity inputs use the host generators above."""
+    g = torch.Generator(device=t.device).manual_seed(int(seed))
+    if dist == "normal":
+        return t.normal_(0.0, scale, generator=g)
+    if dist == "uniform":
+        return t.uniform_(-scale, scale, generator=g)
+    raise ValueError(dist)
