@@ -17,6 +17,14 @@
 //               fp32 partial -> global) and comm tiles (128-bit vector copy /
 //               rank-order fp32 reduce), so the comm tiles of one SM run
 //               while its tensor cores work on the next GEMM tile.
+// CTA pairs (template CG = 2, launched as clusters of two): a GEMM item is a
+// 256 x BN tile.  The even CTA's scheduler publishes every item into both
+// CTAs' rings and its MMA thread issues tcgen05.mma.cta_group::2 (M = 256)
+// for both; each CTA's TMA producer loads its 128 rows of A and BN/2 columns
+// of B, counted on the even CTA's full barrier; each CTA's workers drain
+// their own 128 accumulator rows and release them on the even CTA's
+// acc_empty barrier.  Comm items (all_gather_matmul gathers) run in both
+// CTAs, each on its own 128 rows.
 // Every wait is bounded (globaltimer); a wait that gives up records the
 // failure in the workspace status word, sets the launch's abort epoch, and
 // every role drains its in-flight async work and leaves.
@@ -152,6 +160,7 @@ struct Ctl {
     WsHeader* ws;
     uint32_t epoch;
     unsigned long long limit;
+    int half;  // CTA-pair kernels: this CTA's rank in the pair (0 issues the MMAs); else 0
 };
 
 __device__ __forceinline__ bool launch_aborted(const Ctl& c) {
@@ -184,11 +193,17 @@ __device__ __forceinline__ uint32_t arrive_count(unsigned long long* ctr, uint32
 }
 
 // Bounded wait on an mbarrier phase. false = gave up (timeout or abort).
-__device__ __forceinline__ bool wait_bar(const Ctl& c, uint64_t* bar, uint32_t parity, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+// `cluster`: the barrier receives release-arrivals from the peer CTA of a
+// pair, so the wait acquires at cluster scope.
+__device__ __forceinline__ bool try_bar(uint64_t* bar, uint32_t parity, bool cluster) {
+    return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+__device__ __forceinline__ bool wait_bar(const Ctl& c, uint64_t* bar, uint32_t parity, int where,
+                                         bool cluster = false) {
+    if (try_bar(bar, parity, cluster)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_bar(bar, parity, cluster)) return true;
         if ((i & 15) == 0) {
             if (launch_aborted(c)) return false;
             if (global_timer_ns() - t0 > c.limit) {
@@ -285,6 +300,15 @@ __device__ __forceinline__ uint32_t gemm_index(const Params& p, uint32_t t, int 
     return sg * T * p.W + static_cast<uint32_t>(s) * Tsg + (t - sg * T);
 }
 
+// This CTA's block of BM rows inside GEMM item gc: an item's m-block spans CG
+// such blocks, one per CTA of a pair.  matmul_all_gather counts blocks inside
+// the item's rank; the other ops count them over all M rows.
+template <int CG>
+__device__ __forceinline__ int own_block(const Params& p, const GemmCoord& gc, int half) {
+    const int mb = (p.op == OP_MM_AG) ? gc.mb % p.mb_per_rank : gc.mb;
+    return mb * CG + half;
+}
+
 // all_gather_matmul: number of gather items (ordered m-block by m-block, W
 // shards each) that must be claimed before GEMM item x may be published: all
 // shards of every m-block up to x's own.  Inside a swizzle group the first
@@ -313,10 +337,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
 }
 
 // ============================================================ shared state
-template <int BN, int STAGES>
+// CG = 2: the CTA pair computes a (2 BM) x BN tile; this CTA holds BM rows of
+// A and BN / 2 columns of B per stage.
+template <int BN, int STAGES, int CG>
 struct Smem {
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t B_BYTES = (BN / CG) * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
@@ -372,8 +398,8 @@ struct Smem {
 // it depends on has been claimed (by this or another CTA), so the ring order of
 // every CTA is a topological order of the dependency graph and no CTA can wait
 // on work that nobody will run.
-template <int BN, int STAGES>
-__device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
+template <int BN, int STAGES, int CG>
+__device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm) {
     Tracer tr;
     tr.init(p, TR_SCHED);
     uint32_t ring_n = 0;
@@ -381,10 +407,16 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
     const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
     const bool prefer_gemm = p.gemm_ctas < 0 || static_cast<int>(blockIdx.x) < p.gemm_ctas;
 
+    // CTA pairs: the even CTA's scheduler feeds both CTAs' rings (the odd
+    // CTA's consumers release slots on the even CTA's item_empty barriers)
     auto publish = [&](uint32_t item) -> bool {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
-        if (!wait_bar(ctl, &sm.item_empty[slot], (use & 1) ^ 1, WAIT_ITEM_EMPTY)) return false;
+        if (!wait_bar(ctl, &sm.item_empty[slot], (use & 1) ^ 1, WAIT_ITEM_EMPTY, CG == 2)) return false;
         sm.ring[slot] = item;
+        if (CG == 2) {
+            st_shared_cluster_u32(mapa_shared(const_cast<uint32_t*>(&sm.ring[slot]), 1), item);
+            mbar_arrive_cluster(mapa_shared(&sm.item_full[slot], 1));
+        }
         mbar_arrive(&sm.item_full[slot]);
         ++ring_n;
         tr.rec(EV_CLAIM, item);
@@ -488,12 +520,22 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
     tr.finish();
 }
 
+// A consumer is done with ring slot `slot` (CTA pairs: the even CTA's
+// item_empty barrier counts the consumers of both CTAs).
+template <int BN, int STAGES, int CG>
+__device__ __forceinline__ void release_item(Smem<BN, STAGES, CG>& sm, uint32_t slot) {
+    if (CG == 2)
+        mbar_arrive_cluster(mapa_shared(&sm.item_empty[slot], 0));
+    else
+        mbar_arrive(&sm.item_empty[slot]);
+}
+
 // ============================================================ TMA producer
 // Follows the item ring; for every GEMM item streams its K-blocks of A and B
 // into the STAGES-deep shared-memory pipeline (acquiring the gather flags of
 // all_gather_matmul shards just before their first K-block).
-template <int BN, int STAGES>
-__device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
+template <int BN, int STAGES, int CG>
+__device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm) {
     Tracer tr;
     tr.init(p, TR_TMA);
     uint32_t stage = 0, phase = 0, ring_n = 0;
@@ -503,26 +545,23 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
 
     auto load_gemm = [&](uint32_t g) -> bool {
         const GemmCoord gc = decode_gemm(p, g);
-        int a_row, a_rank;
-        if (p.op == OP_MM_AG) {
-            a_row = (gc.mb % p.mb_per_rank) * BM;
-            a_rank = gc.rank;
-        } else {
-            a_row = gc.mb * BM;
-            a_rank = reduce_op ? gc.rank : 0;
-        }
+        const int blk = own_block<CG>(p, gc, ctl.half);
+        const int a_row = blk * BM;
+        const int a_rank = (p.op == OP_MM_AG || reduce_op) ? gc.rank : 0;
         const int b_rank = reduce_op ? gc.rank : 0;
         int acquired = 0;  // all_gather_matmul: shards whose flags are held
-        if (p.op == OP_AG_MM) {
+        if (p.op == OP_AG_MM && a_row >= p.M) {
+            acquired = p.W;  // this CTA's half of a pair tile lies below the last row: no gathers
+        } else if (p.op == OP_AG_MM) {
             // an m-block seen complete before needs no flag traffic; else check
             // all W shard flags at once and take the per-shard waits below
             // only for the shards still missing
-            const bool cacheable = gc.mb < Smem<BN, STAGES>::READY_BITS;
+            const bool cacheable = gc.mb < Smem<BN, STAGES, CG>::READY_BITS;
             if (cacheable && (sm.ready_bits[gc.mb >> 5] >> (gc.mb & 31) & 1u)) {
                 acquired = p.W;
             } else {
                 uint32_t seen = 0;
-                for (int s = 0; s < p.W; ++s) seen += ld_acquire_gpu(&p.flags[gc.mb * p.W + s]) == ctl.epoch ? 1u : 0u;
+                for (int s = 0; s < p.W; ++s) seen += ld_acquire_gpu(&p.flags[blk * p.W + s]) == ctl.epoch ? 1u : 0u;
                 if (seen == static_cast<uint32_t>(p.W)) {
                     acquired = p.W;
                     fence_proxy_async_global();
@@ -535,22 +574,35 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
                 const int s_hi = min(p.W - 1, (kb * BK + BK - 1) / p.K_local);
                 if (s_hi >= acquired) {
                     for (int s = acquired; s <= s_hi; ++s) {
-                        const int fi = gc.mb * p.W + s;
+                        const int fi = blk * p.W + s;
                         if (!wait_flag(ctl, &p.flags[fi], WAIT_FLAG_GATHER, fi)) return false;
                     }
                     acquired = s_hi + 1;
                     fence_proxy_async_global();
-                    if (acquired == p.W && gc.mb < Smem<BN, STAGES>::READY_BITS)
+                    if (acquired == p.W && gc.mb < Smem<BN, STAGES, CG>::READY_BITS)
                         sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
                 }
             }
             if (!wait_bar(ctl, &sm.empty[stage], phase ^ 1, WAIT_SMEM_EMPTY)) return false;
-            mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES>::STAGE_BYTES);
-            tma_load_3d(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, &sm.full[stage]);
+            if (CG == 1) {
+                mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES, CG>::STAGE_BYTES);
+                tma_load_3d(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, &sm.full[stage]);
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-                tma_load_3d(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, gc.nb * BN + c * 64,
-                            kb * BK, b_rank, &sm.full[stage]);
+                for (int c = 0; c < BN / 64; ++c)
+                    tma_load_3d(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, gc.nb * BN + c * 64,
+                                kb * BK, b_rank, &sm.full[stage]);
+            } else {
+                // both CTAs' boxes count on the even CTA's full barrier, which
+                // expects the pair's bytes (the odd CTA's may land first: the
+                // transaction count may dip below zero inside a phase)
+                if (ctl.half == 0) mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES, CG>::STAGE_BYTES * CG);
+                const uint32_t fb = mapa_shared(&sm.full[stage], 0);
+                tma_load_3d_pair(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, fb);
+#pragma unroll
+                for (int c = 0; c < BN / CG / 64; ++c)
+                    tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB,
+                                     gc.nb * BN + ctl.half * (BN / CG) + c * 64, kb * BK, b_rank, fb);
+            }
             issued_phase[stage] = phase;
             used_mask |= 1u << stage;
             if (++stage == STAGES) {
@@ -564,9 +616,9 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
     uint32_t leases = 0;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
-        if (!wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_TMA)) break;
+        if (!wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_TMA, CG == 2)) break;
         const uint32_t item = sm.ring[slot];
-        mbar_arrive(&sm.item_empty[slot]);
+        release_item(sm, slot);
         ++ring_n;
         if (item == ITEM_END) break;
         if (item & ITEM_COMM) {
@@ -587,16 +639,20 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm) {
         tr.rec(EV_END, item);
     }
     tr.finish();
-    // drain: every TMA load issued into a stage has landed before the CTA exits
+    // drain: every TMA load issued into a stage has landed before the CTA
+    // exits.  The odd CTA of a pair cannot wait on the even CTA's full
+    // barrier; it waits until the MMA has consumed its last fill of each stage.
     for (int s = 0; s < STAGES; ++s)
-        if (used_mask & (1u << s)) drain_bar(ctl, &sm.full[s], issued_phase[s], WAIT_TEARDOWN_TMA);
+        if (used_mask & (1u << s))
+            drain_bar(ctl, ctl.half ? &sm.empty[s] : &sm.full[s], issued_phase[s], WAIT_TEARDOWN_TMA);
 }
 
 // ============================================================ MMA issuer
-template <int BN, int STAGES>
-__device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem) {
-    constexpr uint32_t IDESC_F16 = make_idesc(0, BM, BN);
-    constexpr uint32_t IDESC_BF16 = make_idesc(1, BM, BN);
+template <int BN, int STAGES, int CG>
+__device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem) {
+    // CTA pairs: one instruction covers the pair's (2 BM) x BN tile
+    constexpr uint32_t IDESC_F16 = make_idesc(0, BM * CG, BN);
+    constexpr uint32_t IDESC_BF16 = make_idesc(1, BM * CG, BN);
     const uint32_t idesc = p.bf16 ? IDESC_BF16 : IDESC_F16;
     Tracer tr;
     tr.init(p, TR_MMA);
@@ -610,7 +666,8 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
         if (item == ITEM_END) break;
         if (item & ITEM_COMM) continue;
         const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
-        if (!wait_bar(ctl, &sm.acc_empty[buf], (ause & 1) ^ 1, WAIT_ACC_EMPTY)) break;
+        // CTA pairs: the workers of both CTAs release the accumulator here
+        if (!wait_bar(ctl, &sm.acc_empty[buf], (ause & 1) ^ 1, WAIT_ACC_EMPTY, CG == 2)) break;
         tc_fence_after();
         tr.rec(EV_BEGIN, item);
         const uint32_t d = tmem + buf * BN;
@@ -630,23 +687,30 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, u
             for (int k = 0; k < BK / UMMA_K; ++k) {
                 // advance A by 16 columns (32 B inside the swizzled row) and
                 // B by 16 rows (2 KB); descriptors hold addresses >> 4
-                umma_f16(d, adesc + static_cast<uint64_t>(k * 2), bdesc + static_cast<uint64_t>(k * 128),
-                         idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_f16<CG>(d, adesc + static_cast<uint64_t>(k * 2), bdesc + static_cast<uint64_t>(k * 128),
+                             idesc, (kb | k) != 0 ? 1u : 0u);
             }
-            umma_commit(&sm.empty[stage]);
+            // the stage is free again in both CTAs of a pair
+            if (CG == 2)
+                umma_commit_pair_both(&sm.empty[stage]);
+            else
+                umma_commit<1>(&sm.empty[stage]);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
             }
         }
         if (!ok) break;
-        umma_commit(&sm.acc_full[buf]);
+        if (CG == 2)
+            umma_commit_pair_both(&sm.acc_full[buf]);
+        else
+            umma_commit<1>(&sm.acc_full[buf]);
         tr.rec(EV_END, item);
         ++acc_i;
     }
     tr.finish();
     // drain: every MMA issued by this thread has completed
-    umma_commit(sm.final_bar);
+    umma_commit<CG>(sm.final_bar);
     drain_bar(ctl, sm.final_bar, 0, WAIT_TEARDOWN_MMA);
 }
 
@@ -660,7 +724,7 @@ struct WorkerCtx {
     uint32_t sphase;  // parity bits of this warp's two running-sum load barriers
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx& wc);
 
 // Distributed reduce (reduce ops, reduce_mode 2).  Output tile t is cut into W
@@ -795,12 +859,12 @@ __device__ __forceinline__ bool parts_done(const Params& p, const PartState& ps)
 // not complete (warp-uniform: lane 0 polls).
 template <int BN>
 __device__ bool wait_bar_working(const Params& p, const Ctl& c, uint64_t* bar, uint32_t parity, int where,
-                                 PartState& ps, WorkerCtx& wc) {
+                                 PartState& ps, WorkerCtx& wc, bool cluster = false) {
     uint64_t t0 = 0;
     bool timing = false;
     for (uint32_t i = 0;; ++i) {
         int ready = 0;
-        if (wc.lane == 0) ready = mbar_try_wait(bar, parity) ? 1 : 0;
+        if (wc.lane == 0) ready = try_bar(bar, parity, cluster) ? 1 : 0;
         if (__shfl_sync(0xFFFFFFFFu, ready, 0)) return true;
         if (part_step<BN>(p, c.epoch, ps, wc)) {
             timing = false;  // progress: restart the idle clock
@@ -821,8 +885,8 @@ __device__ bool wait_bar_working(const Params& p, const Ctl& c, uint64_t* bar, u
 }
 
 // barrier over the worker warps built on an mbarrier (bounded, abortable)
-template <int BN, int STAGES>
-__device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES>& sm, WorkerCtx& wc) {
+template <int BN, int STAGES, int CG>
+__device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES, CG>& sm, WorkerCtx& wc) {
     __syncwarp();
     bool ok = true;
     if (wc.lane == 0) {
@@ -833,9 +897,19 @@ __device__ __forceinline__ bool worker_sync(const Ctl& ctl, Smem<BN, STAGES>& sm
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
 }
 
+// This warp has read its accumulator slice (CTA pairs: the even CTA's
+// acc_empty barrier counts the worker warps of both CTAs).
+template <int BN, int STAGES, int CG>
+__device__ __forceinline__ void release_acc(Smem<BN, STAGES, CG>& sm, uint32_t buf) {
+    if (CG == 2)
+        mbar_arrive_cluster(mapa_shared(&sm.acc_empty[buf], 0));
+    else
+        mbar_arrive(&sm.acc_empty[buf]);
+}
+
 // GEMM epilogue of one tile: TMEM -> registers -> (+bias) -> global.
-template <int BN, int STAGES>
-__device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem,
+template <int BN, int STAGES, int CG>
+__device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem,
                          uint32_t g, uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
@@ -843,6 +917,7 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     tr.rec(EV_READY, g);
 
     const GemmCoord gc = decode_gemm(p, g);
+    const int blk = own_block<CG>(p, gc, ctl.half);
     const int r_in_tile = wc.q * 32 + wc.lane;
     const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
     // output row of this thread and whether it exists
@@ -850,12 +925,12 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     int bias_row;   // index into a per-row bias
     bool row_ok;
     if (p.op == OP_MM_AG) {
-        const int lrow = (gc.mb % p.mb_per_rank) * BM + r_in_tile;
+        const int lrow = blk * BM + r_in_tile;
         row_ok = lrow < p.M;
         row = gc.rank * p.M + lrow;
         bias_row = lrow;
     } else {
-        row = gc.mb * BM + r_in_tile;
+        row = blk * BM + r_in_tile;
         row_ok = row < p.M;
         bias_row = row;
     }
@@ -873,23 +948,25 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     // Each 32 x 32 chunk (the warp's 32 rows, one per lane) goes registers ->
     // swizzled shared-memory staging -> TMA tensor store, so global memory
     // sees whole 128-byte lines instead of 16-byte pieces of 32 rows.
-    uint8_t* stg = sm.stage_out + wc.w * Smem<BN, STAGES>::STAGE_OUT_BYTES;
+    uint8_t* stg = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
     // TMA coordinates of the warp's 32-row slab
-    int c_row, c_blk, c_reg_lo = 0, c_reg_hi = 1;
+    const int c_row = blk * BM + wc.q * 32;
+    int c_blk, c_reg_lo = 0, c_reg_hi = 1;
     if (reduce_op) {
-        c_row = gc.mb * BM + wc.q * 32;
         c_blk = gc.rank;
     } else if (p.op == OP_MM_AG) {
-        c_row = (gc.mb % p.mb_per_rank) * BM + wc.q * 32;
         c_blk = gc.rank;
         if (p.replicate) c_reg_hi = p.W;
     } else {
-        c_row = gc.mb * BM + wc.q * 32;
         c_blk = 0;
         if (p.replicate && p.op == OP_AG_MM) c_reg_hi = p.W;
     }
+    // CTA pairs: nothing to store when this CTA's half lies below the last
+    // row (the accumulator is still released after acc_full, in step with
+    // the pair)
+    const int cols_end = (CG == 2 && blk * BM >= p.M) ? 0 : COLS;
 #pragma unroll 1
-    for (int cc = 0; cc < COLS; cc += 32) {
+    for (int cc = 0; cc < cols_end; cc += 32) {
         uint32_t r[32];
         if (p.k_blocks > 0) {
             tmem_ld_32x32b_x32(tbase + cc, r);
@@ -948,7 +1025,7 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, 
     }
     tc_fence_before();
     __syncwarp();
-    if (wc.lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+    if (wc.lane == 0) release_acc(sm, buf);
 
     if (reduce_op) {
         // publish this rank's partial tile: all worker warps' stores complete and
@@ -1000,23 +1077,33 @@ __device__ __forceinline__ bool wait_count(const Ctl& c, const unsigned long lon
 // then advances the counter.  This is a ring reduce-scatter/all-reduce done
 // per tile inside the GEMM epilogues; each wait is on a GEMM item with a
 // smaller index, which was claimed earlier and never waits on this one.
-template <int BN, int STAGES>
-__device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem, uint32_t g,
+template <int BN, int STAGES, int CG>
+__device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem, uint32_t g,
                                uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
     tr.rec(EV_READY, g);
     const GemmCoord gc = decode_gemm(p, g);
+    const int blk = own_block<CG>(p, gc, ctl.half);
+    if (CG == 2 && blk * BM >= p.M) {
+        // this CTA's half of the pair tile lies below the last row: no
+        // partial, no sum; release the accumulator in step with the pair
+        tc_fence_before();
+        __syncwarp();
+        if (wc.lane == 0) release_acc(sm, buf);
+        return true;
+    }
     const int s = gc.rank;
     const bool last = (s == p.W - 1);
-    const int row = gc.mb * BM + wc.q * 32 + wc.lane;
+    const int row = blk * BM + wc.q * 32 + wc.lane;
     const char* bias_base =
         p.has_bias ? p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_bias : nullptr;
     float row_bias = 0.f;
     if (p.has_bias && p.bias_on_m && row < p.M)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
-    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.flags) + gc.tile;
+    // one counter per BM-row block and column block
+    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.flags) + (blk * p.n_blocks + gc.nb);
     const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
     if (s > 0) {
         int ok = 1;
@@ -1027,9 +1114,9 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
     constexpr int NCH = COLS / 32;
     const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
-    uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES>::STAGE_OUT_BYTES;
+    uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
     uint64_t* lbar = sm.sbar + 2 * wc.w;
-    const int c_row = gc.mb * BM + wc.q * 32;
+    const int c_row = blk * BM + wc.q * 32;
     const int colbase = gc.nb * BN + wc.h * COLS;
     // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
     const int nch = max(0, min(NCH, (p.N - colbase) / 32));
@@ -1129,7 +1216,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     }
     tc_fence_before();
     __syncwarp();
-    if (wc.lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+    if (wc.lane == 0) release_acc(sm, buf);
     if (!last) {
         // S[t] complete and visible, then hand the tile to rank s+1
         if (wc.lane == 0) {
@@ -1146,10 +1233,13 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
 }
 
 // all_gather_matmul gather tile: shard s rows of m-block mb -> gathered buffer.
-template <int BN, int STAGES>
-__device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t c,
+template <int BN, int STAGES, int CG>
+__device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c,
                             WorkerCtx& wc) {
-    const int mb = static_cast<int>(c / p.W), s = static_cast<int>(c % p.W);
+    // CTA pairs: both CTAs run the item, each copying (and flagging) its own
+    // block of BM rows of the pair's m-block
+    const int mb = static_cast<int>(c / p.W) * CG + ctl.half, s = static_cast<int>(c % p.W);
+    if (mb * BM >= p.M) return true;  // below the last row: nothing to copy, no consumer
     const int rows = min(BM, p.M - mb * BM);
     const int vpr = p.K_local / 8;  // 16-byte vectors per shard row
     const int Kv = p.K / 8;         // vectors per gathered row
@@ -1179,13 +1269,14 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
     fence_proxy_async_global();
     __threadfence();
     if (!worker_sync(ctl, sm, wc)) return false;
-    if (wc.w == 0 && wc.lane == 0 && p.debug_skip != c + 1) st_release_gpu(&p.flags[c], ctl.epoch);
+    const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
+    if (wc.w == 0 && wc.lane == 0 && p.debug_skip != fi + 1) st_release_gpu(&p.flags[fi], ctl.epoch);
     return true;
 }
 
 // matmul_reduce_scatter / matmul_all_reduce comm tile: rank-order fp32 sum
 // of the W partial tiles of output tile c, rounded and scattered.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __device__ bool reduce_tile(const Params& p, const Ctl& ctl, uint32_t c, WorkerCtx& wc) {
     bool ok = true;
     if (wc.lane == 0) {
@@ -1195,7 +1286,7 @@ __device__ bool reduce_tile(const Params& p, const Ctl& ctl, uint32_t c, WorkerC
         }
     }
     if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return false;
-    reduce_body<BN, STAGES>(p, c, wc);
+    reduce_body<BN, STAGES, CG>(p, c, wc);
     return true;
 }
 
@@ -1204,7 +1295,7 @@ __device__ bool reduce_tile(const Params& p, const Ctl& ctl, uint32_t c, WorkerC
 // store instruction of a warp covers 512 contiguous bytes.  SC ranks of a row
 // are loaded together before their adds; partials are summed in rank order
 // 0..W-1 in fp32.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx& wc) {
     constexpr int CPL = BN / 4 / 32;  // float4 chunks per lane per row
     constexpr int SC = 4;             // ranks per load batch
@@ -1279,9 +1370,9 @@ __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx&
 // (all W ranks for all-reduce / reduce-scatter, rank s for all-gather) into one
 // buffer while the other is summed in rank order (fp32) and bulk-stored to the
 // destinations.  Bytes in flight per SM: about half the stage area.
-template <int BN, int STAGES>
-__device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t c, WorkerCtx& wc) {
-    constexpr uint32_t AREA = STAGES * Smem<BN, STAGES>::STAGE_BYTES / NUM_WORKER_WARPS;
+template <int BN, int STAGES, int CG>
+__device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c, WorkerCtx& wc) {
+    constexpr uint32_t AREA = STAGES * Smem<BN, STAGES, CG>::STAGE_BYTES / NUM_WORKER_WARPS;
     constexpr uint32_t HALF = AREA / 2;
     uint8_t* area = sm.tiles + wc.w * AREA;
     uint64_t* bar = sm.sbar + 2 * wc.w;
@@ -1404,8 +1495,8 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES>&
     return true;
 }
 
-template <int BN, int STAGES>
-__device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& sm, uint32_t tmem,
+template <int BN, int STAGES, int CG>
+__device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem,
                             int warp, int lane) {
     WorkerCtx wc;
     wc.w = warp - FIRST_WORKER_WARP;
@@ -1425,11 +1516,13 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
     bool ok = true;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
-        ok = wait_bar_working<BN>(p, ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_WORKER, ps, wc);
+        ok = wait_bar_working<BN>(p, ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_WORKER, ps, wc, CG == 2);
         if (!ok) break;
-        const uint32_t item = sm.ring[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+        // lane 0 did the acquire; it reads the slot and hands the item on
+        uint32_t item = 0;
+        if (lane == 0) item = sm.ring[slot];
+        item = __shfl_sync(0xFFFFFFFFu, item, 0);
+        if (lane == 0) release_item(sm, slot);
         ++ring_n;
         if (item == ITEM_END) break;
         tr.rec(EV_BEGIN, item);
@@ -1441,11 +1534,11 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
                 int got = 1;
                 if (lane == 0) got = wait_bar(ctl, sm.lease, leases & 1, WAIT_LEASE) ? 1 : 0;
                 ++leases;
-                ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0 && coll_tile_tma<BN, STAGES>(p, ctl, sm, c, wc);
+                ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0 && coll_tile_tma<BN, STAGES, CG>(p, ctl, sm, c, wc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.lease_done);
             } else {
-                ok = reduce_tile<BN, STAGES>(p, ctl, c, wc);
+                ok = reduce_tile<BN, STAGES, CG>(p, ctl, c, wc);
             }
         } else {
             if (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR))
@@ -1489,13 +1582,17 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES>& s
 }
 
 // ============================================================ kernel
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const __grid_constant__ Params p) {
     constexpr int TMEM_COLS = 2 * BN;
     extern __shared__ uint8_t smem_raw[];
-    Smem<BN, STAGES> sm;
+    Smem<BN, STAGES, CG> sm;
     sm.carve(smem_raw);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // CTA pairs (cluster of 2): the even CTA runs the scheduler and issues the
+    // MMAs for both; each CTA loads its halves of A and B and drains its own
+    // half of the accumulator
+    const int half = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -1504,18 +1601,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.acc_full[b], 1);
-            mbar_init(&sm.acc_empty[b], NUM_WORKER_WARPS);
+            mbar_init(&sm.acc_empty[b], CG * NUM_WORKER_WARPS);
         }
         for (int i = 0; i < RING; ++i) {
             mbar_init(&sm.item_full[i], 1);
-            mbar_init(&sm.item_empty[i], 2 + NUM_WORKER_WARPS);  // MMA + TMA + workers
+            // MMA + TMA + workers (pairs: plus the odd CTA's TMA + workers)
+            mbar_init(&sm.item_empty[i], 2 + NUM_WORKER_WARPS + (CG == 2 ? 1 + NUM_WORKER_WARPS : 0));
         }
         mbar_init(sm.wbar, NUM_WORKER_WARPS);
         mbar_init(sm.final_bar, 1);
         for (int i = 0; i < 2 * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
         mbar_init(sm.lease, 1);
         mbar_init(sm.lease_done, NUM_WORKER_WARPS);
-        for (int i = 0; i < Smem<BN, STAGES>::READY_BITS / 32; ++i) sm.ready_bits[i] = 0u;
+        for (int i = 0; i < Smem<BN, STAGES, CG>::READY_BITS / 32; ++i) sm.ready_bits[i] = 0u;
         fence_mbar_init();
         uint32_t e = *reinterpret_cast<volatile uint32_t*>(&p.ws->epoch) + 1u;
         if (e == 0u) e = 1u;
@@ -1527,31 +1625,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         if (p.n_gemm > 0) tma_prefetch_desc(&p.tmC);
         if (p.n_gemm > 0 && p.reduce_mode == 3) tma_prefetch_desc(&p.tmS);
     }
-    if (warp == 1) tmem_alloc<TMEM_COLS>(sm.tmem_slot);
+    if (warp == 1) tmem_alloc<TMEM_COLS, CG>(sm.tmem_slot);
     tc_fence_before();
     __syncthreads();
+    // pairs: both CTAs' barriers are initialised before either signals the other's
+    if (CG == 2) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot;
-    const Ctl ctl{p.ws, *sm.epoch_slot, p.wait_ns};
+    const Ctl ctl{p.ws, *sm.epoch_slot, p.wait_ns, half};
 
     if (warp == 0) {
-        if (lane == 0) run_scheduler<BN, STAGES>(p, ctl, sm);
+        if (lane == 0 && half == 0) run_scheduler<BN, STAGES, CG>(p, ctl, sm);
         __syncwarp();
     } else if (warp == 2) {
-        if (lane == 0) run_tma<BN, STAGES>(p, ctl, sm);
+        if (lane == 0) run_tma<BN, STAGES, CG>(p, ctl, sm);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) run_mma<BN, STAGES>(p, ctl, sm, tmem);
+        if (lane == 0 && half == 0) run_mma<BN, STAGES, CG>(p, ctl, sm, tmem);
         __syncwarp();
     } else {
-        run_workers<BN, STAGES>(p, ctl, sm, tmem, warp, lane);
+        run_workers<BN, STAGES, CG>(p, ctl, sm, tmem, warp, lane);
     }
 
     tc_fence_before();
     __syncthreads();
+    // pairs: neither CTA leaves (or frees tensor memory) while the other may
+    // still signal its barriers or read the accumulators the MMAs wrote
+    if (CG == 2) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<TMEM_COLS>(tmem);
+        tmem_dealloc<TMEM_COLS, CG>(tmem);
     }
     if (threadIdx.x == 0) {
         __threadfence();

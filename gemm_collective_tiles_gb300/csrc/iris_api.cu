@@ -20,6 +20,9 @@ namespace {
 
 constexpr int BN_WIDE = 256, STAGES_WIDE = 4;
 constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
+// CTA pairs (tile_m 256): 256 x 256 tiles over two SMs; each SM stages
+// 128 x 64 of A and 64 x 128 of B (32 KB) per K-block, six deep
+constexpr int STAGES_PAIR = 6;
 constexpr size_t WS_HEADER = 256;
 constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
 
@@ -60,25 +63,64 @@ EncodeTiledFn encoder() {
     return g_encode;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 constexpr size_t smem_bytes() {
-    return Smem<BN, STAGES>::BYTES;
+    return Smem<BN, STAGES, CG>::BYTES;
+}
+
+int g_pair_clusters[64] = {0};  // co-resident CTA pairs of the pair kernel, per device
+
+cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    lc.gridDim = dim3(grid, 1, 1);
+    lc.blockDim = dim3(NUM_THREADS, 1, 1);
+    lc.dynamicSmemBytes = smem_bytes<BN_WIDE, STAGES_PAIR, 2>();
+    lc.stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = 2;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return lc;
 }
 
 int ensure_attrs(int dev) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (dev < 0 || dev >= 64) return IRIS_ECUDA;
     if (g_attr_done[dev]) return IRIS_OK;
-    cudaError_t e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>,
+    cudaError_t e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE, 1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<BN_WIDE, STAGES_WIDE>()));
+                                         static_cast<int>(smem_bytes<BN_WIDE, STAGES_WIDE, 1>()));
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_n 256)", static_cast<int>(e));
-    e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>,
+    e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW, 1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN_NARROW, STAGES_NARROW>()));
+                             static_cast<int>(smem_bytes<BN_NARROW, STAGES_NARROW, 1>()));
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_n 128)", static_cast<int>(e));
+    e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN_WIDE, STAGES_PAIR, 2>()));
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_m 256)", static_cast<int>(e));
+    // how many CTA pairs fit at once (one CTA per SM; a pair needs two SMs of
+    // one GPC): the persistent pair grid is twice that
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IRIS_ECUDA;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t lc = pair_launch_config(sms - (sms & 1), 0, &attr);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR, 2>, &lc);
+    if (e != cudaSuccess || clusters < 1) return cuda_fail("cudaOccupancyMaxActiveClusters", static_cast<int>(e));
+    g_pair_clusters[dev] = clusters;
     g_attr_done[dev] = true;
     return IRIS_OK;
+}
+
+// co-resident CTA pairs on the current device (0 on error)
+int pair_clusters() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || ensure_attrs(dev) != IRIS_OK) return 0;
+    return g_pair_clusters[dev];
 }
 
 int num_sms_current(int* n) {
@@ -93,6 +135,8 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Resolved configuration.
 struct Cfg {
+    int tile_m;   // requested: 0 = per op default, 128, 256 (CTA pairs)
+    int cg;       // resolved: 1 = one CTA per tile, 2 = CTA pairs
     int tile_n, group_m, gemm_ctas, comm_block, replicate, bias_on_m, grid;
     unsigned long long wait_ns;
     uint32_t debug_skip;
@@ -107,7 +151,11 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     iris_b200_config z;
     std::memset(&z, 0, sizeof(z));
     if (!c) c = &z;
-    if (c->tile_m != 0 && c->tile_m != BM) return IRIS_EINVAL;
+    if (c->tile_m != 0 && c->tile_m != BM && c->tile_m != 2 * BM) return IRIS_EINVAL;
+    if (c->tile_m == 2 * BM && (op == IRIS_OP_CONCURRENT || (c->tile_n != 0 && c->tile_n != 256)))
+        return IRIS_EINVAL;
+    out.tile_m = c->tile_m;
+    out.cg = 1;
     if (c->tile_k != 0 && c->tile_k != BK) return IRIS_EINVAL;
     if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256) return IRIS_EINVAL;
     out.tile_n = c->tile_n ? c->tile_n : (N <= 128 ? 128 : 256);
@@ -155,6 +203,28 @@ int resolve_reduce_mode(const iris_b200_config* c, iris_op op, int64_t N, int W)
     if (req == 1 || req == 2) return req;
     if (req == 3) return chain_ok ? 3 : -1;
     return -1;
+}
+
+// CTA pairs (tile_m 256) wherever they apply: every op but the concurrent
+// mode, 256-wide tiles, and the chained schedule for the reduce ops.  The
+// default is pairs; tile_m 128 keeps one CTA per tile.  The pair grid is every
+// co-resident pair (at most grid / 2).
+int resolve_pair(Cfg& c, iris_op op) {
+    const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
+    const bool applies = op != IRIS_OP_CONCURRENT && c.tile_n == BN_WIDE && (!reduce_op || c.reduce_mode == 3);
+    if (c.tile_m == 2 * BM && !applies) return IRIS_EINVAL;
+    c.cg = (c.tile_m == BM || !applies) ? 1 : 2;
+    if (c.cg == 2) {
+        const int pairs = std::min(pair_clusters(), c.grid / 2);
+        if (pairs < 1) {
+            if (c.tile_m == 2 * BM) return c.grid < 2 ? IRIS_EINVAL : IRIS_ECUDA;
+            c.cg = 1;
+            return IRIS_OK;
+        }
+        c.grid = 2 * pairs;
+        c.gemm_ctas = std::min(c.gemm_ctas, c.grid);
+    }
+    return IRIS_OK;
 }
 
 // Sizes of the workspace pieces for one call.
@@ -238,10 +308,11 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.m_blocks = m_blocks;
     p.n_blocks = static_cast<int>(cdiv(N, c.tile_n));
     p.k_blocks = static_cast<int>(cdiv(K, BK));
-    p.group_m = c.group_m;
+    // CTA pairs: an m-block is 2 x 128 rows; group_m stays in 128-row units
+    p.group_m = std::max(1, c.group_m / c.cg);
     p.n_tiles = p.m_blocks * p.n_blocks;
     p.gemm_ctas = c.gemm_ctas;
-    p.lookahead = static_cast<uint32_t>(c.grid);
+    p.lookahead = static_cast<uint32_t>(c.grid / c.cg);
     p.replicate = c.replicate;
     p.bias_on_m = c.bias_on_m;
     p.wait_ns = c.wait_ns;
@@ -257,12 +328,17 @@ int launch(Params& p, const Cfg& c, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess) return IRIS_ECUDA;
     int rc = ensure_attrs(dev);
     if (rc != IRIS_OK) return rc;
-    if (c.tile_n == BN_WIDE) {
-        fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE>
-            <<<c.grid, NUM_THREADS, smem_bytes<BN_WIDE, STAGES_WIDE>(), stream>>>(p);
+    if (c.cg == 2) {
+        cudaLaunchAttribute attr;
+        const cudaLaunchConfig_t lc = pair_launch_config(c.grid, stream, &attr);
+        const cudaError_t e = cudaLaunchKernelEx(&lc, fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR, 2>, p);
+        if (e != cudaSuccess) return cuda_fail("kernel launch (CTA pairs)", static_cast<int>(e));
+    } else if (c.tile_n == BN_WIDE) {
+        fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE, 1>
+            <<<c.grid, NUM_THREADS, smem_bytes<BN_WIDE, STAGES_WIDE, 1>(), stream>>>(p);
     } else {
-        fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW>
-            <<<c.grid, NUM_THREADS, smem_bytes<BN_NARROW, STAGES_NARROW>(), stream>>>(p);
+        fused_gemm_coll_kernel<BN_NARROW, STAGES_NARROW, 1>
+            <<<c.grid, NUM_THREADS, smem_bytes<BN_NARROW, STAGES_NARROW, 1>(), stream>>>(p);
     }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? IRIS_OK : cuda_fail("kernel launch", static_cast<int>(e));
@@ -343,6 +419,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     if (K_l % 8 != 0 || N % 8 != 0) return IRIS_EALIGN;
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_ALL_GATHER_MATMUL, N, c))) return rc;
+    if ((rc = resolve_pair(c, IRIS_OP_ALL_GATHER_MATMUL))) return rc;
     if ((rc = check_region(heap, off_A, size_t(M) * K_l * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -355,7 +432,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     p.op = OP_AG_MM;
     p.W = W;
     p.bf16 = dtype == IRIS_BF16;
-    const int mblocks = static_cast<int>(cdiv(M, BM));
+    const int mblocks = static_cast<int>(cdiv(M, BM * c.cg));
     fill_geometry(p, M, N, K, mblocks, c);
     p.mb_per_rank = mblocks;
     p.K_local = static_cast<int>(K_l);
@@ -399,6 +476,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if ((rc = resolve_cfg(cfg, op, N, c))) return rc;
     c.reduce_mode = resolve_reduce_mode(cfg, op, N, W);
     if (c.reduce_mode < 0) return IRIS_EINVAL;
+    if ((rc = resolve_pair(c, op))) return rc;
     if ((rc = check_region(heap, off_A, size_t(M) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N_l * 2))) return rc;
@@ -410,7 +488,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     p.op = (op == IRIS_OP_MATMUL_REDUCE_SCATTER) ? OP_MM_RS : OP_MM_AR;
     p.W = W;
     p.bf16 = dtype == IRIS_BF16;
-    const int mblocks = static_cast<int>(cdiv(M, BM));
+    const int mblocks = static_cast<int>(cdiv(M, BM * c.cg));
     fill_geometry(p, M, N, K, mblocks, c);
     p.mb_per_rank = mblocks;
     p.N_local = static_cast<int>(N_l);
@@ -479,6 +557,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     if (K % 8 != 0 || N % 8 != 0) return IRIS_EALIGN;
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_MATMUL_ALL_GATHER, N, c))) return rc;
+    if ((rc = resolve_pair(c, IRIS_OP_MATMUL_ALL_GATHER))) return rc;
     if ((rc = check_region(heap, off_A, size_t(M_l) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -490,7 +569,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     p.op = OP_MM_AG;
     p.W = W;
     p.bf16 = dtype == IRIS_BF16;
-    const int mbpr = static_cast<int>(cdiv(M_l, BM));
+    const int mbpr = static_cast<int>(cdiv(M_l, BM * c.cg));
     fill_geometry(p, M_l, N, K, mbpr * W, c);
     p.mb_per_rank = mbpr;
     p.heap = static_cast<char*>(heap->base);

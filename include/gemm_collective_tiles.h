@@ -92,7 +92,12 @@ typedef enum {
 
 /* Tuning knobs (the iris FusedConfig / concurrent gemm_wgs).  0 = default. */
 typedef struct {
-    int tile_m;            /* GEMM tile rows: 128 (only value) */
+    int tile_m;            /* GEMM tile rows: 256 = one tile per pair of SMs (a
+                              2-CTA cluster sharing the tensor-core instruction;
+                              the default wherever it applies: all ops but the
+                              concurrent mode, tile_n 256, chained reduce), or
+                              128 = one tile per SM (the concurrent mode, tile_n
+                              128 and the other reduce schedules always use it) */
     int tile_n;            /* GEMM tile columns: 128 or 256 (default 256) */
     int tile_k;            /* K step per pipeline stage: 64 (only value) */
     int group_m;           /* GROUP_M tile swizzle width in M blocks (default 32) */

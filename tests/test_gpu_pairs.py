@@ -1,0 +1,112 @@
+"""CTA-pair tiles against one-CTA tiles and the oracle.
+
+With tile_m 256 a 2-CTA cluster shares one tensor-core instruction per
+256 x 256 tile: each CTA stages 128 rows of A and 128 columns of B and drains
+its own 128 accumulator rows.  With tile_m 128 every CTA owns a 128 x 256
+tile.  Both must give the same bits (each output element is the same
+K-ordered fp32 accumulation) and, on small-integer inputs, exactly the
+oracle's values.  Row counts are chosen so the odd CTA's half of the last
+pair tile is full, partly below the last row, or wholly below it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gemm_collective_tiles_gb300 import query_status
+from gemm_collective_tiles_gb300.runner import FusedProblem
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_exact(got, want):
+    assert got.shape == want.shape
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+def run(x, tile_m, extra=None):
+    cfg = {"tile_m": tile_m}
+    cfg.update(extra or {})
+    prob = FusedProblem(x.op, x.W, x.M, x.N, x.K, x.dtype, bias=x.bias is not None, config=cfg)
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    return prob.outputs()
+
+
+def oracle_outputs(x):
+    if x.op == "ag_mm":
+        out, g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+        return [out], g
+    if x.op == "mm_rs":
+        return oracle.matmul_reduce_scatter(x.A, x.B, x.bias), None
+    if x.op == "mm_ar":
+        return [oracle.matmul_all_reduce(x.A, x.B, x.bias)], None
+    return [oracle.matmul_all_gather(x.A, x.B[0], x.bias)], None
+
+
+# (op, W, M, N, K): M (or M / W for matmul_all_gather) ends a pair tile with
+# the odd half full (256, 512), partial (200, 300, 129) or empty (100, 60)
+CASES = [
+    ("ag_mm", 4, 100, 512, 256), ("ag_mm", 4, 200, 520, 128), ("ag_mm", 8, 640, 256, 512),
+    ("ag_mm", 2, 129, 264, 64),
+    ("mm_rs", 4, 100, 512, 256), ("mm_rs", 4, 300, 1024, 128), ("mm_rs", 2, 512, 256, 192),
+    ("mm_ar", 2, 60, 256, 128), ("mm_ar", 4, 300, 512, 64), ("mm_ar", 8, 256, 256, 256),
+    ("mm_ag", 4, 4 * 100, 256, 128), ("mm_ag", 2, 2 * 300, 512, 64), ("mm_ag", 8, 8 * 256, 264, 128),
+]
+
+
+@pytest.mark.parametrize("op,W,M,N,K", CASES)
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_pair_tiles_exact_integer(op, W, M, N, K, dt):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, dt, seed=900 + W * 7 + M, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    pair = run(x, 256)
+    single = run(x, 128)
+    want, want_g = oracle_outputs(x)
+    n_out = W if op == "mm_rs" else 1
+    for r in range(n_out):
+        assert_exact(bits(pair["out"][r]), want[r])
+        assert_exact(bits(single["out"][r]), want[r])
+    if want_g is not None:
+        assert_exact(bits(pair["gathered"]), want_g)
+
+
+@pytest.mark.parametrize("op", ["ag_mm", "mm_rs", "mm_ar", "mm_ag"])
+def test_pair_tiles_match_single_cta_random(op):
+    """Random inputs: tile_m 256 and tile_m 128 agree bit for bit."""
+    W = 4
+    M = 4 * 384 if op == "mm_ag" else 640
+    x = synthetic.make_fused_inputs(op, W, M, 768, 512, "bf16", seed=77, dist="normal", scale=0.5,
+                                    bias=True)
+    pair = run(x, 256)
+    single = run(x, 128)
+    for a, b in zip(pair["out"], single["out"]):
+        assert_exact(bits(a), bits(b))
+
+
+def test_pair_tiles_replicated_and_small_grid():
+    """Replicated outputs and a grid of one pair (every tile through the
+    same two CTAs, so both rings wrap many times)."""
+    x = synthetic.make_fused_inputs("mm_ar", 4, 520, 512, 128, "bf16", seed=78, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    want = oracle.matmul_all_reduce(x.A, x.B, x.bias)
+    for extra in ({"replicate_outputs": 1}, {"grid": 2}, {"grid": 3, "group_m": 2}):
+        outs = run(x, 256, extra)
+        for r in range(4 if extra.get("replicate_outputs") else 1):
+            assert_exact(bits(outs["out"][r]), want)
+
+
+def test_pair_tiles_rejected_where_they_do_not_apply():
+    from gemm_collective_tiles_gb300 import _native
+    x = synthetic.make_fused_inputs("mm_rs", 2, 256, 256, 64, "bf16", seed=79, dist="int", scale=2)
+    for extra in ({"tile_n": 128}, {"reduce_mode": 1}, {"reduce_mode": 2}):
+        with pytest.raises(_native.IrisError) as e:
+            run(x, 256, extra)
+        assert e.value.code == _native.IRIS_EINVAL
