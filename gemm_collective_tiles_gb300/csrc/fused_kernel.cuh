@@ -423,10 +423,36 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         return true;
     };
 
+    // all_gather_matmul start-up: before its first GEMM item every scheduler
+    // claims an even share of the gathers the first wave of GEMM items needs,
+    // so those copies run on all SMs at once instead of on the few CTAs whose
+    // first items would otherwise have to claim them (gathers depend on
+    // nothing, so claiming them first is always safe)
+    bool first_gemm = true;
+    auto take_first_share = [&]() -> bool {
+        const uint32_t first_need = gather_need(p, min(p.lookahead, p.n_gemm) - 1);
+        const uint32_t nsched = gridDim.x / CG;
+        const uint32_t share = (first_need + nsched - 1) / nsched;
+        for (uint32_t i = 0; i < share && !comm_dry; ++i) {
+            if (ld_relaxed_gpu(&p.ws->comm_ctr) >= first_need) break;
+            const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
+            if (c >= p.n_comm) {
+                comm_dry = true;
+                break;
+            }
+            if (!publish(ITEM_COMM | c)) return false;
+        }
+        return true;
+    };
+
     // Take one GEMM item (after claiming the gather items it depends on).
     auto take_gemm = [&](bool& got) -> bool {
         got = false;
         if (gemm_dry) return true;
+        if (p.op == OP_AG_MM && first_gemm) {
+            first_gemm = false;
+            if (!take_first_share()) return false;
+        }
         const uint32_t g = atomicAdd(&p.ws->gemm_ctr, 1u);
         if (g >= p.n_gemm) {
             gemm_dry = true;
@@ -1071,12 +1097,14 @@ __device__ __forceinline__ bool wait_count(const Ctl& c, const unsigned long lon
 
 // Chained reduce epilogue (reduce ops, reduce_mode 3): rank s of output tile t
 // waits until ranks 0..s-1 have folded their partials into the fp32 running
-// sum S[t] (tile counter = s), loads S[t] chunk by chunk with TMA, adds its own
-// partial (acc + bias_s) -- so S = ((P_0 + P_1) + P_2) + ... in rank order --
-// and stores S[t] back (s < W-1) or rounds it to the 16-bit output (s = W-1),
-// then advances the counter.  This is a ring reduce-scatter/all-reduce done
-// per tile inside the GEMM epilogues; each wait is on a GEMM item with a
-// smaller index, which was claimed earlier and never waits on this one.
+// sum S[t] (tile counter = s), then folds in its own partial P_s = acc + bias_s,
+// so S = ((P_0 + P_1) + P_2) + ... in rank order: rank 0 stores P_0, a middle
+// rank adds P_s into S[t] with a TMA reduce-add (the add happens at the L2, no
+// read-back), and the last rank loads S[t] chunk by chunk, adds P_{W-1} and
+// rounds to the 16-bit output.  Every rank but the last then advances the
+// counter.  This is a ring reduce-scatter/all-reduce done per tile inside the
+// GEMM epilogues; each wait is on a GEMM item with a smaller index, which was
+// claimed earlier and never waits on this one.
 template <int BN, int STAGES, int CG>
 __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem, uint32_t g,
                                uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
@@ -1126,7 +1154,10 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         mbar_arrive_expect_tx(&lbar[ci & 1], 32 * 32 * 4);
         tma_load_4d(stg_base + (ci & 1) * 4096, &p.tmS, colbase + ci * 32, c_row, 0, 0, &lbar[ci & 1]);
     };
-    if (s > 0 && nch > 0 && wc.lane == 0) issue_load(0);
+    // only the last rank reads the running sum: the middle ranks add their
+    // partial into it at the L2 (TMA reduce-add), in the same rank order
+    const bool reads_sum = last && s > 0;
+    if (reads_sum && nch > 0 && wc.lane == 0) issue_load(0);
 #pragma unroll 1
     for (int ci = 0; ci < nch; ++ci) {
         uint8_t* stg = stg_base + (ci & 1) * 4096;
@@ -1139,7 +1170,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
             for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
         const int col0 = colbase + ci * 32;
-        if (s > 0 && ci + 1 < nch && wc.lane == 0) issue_load(ci + 1);
+        if (reads_sum && ci + 1 < nch && wc.lane == 0) issue_load(ci + 1);
         // P_s = acc + bias_s (fp32)
         float x[32];
 #pragma unroll
@@ -1161,7 +1192,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
                 }
             }
         }
-        if (s > 0) {
+        if (reads_sum) {
             // S_new = S_old + P_s (S_old holds ranks 0..s-1 in order)
             int ok = 1;
             if (wc.lane == 0) {
@@ -1202,8 +1233,10 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         fence_proxy_async_shared();
         __syncwarp();
         if (wc.lane == 0) {
-            if (!last) {
+            if (!last && s == 0) {
                 tma_store_4d(&p.tmS, stg, col0, c_row, 0, 0);
+            } else if (!last) {
+                tma_reduce_add_4d(&p.tmS, stg, col0, c_row, 0, 0);  // S += P_s
             } else if (p.op == OP_MM_RS) {
                 const int rr = col0 / p.N_local;
                 tma_store_4d(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0);
@@ -1247,23 +1280,27 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
                        static_cast<size_t>(mb) * BM * vpr;
     uint4* dst = reinterpret_cast<uint4*>(p.heap + p.off_gathered) + static_cast<size_t>(mb) * BM * Kv +
                  static_cast<size_t>(s) * vpr;
-    // warp w copies rows w, w+8, ...; lanes walk the row's 16-byte vectors
-    constexpr int RU = 2, CU = 4;
-    for (int r0 = wc.w; r0 < rows; r0 += NUM_WORKER_WARPS * RU) {
-        for (int v0 = wc.lane; v0 < vpr; v0 += 32 * CU) {
-            uint4 v[RU][CU];
+    // The shard block (rows x vpr vectors, contiguous) is copied as one flat
+    // range: thread t takes vectors t, t + 128, ...; U loads per thread are in
+    // flight before their stores (32 KB per CTA), whatever the row length.
+    constexpr int U = 16;
+    constexpr int NT = NUM_WORKER_WARPS * 32;
+    const int tid = wc.w * 32 + wc.lane;
+    const int total = rows * vpr;
+    for (int base = 0; base < total; base += NT * U) {
+        uint4 v[U];
 #pragma unroll
-            for (int u = 0; u < RU; ++u)
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * NT + tid;
+            if (i < total) v[u] = src[i];
+        }
 #pragma unroll
-                for (int k = 0; k < CU; ++k)
-                    if (r0 + u * NUM_WORKER_WARPS < rows && v0 + 32 * k < vpr)
-                        v[u][k] = src[static_cast<size_t>(r0 + u * NUM_WORKER_WARPS) * vpr + v0 + 32 * k];
-#pragma unroll
-            for (int u = 0; u < RU; ++u)
-#pragma unroll
-                for (int k = 0; k < CU; ++k)
-                    if (r0 + u * NUM_WORKER_WARPS < rows && v0 + 32 * k < vpr)
-                        dst[static_cast<size_t>(r0 + u * NUM_WORKER_WARPS) * Kv + v0 + 32 * k] = v[u][k];
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * NT + tid;
+            if (i < total) {
+                const int r = i / vpr;
+                dst[static_cast<size_t>(r) * Kv + (i - r * vpr)] = v[u];
+            }
         }
     }
     fence_proxy_async_global();

@@ -148,6 +148,16 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* s
         "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src))
         : "memory");
 }
+// 4-D tiled reduce-add of one box from shared memory into global memory
+// (element type from the tensor map; performed at the L2; bulk-group completion)
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, const void* smem_src, int c0, int c1,
+                                                  int c2, int c3) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src))
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until every committed bulk store has finished READING shared memory
 __device__ __forceinline__ void bulk_wait_read_all() {
