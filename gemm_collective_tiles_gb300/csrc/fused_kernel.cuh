@@ -309,18 +309,37 @@ __device__ __forceinline__ int own_block(const Params& p, const GemmCoord& gc, i
     return mb * CG + half;
 }
 
-// all_gather_matmul: number of gather items (ordered m-block by m-block, W
-// shards each) that must be claimed before GEMM item x may be published: all
-// shards of every m-block up to x's own.  Inside a swizzle group the first
-// items visit the group's m-blocks in order, so the need grows one m-block per
-// item there and stays at the whole group afterwards (monotonic in x).
+// all_gather_matmul gather items are numbered swizzle group by swizzle group
+// (the groups of group_m m-blocks the GEMM order walks through) and, inside a
+// group, shard-major: item = first_m * W + s * gsz + (mb - first_m).  Every
+// m-block's shard 0 comes before any shard 1, so with the gathers spread over
+// all CTAs the first K-blocks of the group's tiles arrive first.
+struct GatherCoord {
+    int mb, s;
+};
+__device__ __forceinline__ GatherCoord decode_gather(const Params& p, uint32_t c) {
+    const uint32_t per_group = static_cast<uint32_t>(p.group_m) * p.W;
+    const int first_m = static_cast<int>(c / per_group) * p.group_m;
+    const int gsz = min(p.m_blocks - first_m, p.group_m);
+    const int local = static_cast<int>(c - static_cast<uint32_t>(first_m) * p.W);
+    GatherCoord gc;
+    gc.s = local / gsz;
+    gc.mb = first_m + (local - gc.s * gsz);
+    return gc;
+}
+
+// Number of gather items that must be claimed before GEMM item x may be
+// published: every item of the groups before x's, and in x's group the items
+// up to shard W-1 of x's m-block.  Inside a group the GEMM order first visits
+// its m-blocks in order, so the need grows by one per item there and stays at
+// the whole group afterwards (monotonic in x).
 __device__ __forceinline__ uint32_t gather_need(const Params& p, uint32_t x) {
     const uint32_t group_size = static_cast<uint32_t>(p.group_m) * p.n_blocks;
     const uint32_t group = x / group_size;
     const int first_m = static_cast<int>(group) * p.group_m;
     const int gsz = min(p.m_blocks - first_m, p.group_m);
     const int local = static_cast<int>(x - group * group_size);
-    return static_cast<uint32_t>(first_m + min(local, gsz - 1) + 1) * p.W;
+    return static_cast<uint32_t>(first_m) * p.W + static_cast<uint32_t>((p.W - 1) * gsz + min(local, gsz - 1) + 1);
 }
 
 __device__ __forceinline__ float bits16_to_float(uint32_t b, int bf16) {
@@ -1109,11 +1128,22 @@ template <int BN, int STAGES, int CG>
 __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem, uint32_t g,
                                uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
+    const GemmCoord gc = decode_gemm(p, g);
+    const int blk = own_block<CG>(p, gc, ctl.half);
+    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
+    constexpr int NCH = COLS / 32;
+    const int c_row = blk * BM + wc.q * 32;
+    const int colbase = gc.nb * BN + wc.h * COLS;
+    // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
+    const int nch = max(0, min(NCH, (p.N - colbase) / 32));
+    if (gc.rank == p.W - 1 && gc.rank > 0 && blk * BM < p.M && wc.lane == 0) {
+        // the last rank will read this warp's running-sum rows: pull them into
+        // L2 while the tile's MMAs still run
+        for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, 0, 0);
+    }
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
     tr.rec(EV_READY, g);
-    const GemmCoord gc = decode_gemm(p, g);
-    const int blk = own_block<CG>(p, gc, ctl.half);
     if (CG == 2 && blk * BM >= p.M) {
         // this CTA's half of the pair tile lies below the last row: no
         // partial, no sum; release the accumulator in step with the pair
@@ -1139,15 +1169,9 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
         if (wc.lane == 0) fence_proxy_async_global();  // S[t] was written by the TMA of another SM
     }
-    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
-    constexpr int NCH = COLS / 32;
     const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
     uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
     uint64_t* lbar = sm.sbar + 2 * wc.w;
-    const int c_row = blk * BM + wc.q * 32;
-    const int colbase = gc.nb * BN + wc.h * COLS;
-    // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
-    const int nch = max(0, min(NCH, (p.N - colbase) / 32));
     auto issue_load = [&](int ci) {
         // the staging half must be free: earlier stores have read it
         bulk_wait_read_all();
@@ -1271,7 +1295,8 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
                             WorkerCtx& wc) {
     // CTA pairs: both CTAs run the item, each copying (and flagging) its own
     // block of BM rows of the pair's m-block
-    const int mb = static_cast<int>(c / p.W) * CG + ctl.half, s = static_cast<int>(c % p.W);
+    const GatherCoord gq = decode_gather(p, c);
+    const int mb = gq.mb * CG + ctl.half, s = gq.s;
     if (mb * BM >= p.M) return true;  // below the last row: nothing to copy, no consumer
     const int rows = min(BM, p.M - mb * BM);
     const int vpr = p.K_local / 8;  // 16-byte vectors per shard row

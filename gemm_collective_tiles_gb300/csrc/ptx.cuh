@@ -113,6 +113,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
         : "memory");
 }
 
+// bring one box of a 4-D tensor into L2 (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // 4-D tiled load of one box into shared memory, completing on `bar` (tx bytes)
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m, int c0, int c1, int c2,
                                             int c3, uint64_t* bar) {
