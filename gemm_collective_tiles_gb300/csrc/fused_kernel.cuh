@@ -1487,9 +1487,12 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         dst_base = p.off_cout + b0;
         dst_all = (p.coll == COLL_AR);
     }
-    // the warp's contiguous slice (16-byte granules) of [b0, b1), as offsets from b0
+    // the warp's contiguous slice (16-byte granules) of [b0, b1), as offsets
+    // from b0; a CTA pair runs the item together, one slice per worker warp
+    // of either CTA
     const size_t g_tot = (b1 - b0) / 16;
-    const size_t g_lo = g_tot * wc.w / NUM_WORKER_WARPS, g_hi = g_tot * (wc.w + 1) / NUM_WORKER_WARPS;
+    const size_t ww = static_cast<size_t>(ctl.half * NUM_WORKER_WARPS + wc.w), nww = CG * NUM_WORKER_WARPS;
+    const size_t g_lo = g_tot * ww / nww, g_hi = g_tot * (ww + 1) / nww;
     const uint32_t sub = (HALF / src_n) & ~15u;  // bytes per source per sub-chunk
     const size_t s_lo = g_lo * 16, s_hi = g_hi * 16;
     const int nsub = static_cast<int>((s_hi - s_lo + sub - 1) / sub);

@@ -155,8 +155,7 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     std::memset(&z, 0, sizeof(z));
     if (!c) c = &z;
     if (c->tile_m != 0 && c->tile_m != BM && c->tile_m != 2 * BM) return IRIS_EINVAL;
-    if (c->tile_m == 2 * BM && (op == IRIS_OP_CONCURRENT || (c->tile_n != 0 && c->tile_n != 256)))
-        return IRIS_EINVAL;
+    if (c->tile_m == 2 * BM && c->tile_n != 0 && c->tile_n != 256) return IRIS_EINVAL;
     out.tile_m = c->tile_m;
     out.cg = 1;
     if (c->tile_k != 0 && c->tile_k != BK) return IRIS_EINVAL;
@@ -208,14 +207,15 @@ int resolve_reduce_mode(const iris_b200_config* c, iris_op op, int64_t N, int W)
     return -1;
 }
 
-// CTA pairs (tile_m 256) wherever they apply: every op but the concurrent
-// mode, 256-wide tiles, and the chained schedule for the reduce ops.  The
-// default is pairs; tile_m 128 keeps one CTA per tile.  The pair grid is every
+// CTA pairs (tile_m 256) wherever they apply: 256-wide tiles, the chained
+// schedule for the reduce ops, and a GEMM in the launch (a collective-only
+// launch of the concurrent mode keeps one CTA per item).  The default is
+// pairs; tile_m 128 keeps one CTA per tile.  The pair grid is every
 // co-resident pair (at most grid / 2).
-int resolve_pair(Cfg& c, iris_op op) {
+int resolve_pair(Cfg& c, iris_op op, bool has_gemm = true) {
     const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
-    const bool applies = op != IRIS_OP_CONCURRENT && c.tile_n == BN_WIDE && (!reduce_op || c.reduce_mode == 3);
-    if (c.tile_m == 2 * BM && !applies) return IRIS_EINVAL;
+    const bool applies = has_gemm && c.tile_n == BN_WIDE && (!reduce_op || c.reduce_mode == 3);
+    if (c.tile_m == 2 * BM && !applies && has_gemm) return IRIS_EINVAL;
     c.cg = (c.tile_m == BM || !applies) ? 1 : 2;
     if (c.cg == 2) {
         const int pairs = std::min(pair_clusters(), c.grid / 2);
@@ -636,6 +636,8 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
         c.grid = grid;
         c.gemm_ctas = part == 1 ? grid : 0;
     }
+    const bool launch_gemm = has_gemm && part != 2;
+    if ((rc = resolve_pair(c, IRIS_OP_CONCURRENT, launch_gemm))) return rc;
     if (count > 0) {
         if (size_t(c.comm_block) * esz % 16 != 0) return IRIS_EALIGN;
         const size_t in_bytes = size_t(count) * esz;
@@ -661,7 +663,7 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
              : coll == IRIS_COLL_ALL_TO_ALL    ? COLL_A2A
                                                : COLL_BC;
     p.root = c.root;
-    const int mblocks = static_cast<int>(cdiv(M, BM));
+    const int mblocks = static_cast<int>(cdiv(M, BM * c.cg));
     fill_geometry(p, M, N, K, mblocks, c);
     p.mb_per_rank = mblocks;
     p.C = C;

@@ -94,10 +94,13 @@ typedef enum {
 typedef struct {
     int tile_m;            /* GEMM tile rows: 256 = one tile per pair of SMs (a
                               2-CTA cluster sharing the tensor-core instruction;
-                              the default wherever it applies: all ops but the
-                              concurrent mode, tile_n 256, chained reduce), or
-                              128 = one tile per SM (the concurrent mode, tile_n
-                              128 and the other reduce schedules always use it) */
+                              the default wherever it applies: tile_n 256, the
+                              chained reduce schedule, a launch with a GEMM), or
+                              128 = one tile per SM (tile_n 128, the other reduce
+                              schedules and collective-only launches always use
+                              it).  With pairs, a CTA split (gemm_ctas) is taken
+                              per pair: the pair whose even CTA is below gemm_ctas
+                              prefers the GEMM queue. */
     int tile_n;            /* GEMM tile columns: 128 or 256 (default 256) */
     int tile_k;            /* K step per pipeline stage: 64 (only value) */
     int group_m;           /* GROUP_M tile swizzle width in M blocks (default 32) */

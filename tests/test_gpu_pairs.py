@@ -110,3 +110,39 @@ def test_pair_tiles_rejected_where_they_do_not_apply():
         with pytest.raises(_native.IrisError) as e:
             run(x, 256, extra)
         assert e.value.code == _native.IRIS_EINVAL
+
+
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter", "all_gather", "all_to_all", "broadcast"])
+def test_pair_tiles_concurrent_mode(coll):
+    """Concurrent mode with CTA pairs: both CTAs of a pair run each collective
+    item (one slice per worker warp of either CTA) on their leased stages.
+    GEMM bits equal the one-CTA run's; the collective is bit-exact."""
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem
+    W, count = 4, 5 * 16384 + 4096
+    M, N, K = 520, 768, 256   # ragged M: the last pair tile's odd half is partial
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=95, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=96)
+    outs = {}
+    for tile_m in (256, 128):
+        prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count,
+                                 config={"tile_m": tile_m, "comm_block": 16384, "gemm_ctas": 60})
+        prob.upload(A, B, X)
+        prob.poison_outputs()
+        prob.run()
+        assert query_status(prob.ws)[0] == 0
+        outs[tile_m] = prob.outputs()
+    assert_exact(bits(outs[256]["C"]), oracle.gemm(A, B))
+    assert_exact(bits(outs[256]["C"]), bits(outs[128]["C"]))
+    if coll == "all_reduce":
+        want = [oracle.all_reduce(X)] * W
+    elif coll == "reduce_scatter":
+        want = oracle.reduce_scatter(X)
+    elif coll == "all_gather":
+        want = [oracle.all_gather(X)] * W
+    elif coll == "all_to_all":
+        want = oracle.all_to_all(X)
+    else:
+        want = oracle.broadcast(X, 0)
+    for r in range(W):
+        got = outs[256]["x"][r].contiguous().view(torch.uint8).numpy()
+        assert np.array_equal(got, np.ascontiguousarray(want[r]).view(np.uint8).reshape(-1)), f"rank {r}"
