@@ -408,7 +408,9 @@ def run_shape_sweep(args, cfg):
     path it replaces: the gather as one torch.cat of the W K-shards, then a
     cuBLAS matmul.  Prints one JSON row per shape, then a summary line.
     Both arms write into the same region-0 buffers; the fused output of a
-    sampled row block is compared with cuBLAS's before the latter overwrites it."""
+    sampled row block is compared with cuBLAS's before the latter overwrites it.
+    Each arm is timed as the median of back-to-back calls (L2 flushed before
+    every call), like the bench line."""
     from gemm_collective_tiles_gb300 import query_status
     from gemm_collective_tiles_gb300.runner import FusedProblem
     torch.cuda.set_device(0)
@@ -421,19 +423,19 @@ def run_shape_sweep(args, cfg):
     rows = []
 
     def timed(fn, reps, warm=2):
+        # back to back like the bench line: an L2 flush, then the timed call,
+        # with no host synchronisation (and no idle GPU) between calls
         for _ in range(warm):
             fn()
         torch.cuda.synchronize()
-        ms = []
-        for _ in range(reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in ev:
             flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
             e1.record(stream)
-            torch.cuda.synchronize()
-            ms.append(e0.elapsed_time(e1))
-        return statistics.median(ms)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
 
     for idx, (label, M, N, K) in enumerate(synthetic.AG_MM_SHAPES):
         if only and label not in only:

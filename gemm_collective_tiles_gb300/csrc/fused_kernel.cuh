@@ -103,7 +103,8 @@ struct Params {
     uint32_t n_gemm, n_comm;
     uint32_t n_parts;    // reduce ops, distributed parts schedule: output tiles x W row parts
     int gemm_ctas;    // CTAs preferring GEMM; < 0 = balanced
-    uint32_t lookahead;
+    uint32_t lookahead;  // all_gather_matmul: GEMM items ahead whose gathers are claimed early
+    uint32_t first_wave; // GEMM items of the first wave (one per CTA or CTA pair)
     char* heap;
     unsigned long long rank_stride;
     unsigned long long off_A, off_out, off_bias, off_gathered, off_in, off_cout;
@@ -449,7 +450,7 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
     // nothing, so claiming them first is always safe)
     bool first_gemm = true;
     auto take_first_share = [&]() -> bool {
-        const uint32_t first_need = gather_need(p, min(p.lookahead, p.n_gemm) - 1);
+        const uint32_t first_need = gather_need(p, min(p.first_wave, p.n_gemm) - 1);
         const uint32_t nsched = gridDim.x / CG;
         const uint32_t share = (first_need + nsched - 1) / nsched;
         for (uint32_t i = 0; i < share && !comm_dry; ++i) {
@@ -479,8 +480,10 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         }
         if (p.op == OP_AG_MM) {
             // gathers g itself needs are claimed before g (mandatory); gathers
-            // for items up to `lookahead` ahead are claimed at most
-            // GATHER_AHEAD per GEMM item, so they spread over many CTAs
+            // for items up to `lookahead` (one swizzle group) ahead are claimed
+            // at most GATHER_AHEAD per GEMM item, so the next group's gathers
+            // spread over many CTAs and run in the background of the current
+            // group's tiles instead of in a burst at the group boundary
             const uint32_t need = gather_need(p, g);
             const uint32_t need_ahead = gather_need(p, min(g + p.lookahead, p.n_gemm - 1));
             int ahead = 0;
@@ -1317,14 +1320,15 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = base + u * NT + tid;
-            if (i < total) v[u] = src[i];
+            if (i < total) v[u] = __ldcs(src + i);  // read once: evict-first
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = base + u * NT + tid;
             if (i < total) {
                 const int r = i / vpr;
-                dst[static_cast<size_t>(r) * Kv + (i - r * vpr)] = v[u];
+                // not re-read until its GEMM tiles run: evict-first
+                __stcs(dst + static_cast<size_t>(r) * Kv + (i - r * vpr), v[u]);
             }
         }
     }

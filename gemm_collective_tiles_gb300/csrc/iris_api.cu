@@ -315,7 +315,10 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.group_m = std::max(1, c.group_m / c.cg);
     p.n_tiles = p.m_blocks * p.n_blocks;
     p.gemm_ctas = c.gemm_ctas;
-    p.lookahead = static_cast<uint32_t>(c.grid / c.cg);
+    p.first_wave = static_cast<uint32_t>(c.grid / c.cg);
+    // all_gather_matmul claims a swizzle group's gathers while the group before
+    // it runs (measured: long-K shapes lose ~20 % with a one-wave look-ahead)
+    p.lookahead = static_cast<uint32_t>(p.group_m) * p.n_blocks;
     p.replicate = c.replicate;
     p.bias_on_m = c.bias_on_m;
     p.wait_ns = c.wait_ns;
