@@ -177,8 +177,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->gemm_ctas < -1 || c->gemm_ctas > out.grid) return IRIS_EINVAL;
     if (c->gemm_ctas != 0)
         out.gemm_ctas = c->gemm_ctas;
-    else  // concurrent: 55% of the CTAs prefer the GEMM (measured best split); others: all
-        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? std::max(1, (out.grid * 55 + 50) / 100) : out.grid;
+    else  // concurrent: 65% of the CTAs prefer the GEMM (measured best split with CTA pairs); others: all
+        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? std::max(1, (out.grid * 65 + 50) / 100) : out.grid;
     out.wait_ns = c->wait_ns ? c->wait_ns : DEFAULT_WAIT_NS;
     if (c->debug_skip_flag < 0) return IRIS_EINVAL;
     out.debug_skip = static_cast<uint32_t>(c->debug_skip_flag);

@@ -10,9 +10,9 @@ queue is empty takes from the other).  All-reduce tiles read and write every
 rank (2W transfers per tile), so they need the most CTAs to saturate memory;
 the other collectives move fewer bytes per tile.
 
-Constants are calibrated on GB300 measurements of this library (the pure GEMM
-of the concurrent path and the stand-alone all-reduce); they can be replaced
-by the caller.
+Constants are calibrated on GB300 measurements of this library (the GEMM and
+the all-reduce of the concurrent path, each timed alone on 8 to 152 CTAs);
+they can be replaced by the caller.
 """
 from __future__ import annotations
 
@@ -25,8 +25,8 @@ from typing import Dict, List, Optional, Sequence
 @dataclasses.dataclass
 class Machine:
     sms: int = 152
-    gemm_tflops_per_sm: float = 10.3      # 1.57 PFLOP/s bf16 over 152 SMs
-    comm_gbs_per_sm: float = 80.0         # one SM's collective engine alone
+    gemm_tflops_per_sm: float = 11.9      # CTA-pair GEMM 8192^3 bf16 at 1.81 PFLOP/s over 152 SMs
+    comm_gbs_per_sm: float = 65.0         # one CTA's collective engine (all-reduce, linear up to ~96 CTAs)
     hbm_gbs: float = 6774.0               # measured copy bandwidth
     gemm_hbm_share: float = 0.12          # HBM fraction the GEMM operands use when all SMs run it
     tile_overhead_us: float = 1.0         # claim + pipeline fill per tile

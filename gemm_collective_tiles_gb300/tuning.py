@@ -100,7 +100,7 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
             for d in predictor.predict_split(wl, m=predictor.Machine(sms=sm_count), top_k=4):
                 out.insert(1, {"gemm_ctas": d["gemm_ctas"]})
         else:
-            for frac in (0.55, 0.45, 0.65, 0.35, 0.75):
+            for frac in (0.65, 0.55, 0.75, 0.45, 0.85):
                 out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
     # drop duplicates, keep order
     seen, uniq = set(), []

@@ -107,7 +107,7 @@ typedef struct {
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
                               other queue when its own runs dry.  0 = op default
-                              (concurrent: 55% of the grid; the dependent ops: all
+                              (concurrent: 65% of the grid; the dependent ops: all
                               CTAs); -1 = balanced (every CTA draws from both queues
                               so that both finish together). */
     int stages;            /* reserved: pipeline depth is fixed per tile_n */
