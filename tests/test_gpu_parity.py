@@ -173,6 +173,29 @@ def test_mm_all_reduce_random_bias_on_m():
                  "bf16")
 
 
+@pytest.mark.parametrize("tile_m", [256, 128])
+def test_mm_reduce_scatter_subnormal_partials(tile_m):
+    """Partials that are fp32 subnormals (entries +-{0,1,2} x 2^-70, products
+    near 2^-140): the tensor-core accumulation, the middle ranks' reduce-adds
+    at the L2 and the last rank's add all keep them, so the outputs (bf16, which
+    shares fp32's exponent range) equal the oracle's bit for bit."""
+    W, M, N, K = 4, 256, 256, 64
+    g = torch.Generator().manual_seed(5)
+
+    def tiny(shape):
+        sign = torch.randint(0, 2, shape, generator=g).float() * 2 - 1
+        mag = torch.randint(0, 3, shape, generator=g).float()
+        return (sign * mag * 2.0 ** -70).to(torch.bfloat16)
+    A = [tiny((M, K)) for _ in range(W)]
+    B = [tiny((K, N)) for _ in range(W)]
+    x = synthetic.FusedInputs("mm_rs", W, M, N, K, "bf16", A, B, None)
+    _, outs = run_fused(x, config={"tile_m": tile_m})
+    want = oracle.matmul_reduce_scatter(A, B, None)
+    assert sum(int((w & 0x7FFF != 0).sum()) for w in want) > 500   # the case is not all zeros
+    for r in range(W):
+        assert_exact(bits(outs["out"][r]), want[r])
+
+
 def test_rs_slices_concatenate_to_ar():
     """The two reduce ops agree bit for bit (same partials, same order)."""
     x = synthetic.make_fused_inputs("mm_rs", 4, 256, 512, 128, "bf16", seed=44, dist="normal",
