@@ -42,6 +42,22 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_NAME = "fused_gemm_coll_kernel"
 OP_NAMES = {"ag_mm": "all_gather_matmul", "mm_rs": "matmul_reduce_scatter",
             "mm_ag": "matmul_all_gather", "mm_ar": "matmul_all_reduce"}
+# Published all_gather_matmul TFLOPS for the same shapes at world size 8
+# (ROCm/iris PR #506, "Performance (ws=8, MI300X)" table): another GPU, so
+# vs_baseline is context, not a target.  The pages publish no numbers for the
+# other ops or the concurrent mode.
+PAGES_TFLOPS_MI300X = {
+    ("ag_mm", 8, 131072, 16384, 16384): 420.5, ("ag_mm", 8, 147456, 28672, 4096): 466.5,
+    ("ag_mm", 8, 327680, 28672, 4096): 474.7, ("ag_mm", 8, 229376, 28672, 4096): 471.5,
+    ("ag_mm", 8, 8192, 8192, 262144): 161.6, ("ag_mm", 8, 262144, 8192, 8192): 253.0,
+    ("ag_mm", 8, 16384, 16384, 131072): 314.5, ("ag_mm", 8, 262144, 28672, 8192): 442.1,
+    ("ag_mm", 8, 196608, 18432, 16384): 445.4, ("ag_mm", 8, 4096, 14336, 4096): 248.9,
+    ("ag_mm", 8, 4096, 11008, 4096): 189.8, ("ag_mm", 8, 4096, 4096, 4096): 90.9,
+}
+
+
+def pages_tflops(op, W, M, N, K):
+    return PAGES_TFLOPS_MI300X.get((op, W, M, N, K))
 
 
 # ------------------------------------------------------------------ helpers
@@ -291,6 +307,50 @@ def workload_config(wl, name, cfg):
     return d
 
 
+def library_reference(prob, wl, stream, flush):
+    """The same op done the plain sequential way with library calls on the same
+    device data: cuBLAS GEMMs (16-bit outputs, as torch.matmul gives) plus
+    torch cat / sum / slice for the collective part.  Run-only (its results
+    are not checked); timed like the bench line, back to back with an L2 flush
+    before every call."""
+    op, W = wl["op"], wl["W"]
+    A = [prob.heap.view(prob.A, r) for r in range(W)]
+    B = [prob.heap.view(prob.B, r if prob.per_rank_b() else 0) for r in range(W)]
+    bias = prob.heap.view(prob.bias, 0) if prob.bias is not None else None
+
+    def add_bias(x):
+        return x if bias is None else x + bias
+
+    if op == "ag_mm":
+        def fn():
+            return add_bias(torch.cat(A, dim=1) @ B[0])
+        what = "torch.cat of the W shards, then one cuBLAS matmul"
+    elif op == "mm_ag":
+        def fn():
+            return torch.cat([add_bias(a @ B[0]) for a in A], dim=0)
+        what = "W cuBLAS matmuls, then torch.cat along M"
+    else:
+        def fn():
+            s = torch.stack([add_bias(A[r] @ B[r]).float() for r in range(W)]).sum(0)
+            return torch.chunk(s.to(A[0].dtype), W, dim=1) if op == "mm_rs" else s.to(A[0].dtype)
+        what = "W cuBLAS matmuls (16-bit partials), fp32 torch.sum over ranks, " + (
+            "split along N" if op == "mm_rs" else "rounded once")
+    flops = prob.flops()
+    reps = max(3, min(20, int(2e16 / flops)))
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    return {"what": what, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "reps": reps}
+
+
 def run_concurrent(args, cfg):
     """Independent GEMM (bf16 8192^3, normal(0,1), seed 3) sharing the SMs with
     an all-reduce of W=8 fp32 buffers of 64Mi elements (uniform[-1,1], seed 4).
@@ -474,7 +534,8 @@ def run_shape_sweep(args, cfg):
         rows.append({"shape": label, "M": M, "N": N, "K": K, "ms": ms_fused, "tflops": tf,
                      "frac_of_peak": tf / peak, "cat_cublas_ms": ms_seq,
                      "cat_cublas_tflops": flops / (ms_seq * 1e-3) / 1e12, "speedup": ms_seq / ms_fused,
-                     "max_rel_diff_vs_cublas": rel, "reps": reps, "wall_s": time.perf_counter() - t0})
+                     "max_rel_diff_vs_cublas": rel, "reps": reps, "wall_s": time.perf_counter() - t0,
+                     "pages_mi300x_tflops": pages_tflops("ag_mm", W, M, N, K)})
         print(json.dumps(rows[-1]), flush=True)
         del prob, shards, B0, out0, gath0
         torch.cuda.empty_cache()
@@ -641,6 +702,7 @@ def main():
     if rc[0] != 0:
         raise RuntimeError(f"device status after e2e steps: {rc}")
 
+    lib_ref = library_reference(prob, wl, stream, flush)
     if rank != 0:
         return 0
     cpu = None
@@ -650,11 +712,13 @@ def main():
     cfg_out = workload_config(wl, args.workload, cfg)
     cfg_out["l2"] = "flushed before every step (258 MB memset outside the step's events)"
     cfg_out["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU"
+    base = pages_tflops(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"])
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic", "config": cfg_out,
+            "vs_baseline": (value / world / base) if base else None, "dtype": wl["dtype"], "data": "synthetic",
+            "config": cfg_out,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K,
-            "clocks": clocks, "wall_s_timed_region": wall}
+            "clocks": clocks, "wall_s_timed_region": wall, "library_reference": lib_ref}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
