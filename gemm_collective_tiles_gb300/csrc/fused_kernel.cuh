@@ -102,6 +102,7 @@ struct Params {
     int m_blocks, mb_per_rank, n_blocks, k_blocks, group_m, n_tiles;
     uint32_t n_gemm, n_comm;
     uint32_t n_parts;    // reduce ops, distributed parts schedule: output tiles x W row parts
+    uint32_t g_split;    // first GEMM item that is a column half of a split tail tile (n_gemm: none)
     int gemm_ctas;    // CTAs preferring GEMM; < 0 = balanced
     uint32_t lookahead;  // all_gather_matmul: GEMM items ahead whose gathers are claimed early
     uint32_t first_wave; // GEMM items of the first wave (one per CTA or CTA pair)
@@ -266,12 +267,25 @@ __device__ __forceinline__ void swizzle_tile(const Params& p, uint32_t t, int& m
 struct GemmCoord {
     int rank, mb, nb;
     uint32_t tile;
+    int hn;  // -1: the whole tile; 0 / 1: column half of a split tail tile
 };
+// GEMM items from g_split on are the column halves of the last tiles (the
+// launch's final, partly empty wave split in two, so it takes half a tile's
+// time): item g_split + 2i + h is half h of tile g_split + i.
+__device__ __forceinline__ uint32_t tile_item(const Params& p, uint32_t g, int& hn) {
+    if (g < p.g_split) {
+        hn = -1;
+        return g;
+    }
+    hn = static_cast<int>((g - p.g_split) & 1u);
+    return p.g_split + ((g - p.g_split) >> 1);
+}
 __device__ __forceinline__ uint32_t group_tiles(const Params& p) {
     return static_cast<uint32_t>(p.group_m) * p.n_blocks;
 }
-__device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t g) {
+__device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t item) {
     GemmCoord gc;
+    const uint32_t g = tile_item(p, item, gc.hn);
     if (p.op == OP_MM_RS || p.op == OP_MM_AR) {
         if (p.rank_inner) {
             gc.tile = g / p.W;
@@ -380,7 +394,7 @@ struct Smem {
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
-    uint32_t* bcast;
+    uint32_t* spare;  // two unused words (keeps the carve's word offsets)
     uint32_t* ready_bits;
 
     __device__ void carve(uint8_t* raw) {
@@ -404,7 +418,7 @@ struct Smem {
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
-        bcast = u + RING + 2;
+        spare = u + RING + 2;
         ready_bits = u + RING + 4;
 
     }
@@ -484,8 +498,9 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
             // at most GATHER_AHEAD per GEMM item, so the next group's gathers
             // spread over many CTAs and run in the background of the current
             // group's tiles instead of in a burst at the group boundary
-            const uint32_t need = gather_need(p, g);
-            const uint32_t need_ahead = gather_need(p, min(g + p.lookahead, p.n_gemm - 1));
+            int hn_unused;
+            const uint32_t need = gather_need(p, tile_item(p, g, hn_unused));
+            const uint32_t need_ahead = gather_need(p, tile_item(p, min(g + p.lookahead, p.n_gemm - 1), hn_unused));
             int ahead = 0;
             while (!comm_dry) {
                 const uint32_t head = ld_relaxed_gpu(&p.ws->comm_ctr);
@@ -642,14 +657,18 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             } else {
                 // both CTAs' boxes count on the even CTA's full barrier, which
                 // expects the pair's bytes (the odd CTA's may land first: the
-                // transaction count may dip below zero inside a phase)
-                if (ctl.half == 0) mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES, CG>::STAGE_BYTES * CG);
+                // transaction count may dip below zero inside a phase).  A
+                // column half (N = BN / 2) loads one 64-column box per CTA.
+                constexpr uint32_t HALF_BYTES = Smem<BN, STAGES, CG>::A_BYTES + Smem<BN, STAGES, CG>::B_BYTES / 2;
+                const bool hn = gc.hn >= 0;
+                if (ctl.half == 0)
+                    mbar_arrive_expect_tx(&sm.full[stage], (hn ? HALF_BYTES : Smem<BN, STAGES, CG>::STAGE_BYTES) * CG);
                 const uint32_t fb = mapa_shared(&sm.full[stage], 0);
                 tma_load_3d_pair(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, fb);
-#pragma unroll
-                for (int c = 0; c < BN / CG / 64; ++c)
-                    tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB,
-                                     gc.nb * BN + ctl.half * (BN / CG) + c * 64, kb * BK, b_rank, fb);
+                const int bcol = gc.nb * BN + (hn ? gc.hn * (BN / 2) + ctl.half * (BN / 4) : ctl.half * (BN / CG));
+                const int nbox = hn ? BN / 4 / 64 : BN / CG / 64;
+                for (int c = 0; c < nbox; ++c)
+                    tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, bcol + c * 64, kb * BK, b_rank, fb);
             }
             issued_phase[stage] = phase;
             used_mask |= 1u << stage;
@@ -698,10 +717,12 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
 // ============================================================ MMA issuer
 template <int BN, int STAGES, int CG>
 __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem) {
-    // CTA pairs: one instruction covers the pair's (2 BM) x BN tile
+    // CTA pairs: one instruction covers the pair's (2 BM) x BN tile (x BN/2
+    // for the column half of a split tail tile)
     constexpr uint32_t IDESC_F16 = make_idesc(0, BM * CG, BN);
     constexpr uint32_t IDESC_BF16 = make_idesc(1, BM * CG, BN);
-    const uint32_t idesc = p.bf16 ? IDESC_BF16 : IDESC_F16;
+    constexpr uint32_t IDESC_F16_H = make_idesc(0, BM * CG, BN / 2);
+    constexpr uint32_t IDESC_BF16_H = make_idesc(1, BM * CG, BN / 2);
     Tracer tr;
     tr.init(p, TR_MMA);
     uint32_t stage = 0, phase = 0, ring_n = 0, acc_i = 0;
@@ -714,6 +735,9 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         if (item == ITEM_END) break;
         if (item & ITEM_COMM) continue;
         const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
+        int hn;
+        tile_item(p, item, hn);
+        const uint32_t idesc = hn >= 0 ? (p.bf16 ? IDESC_BF16_H : IDESC_F16_H) : (p.bf16 ? IDESC_BF16 : IDESC_F16);
         // CTA pairs: the workers of both CTAs release the accumulator here
         if (!wait_bar(ctl, &sm.acc_empty[buf], (ause & 1) ^ 1, WAIT_ACC_EMPTY, CG == 2)) break;
         tc_fence_after();
@@ -1012,7 +1036,9 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
     // CTA pairs: nothing to store when this CTA's half lies below the last
     // row (the accumulator is still released after acc_full, in step with
     // the pair)
-    const int cols_end = (CG == 2 && blk * BM >= p.M) ? 0 : COLS;
+    // a column half of a split tail tile drains BN/2 columns, offset by coff
+    const int coff = gc.hn >= 0 ? gc.hn * (BN / 2) : 0;
+    const int cols_end = (CG == 2 && blk * BM >= p.M) ? 0 : (gc.hn >= 0 ? COLS / 2 : COLS);
 #pragma unroll 1
     for (int cc = 0; cc < cols_end; cc += 32) {
         uint32_t r[32];
@@ -1023,7 +1049,7 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        const int col0 = gc.nb * BN + wc.h * COLS + cc;
+        const int col0 = gc.nb * BN + coff + wc.h * COLS + cc;
         if (col0 >= p.N) continue;  // whole chunk right of the matrix (warp-uniform)
         // the previous chunk's store must have read the staging buffer
         if (wc.lane == 0) bulk_wait_read_all();
@@ -1136,9 +1162,10 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
     constexpr int NCH = COLS / 32;
     const int c_row = blk * BM + wc.q * 32;
-    const int colbase = gc.nb * BN + wc.h * COLS;
+    // a column half of a split tail tile (only the last rank's tiles are split)
+    const int colbase = gc.nb * BN + (gc.hn >= 0 ? gc.hn * (BN / 2) : 0) + wc.h * COLS;
     // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
-    const int nch = max(0, min(NCH, (p.N - colbase) / 32));
+    const int nch = max(0, min(gc.hn >= 0 ? NCH / 2 : NCH, (p.N - colbase) / 32));
     if (gc.rank == p.W - 1 && gc.rank > 0 && blk * BM < p.M && wc.lane == 0) {
         // the last rank will read this warp's running-sum rows: pull them into
         // L2 while the tile's MMAs still run

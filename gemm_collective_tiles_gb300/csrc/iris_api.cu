@@ -350,6 +350,30 @@ int launch(Params& p, const Cfg& c, cudaStream_t stream) {
     return e == cudaSuccess ? IRIS_OK : cuda_fail("kernel launch", static_cast<int>(e));
 }
 
+// The last wave of GEMM items is partly empty when the item count is not a
+// multiple of the CTA pairs.  When at most half the pairs would get a tile in
+// it, those tail tiles are split into column halves (N = BN / 2) so the wave
+// takes half a tile's time.  Reduce ops split only the last rank's tiles (the
+// chained reduce keeps one counter per whole tile), which in the rank-major
+// order are the final items of the last swizzle group.
+void tail_split(Params& p, const Cfg& c, bool reduce_op) {
+    p.g_split = p.n_gemm;
+    if (c.cg != 2 || p.n_gemm == 0 || c.tile_n != BN_WIDE) return;
+    if (reduce_op && (c.reduce_mode != 3 || c.rank_inner)) return;
+    const uint32_t pairs = static_cast<uint32_t>(c.grid / 2);
+    const uint32_t T = p.n_gemm;
+    const uint32_t tail = T % pairs;
+    if (tail == 0 || 2 * tail > pairs) return;
+    if (reduce_op) {
+        const uint32_t Tg = static_cast<uint32_t>(p.group_m) * p.n_blocks;
+        const uint32_t last_sg = (static_cast<uint32_t>(p.n_tiles) - 1) / Tg;
+        const uint32_t Tsg = std::min(Tg, static_cast<uint32_t>(p.n_tiles) - last_sg * Tg);
+        if (tail > Tsg) return;
+    }
+    p.g_split = T - tail;
+    p.n_gemm = T + tail;
+}
+
 bool dims_ok(int64_t M, int64_t N, int64_t K) {
     const int64_t lim = (int64_t(1) << 31) - 1;
     return M >= 0 && N >= 0 && K >= 0 && M <= lim && N <= lim && K <= lim;
@@ -451,6 +475,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     p.has_bias = has_bias;
     p.n_gemm = (M > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
     p.n_comm = static_cast<uint32_t>(mblocks) * W;
+    tail_split(p, c, false);
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_ALL_GATHER_MATMUL, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         char* g = p.heap + off_gathered;
@@ -509,6 +534,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     p.n_gemm = static_cast<uint32_t>(tiles * W);
     p.n_comm = c.reduce_mode == 1 ? static_cast<uint32_t>(tiles) : 0u;
     p.n_parts = c.reduce_mode == 2 ? static_cast<uint32_t>(tiles * W) : 0u;
+    tail_split(p, c, true);
     if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
@@ -586,6 +612,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     p.has_bias = has_bias;
     p.n_gemm = (M_l > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
     p.n_comm = 0;
+    tail_split(p, c, false);
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_MATMUL_ALL_GATHER, 0, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
@@ -671,6 +698,7 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
     p.mb_per_rank = mblocks;
     p.C = C;
     p.n_gemm = (has_gemm && part != 2) ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    tail_split(p, c, false);
     if (count > 0 && part != 1) {
         p.heap = static_cast<char*>(heap->base);
         p.rank_stride = heap->rank_stride;
