@@ -394,7 +394,6 @@ struct Smem {
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
-    uint32_t* spare;  // two unused words (keeps the carve's word offsets)
     uint32_t* ready_bits;
 
     __device__ void carve(uint8_t* raw) {
@@ -418,7 +417,6 @@ struct Smem {
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
-        spare = u + RING + 2;
         ready_bits = u + RING + 4;
 
     }

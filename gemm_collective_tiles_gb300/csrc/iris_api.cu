@@ -22,10 +22,9 @@ constexpr int BN_WIDE = 256, STAGES_WIDE = 4;
 constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
 // CTA pairs (tile_m 256): 256 x 256 tiles over two SMs; each SM stages
 // 128 x 64 of A and 64 x 128 of B (32 KB) per K-block, six deep
-#ifndef GCT_STAGES_PAIR
-#define GCT_STAGES_PAIR 6
-#endif
-constexpr int STAGES_PAIR = GCT_STAGES_PAIR;
+// (measured: 6 stages ~ 5 stages > 4 stages by 6.5 %; 7 do not fit beside the
+// epilogue staging buffers)
+constexpr int STAGES_PAIR = 6;
 constexpr size_t WS_HEADER = 256;
 constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
 

@@ -284,10 +284,11 @@ IRIS_API int iris_b200_concurrent_two_stream(const void* A, const void* B, void*
 /*
  * all_gather_matmul without a caller-provided workspace.  This entry point
  * has no counterpart on the pages; it exists for callers that cannot
- * allocate device memory themselves -- e.g. code running where cudaMalloc is
- * forbidden or unavailable (inside a CUDA-graph capture, a custom allocator's
- * own bootstrap, or a host framework that owns every allocation) -- and still
- * want the fused op.  The caller passes the heap (inputs and outputs) exactly
+ * allocate device memory themselves and still want the fused op -- e.g. a
+ * custom allocator's own bootstrap (the allocator is not usable yet), a host
+ * framework that owns every device allocation and hands out no scratch, or a
+ * latency-critical path that must not call cudaMalloc (which can synchronise
+ * the device).  The caller passes the heap (inputs and outputs) exactly
  * as for iris_b200_all_gather_matmul.  The queue counters, launch epoch,
  * status word and ready-flags live instead in a fixed static device array of
  * IRIS_NOALLOC_SCRATCH_BYTES bytes inside this library (every GPU that loads

@@ -1,8 +1,8 @@
 """The no-allocation all_gather_matmul entry point.
 
-Some callers cannot allocate device memory themselves (code running inside a
-CUDA-graph capture, an allocator's own bootstrap, or a framework that owns
-every allocation), so the library offers all_gather_matmul with its scratch
+Some callers cannot allocate device memory themselves (an allocator's own
+bootstrap, a framework that owns every allocation, or a latency-critical path
+that must not call cudaMalloc), so the library offers all_gather_matmul with its scratch
 (queue counters, epoch, status and ready-flags) in a static device array
 instead of a caller workspace.  This test calls it through the C ABI twice in
 a row and checks each result against the workspace entry point's output on
