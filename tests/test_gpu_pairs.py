@@ -160,3 +160,30 @@ def test_ag_mm_large_shards(tile_m):
     want, want_g = oracle_outputs(x)
     assert_exact(bits(outs["gathered"]), want_g)
     assert_exact(bits(outs["out"][0]), want[0])
+
+
+# (op, W, M, N, K, grid): with `grid` CTAs (grid/2 pairs) the tile count leaves
+# a last wave at most half full, so its tiles run as two 256 x 128 column
+# halves (for the reduce ops: the last rank's final tiles only)
+TAIL_CASES = [
+    ("mm_rs", 2, 640, 768, 128, 8),     # 9 tiles per rank, 18 items, 4 pairs: 2 tail tiles of rank 1
+    ("mm_ar", 3, 520, 512, 64, 8),      # 6 tiles per rank, 18 items: 2 tail tiles of rank 2
+    ("ag_mm", 4, 600, 768, 256, 8),     # 9 tiles, 4 pairs: 1 tail tile
+    ("mm_ag", 2, 2 * 300, 520, 128, 10),  # 12 tiles, 5 pairs: 2 tail tiles (ragged M and N)
+    ("mm_ag", 2, 2 * 300, 784, 128, 8),   # 16 tiles, 4 pairs: no split (a control)
+]
+
+
+@pytest.mark.parametrize("op,W,M,N,K,grid", TAIL_CASES)
+def test_tail_split_exact(op, W, M, N, K, grid):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=700 + M + N, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    want, want_g = oracle_outputs(x)
+    for extra in ({"grid": grid}, {"grid": 2 * grid}):
+        pair = run(x, 256, extra)
+        single = run(x, 128, extra)
+        for r in range(W if op == "mm_rs" else 1):
+            assert_exact(bits(pair["out"][r]), want[r])
+            assert_exact(bits(single["out"][r]), want[r])
+        if want_g is not None:
+            assert_exact(bits(pair["gathered"]), want_g)
