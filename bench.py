@@ -423,6 +423,32 @@ def run_concurrent(args, cfg):
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) * 1e3 / steps
     two_stream = {str(g): time_two(g) for g in (sms_all // 2, int(sms_all * 0.55), int(sms_all * 0.45))}
+
+    # the same on two green contexts with disjoint SM sets (the split enforced
+    # by the driver): GEMM streams get at least g SMs, the collective the rest
+    from gemm_collective_tiles_gb300 import make_config, sm_partition_release, sm_partition_streams
+
+    def time_green(g):
+        s_gemm, s_comm, gs, cs = sm_partition_streams(g)
+        try:
+            conf = dict(cfg)
+            conf.update(gemm_ctas=gs, grid=gs + cs)
+            two.config = make_config(**conf)
+            for _ in range(2):
+                two.run_two_stream(s_gemm, s_comm)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                two.run_two_stream(s_gemm, s_comm)
+            torch.cuda.synchronize()
+            return gs, (time.perf_counter() - t0) * 1e3 / steps
+        finally:
+            torch.cuda.synchronize()
+            sm_partition_release()
+    green = {}
+    for g in (72, 80, 88, 96):
+        gs, t = time_green(g)
+        green[str(gs)] = t
     del two
     g_only = make(cfg, coll=False)
     c_only = make(cfg, gemm=False)
@@ -442,6 +468,7 @@ def run_concurrent(args, cfg):
                            "gemm_tflops_alone": flops / (ms_g * 1e-3) / 1e12,
                            "all_reduce_gbs_alone": coll_bytes / (ms_c * 1e-3) / 1e9},
             "two_stream_ms_by_gemm_ctas": two_stream,
+            "two_stream_green_ctx_ms_by_gemm_sms": green,
             "gpu_launches": steps, "clocks": clocks}
     if args.sweep:
         sms = torch.cuda.get_device_properties(0).multi_processor_count

@@ -155,11 +155,16 @@ def workspace_size(op: str, M: int, N: int, K: int, world: int, dtype=torch.bflo
 
 
 class Workspace:
-    """Zero-initialised device workspace, reusable across calls on one stream."""
+    """Zero-initialised device workspace, reusable across calls on one stream.
+
+    The zero-fill is finished before the constructor returns, so the first
+    call may run on any stream (a workspace is created once and reused)."""
 
     def __init__(self, nbytes: int, device="cuda"):
         self.nbytes = max(256, _round_up(int(nbytes), 256))
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+        if self.buf.is_cuda:
+            torch.cuda.current_stream(self.buf.device).synchronize()
 
     @property
     def ptr(self) -> int:
@@ -291,6 +296,26 @@ def concurrent_two_stream(A, B, C, coll: str, heap, x_in, x_out, gemm_workspace:
         _DT[x_in.dtype] if x_in is not None else _native.IRIS_F32, _cfgp(config),
         gemm_workspace.ptr, gemm_workspace.nbytes, comm_workspace.ptr, comm_workspace.nbytes,
         _stream(gemm_stream), _stream(comm_stream)))
+
+
+def sm_partition_streams(gemm_sms: int):
+    """Two streams on disjoint SM sets of the current device (CUDA green
+    contexts, owned by the library): the first with at least `gemm_sms` SMs,
+    the second with the rest.  Returns (gemm_stream, comm_stream, gemm_sms,
+    comm_sms) with the streams as torch.cuda.ExternalStream.  For
+    concurrent_two_stream pass config gemm_ctas=gemm_sms, grid=gemm_sms+comm_sms."""
+    g, c = ctypes.c_void_p(), ctypes.c_void_p()
+    gs, cs = ctypes.c_int(), ctypes.c_int()
+    _native.check("iris_b200_sm_partition_streams", _native.load().iris_b200_sm_partition_streams(
+        int(gemm_sms), ctypes.byref(g), ctypes.byref(c), ctypes.byref(gs), ctypes.byref(cs)))
+    dev = torch.cuda.current_device()
+    return (torch.cuda.ExternalStream(g.value, device=dev), torch.cuda.ExternalStream(c.value, device=dev),
+            gs.value, cs.value)
+
+
+def sm_partition_release():
+    """Destroy the current device's SM partition (its streams must be idle)."""
+    _native.check("iris_b200_sm_partition_release", _native.load().iris_b200_sm_partition_release())
 
 
 def query_status(workspace: Workspace, stream=None):

@@ -40,6 +40,8 @@ EXPORTS = (
     "iris_b200_matmul_all_reduce",
     "iris_b200_concurrent_gemm_collective",
     "iris_b200_concurrent_two_stream",
+    "iris_b200_sm_partition_streams",
+    "iris_b200_sm_partition_release",
     "iris_b200_query_status",
     "iris_b200_strerror",
     "iris_b200_num_sms",
@@ -94,6 +96,8 @@ def _declare(lib):
             ci, [vp, vp, vp, i64, i64, i64, ci, ci, heapp, sz, sz, i64, ci, cfgp, vp, sz, vp]),
         "iris_b200_concurrent_two_stream": (
             ci, [vp, vp, vp, i64, i64, i64, ci, ci, heapp, sz, sz, i64, ci, cfgp, vp, sz, vp, sz, vp, vp]),
+        "iris_b200_sm_partition_streams": (ci, [ci, P(vp), P(vp), P(ci), P(ci)]),
+        "iris_b200_sm_partition_release": (ci, []),
         "iris_b200_query_status": (ci, [vp, vp, P(ci), P(ci), P(ci)]),
         "iris_b200_strerror": (ctypes.c_char_p, [ci]),
         "iris_b200_num_sms": (ci, [P(ci)]),

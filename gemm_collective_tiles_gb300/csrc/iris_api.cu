@@ -824,3 +824,122 @@ extern "C" int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, s
     return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, cfg,
                                        scratch, IRIS_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// ---------------------------------------------------------------------------
+// SM partition for the two-stream concurrent mode: two CUDA green contexts
+// with disjoint SM sets and one stream in each.  Driver functions are looked
+// up through the runtime (no link-time dependency on the driver library).
+namespace {
+typedef CUresult (*DeviceGetFn)(CUdevice*, int);
+typedef CUresult (*DeviceGetDevResourceFn)(CUdevice, CUdevResource*, CUdevResourceType);
+typedef CUresult (*SmSplitFn)(CUdevResource*, unsigned int*, const CUdevResource*, CUdevResource*, unsigned int,
+                              unsigned int);
+typedef CUresult (*GenerateDescFn)(CUdevResourceDesc*, CUdevResource*, unsigned int);
+typedef CUresult (*GreenCtxCreateFn)(CUgreenCtx*, CUdevResourceDesc, CUdevice, unsigned int);
+typedef CUresult (*GreenCtxStreamCreateFn)(CUstream*, CUgreenCtx, unsigned int, int);
+typedef CUresult (*StreamDestroyFn)(CUstream);
+typedef CUresult (*GreenCtxDestroyFn)(CUgreenCtx);
+
+struct GreenApi {
+    DeviceGetFn device_get = nullptr;
+    DeviceGetDevResourceFn get_resource = nullptr;
+    SmSplitFn split = nullptr;
+    GenerateDescFn gen_desc = nullptr;
+    GreenCtxCreateFn ctx_create = nullptr;
+    GreenCtxStreamCreateFn stream_create = nullptr;
+    StreamDestroyFn stream_destroy = nullptr;
+    GreenCtxDestroyFn ctx_destroy = nullptr;
+};
+
+// the driver functions at the ABI of the toolkit this file is compiled with
+// (the prototypes above come from its header)
+template <typename F>
+bool driver_fn(const char* name, F& out) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, CUDART_VERSION, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        if (debug_on()) std::fprintf(stderr, "[iris_b200] driver entry point %s unavailable\n", name);
+        return false;
+    }
+    out = reinterpret_cast<F>(fn);
+    return true;
+}
+
+bool green_api(GreenApi& a) {
+    return driver_fn("cuDeviceGet", a.device_get) && driver_fn("cuDeviceGetDevResource", a.get_resource) &&
+           driver_fn("cuDevSmResourceSplitByCount", a.split) && driver_fn("cuDevResourceGenerateDesc", a.gen_desc) &&
+           driver_fn("cuGreenCtxCreate", a.ctx_create) && driver_fn("cuGreenCtxStreamCreate", a.stream_create) &&
+           driver_fn("cuStreamDestroy", a.stream_destroy) && driver_fn("cuGreenCtxDestroy", a.ctx_destroy);
+}
+
+struct Partition {
+    CUgreenCtx ctx[2] = {nullptr, nullptr};
+    CUstream stream[2] = {nullptr, nullptr};
+    int sms[2] = {0, 0};
+};
+Partition g_partition[64];
+std::mutex g_partition_mu;
+
+void partition_destroy(const GreenApi& a, Partition& pt) {
+    for (int i = 0; i < 2; ++i) {
+        if (pt.stream[i]) a.stream_destroy(pt.stream[i]);
+        if (pt.ctx[i]) a.ctx_destroy(pt.ctx[i]);
+        pt.stream[i] = nullptr;
+        pt.ctx[i] = nullptr;
+        pt.sms[i] = 0;
+    }
+}
+}  // namespace
+
+extern "C" int iris_b200_sm_partition_streams(int gemm_sms, cudaStream_t* gemm_stream, cudaStream_t* comm_stream,
+                                              int* gemm_sms_out, int* comm_sms_out) {
+    if (!gemm_stream || !comm_stream) return IRIS_EINVAL;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IRIS_ECUDA;
+    if (num_sms_current(&sms) != IRIS_OK) return IRIS_ECUDA;
+    if (gemm_sms < 1 || gemm_sms >= sms) return IRIS_EINVAL;
+    GreenApi a;
+    if (!green_api(a)) return IRIS_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_partition_mu);
+    Partition& pt = g_partition[dev];
+    partition_destroy(a, pt);  // a new call replaces this device's partition
+    CUdevice cudev;
+    if (a.device_get(&cudev, dev) != CUDA_SUCCESS) return cuda_fail("cuDeviceGet", 0);
+    CUdevResource all, part, rest;
+    std::memset(&part, 0, sizeof(part));
+    std::memset(&rest, 0, sizeof(rest));
+    CUresult r = a.get_resource(cudev, &all, CU_DEV_RESOURCE_TYPE_SM);
+    if (r != CUDA_SUCCESS) return cuda_fail("cuDeviceGetDevResource", static_cast<int>(r));
+    unsigned int groups = 1;
+    r = a.split(&part, &groups, &all, &rest, 0, static_cast<unsigned int>(gemm_sms));
+    if (r != CUDA_SUCCESS || groups != 1 || rest.sm.smCount == 0)
+        return r != CUDA_SUCCESS ? cuda_fail("cuDevSmResourceSplitByCount", static_cast<int>(r)) : IRIS_EINVAL;
+    CUdevResource* res[2] = {&part, &rest};
+    for (int i = 0; i < 2; ++i) {
+        CUdevResourceDesc desc;
+        r = a.gen_desc(&desc, res[i], 1);
+        if (r == CUDA_SUCCESS) r = a.ctx_create(&pt.ctx[i], desc, cudev, CU_GREEN_CTX_DEFAULT_STREAM);
+        if (r == CUDA_SUCCESS) r = a.stream_create(&pt.stream[i], pt.ctx[i], CU_STREAM_NON_BLOCKING, 0);
+        if (r != CUDA_SUCCESS) {
+            partition_destroy(a, pt);
+            return cuda_fail("green context", static_cast<int>(r));
+        }
+        pt.sms[i] = static_cast<int>(res[i]->sm.smCount);
+    }
+    *gemm_stream = reinterpret_cast<cudaStream_t>(pt.stream[0]);
+    *comm_stream = reinterpret_cast<cudaStream_t>(pt.stream[1]);
+    if (gemm_sms_out) *gemm_sms_out = pt.sms[0];
+    if (comm_sms_out) *comm_sms_out = pt.sms[1];
+    return IRIS_OK;
+}
+
+extern "C" int iris_b200_sm_partition_release(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IRIS_ECUDA;
+    GreenApi a;
+    if (!green_api(a)) return IRIS_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_partition_mu);
+    partition_destroy(a, g_partition[dev]);
+    return IRIS_OK;
+}

@@ -282,6 +282,28 @@ IRIS_API int iris_b200_concurrent_two_stream(const void* A, const void* B, void*
                                              cudaStream_t gemm_stream, cudaStream_t comm_stream);
 
 /*
+ * SM partition for the two-stream mode -- ROCm/iris PR #544 (mode
+ * "concurrent": the GEMM and the collective as separate persistent kernels
+ * with an explicit split of the compute units).  Creates two CUDA green
+ * contexts on the current device with disjoint SM sets -- the first with at
+ * least `gemm_sms` SMs (rounded up to the device's partition granularity), the
+ * second with the rest -- and a non-blocking stream in each.  Kernels launched
+ * into *gemm_stream run only on the first set and those in *comm_stream only
+ * on the second, so iris_b200_concurrent_two_stream given these streams (with
+ * cfg->gemm_ctas = *gemm_sms_out and cfg->grid = *gemm_sms_out + *comm_sms_out)
+ * runs its two kernels on disjoint SMs by construction rather than by
+ * occupancy.  The library owns the contexts and streams, one partition per
+ * device: a new call replaces the device's previous partition, and
+ * iris_b200_sm_partition_release destroys it; the caller must have finished
+ * its work on the old streams first.  Returns IRIS_EINVAL for gemm_sms outside
+ * [1, #SMs), IRIS_EUNSUPPORTED when the driver offers no green contexts,
+ * IRIS_ECUDA otherwise.
+ */
+IRIS_API int iris_b200_sm_partition_streams(int gemm_sms, cudaStream_t* gemm_stream, cudaStream_t* comm_stream,
+                                            int* gemm_sms_out, int* comm_sms_out);
+IRIS_API int iris_b200_sm_partition_release(void);
+
+/*
  * all_gather_matmul without a caller-provided workspace.  This entry point
  * has no counterpart on the pages; it exists for callers that cannot
  * allocate device memory themselves and still want the fused op -- e.g. a

@@ -312,6 +312,42 @@ def test_two_stream_mode_bit_exact(coll):
         assert np.array_equal(got, w), r
 
 
+@pytest.mark.parametrize("coll", ["all_reduce", "all_gather", "all_to_all"])
+def test_two_stream_mode_on_sm_partition(coll):
+    """The two-stream mode on streams of two green contexts with disjoint SM
+    sets (the split enforced by the driver, not by occupancy): results bit for
+    bit as before."""
+    from gemm_collective_tiles_gb300 import query_status, sm_partition_release, sm_partition_streams
+    W, count = 8, 8 * 16384
+    M, N, K = 520, 512, 256
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=71, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=72)
+    s_gemm, s_comm, gs, cs = sm_partition_streams(80)
+    try:
+        assert gs >= 80 and cs >= 1
+        prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count,
+                                 config={"comm_block": 8192, "gemm_ctas": gs, "grid": gs + cs})
+        prob.upload(A, B, X)
+        prob.poison_outputs()
+        torch.cuda.synchronize()
+        prob.run_two_stream(s_gemm, s_comm)
+        s_gemm.synchronize()
+        s_comm.synchronize()
+        assert query_status(prob.ws)[0] == 0 and query_status(prob.ws2)[0] == 0
+        out = prob.outputs()
+    finally:
+        torch.cuda.synchronize()
+        sm_partition_release()
+    assert_exact(bits(out["C"]), oracle.gemm(A, B))
+    want = {"all_reduce": lambda: [oracle.all_reduce(X)] * W,
+            "all_gather": lambda: [oracle.all_gather(X)] * W,
+            "all_to_all": lambda: oracle.all_to_all(X)}[coll]()
+    for r in range(W):
+        got = out["x"][r].contiguous().view(torch.uint8).numpy()
+        w = want[r] if want[r].dtype == np.uint8 else want[r].view(np.uint8)
+        assert np.array_equal(got, w), r
+
+
 def test_concurrent_all_reduce_in_place_and_alone():
     W, count = 4, 100000
     X = synthetic.make_coll_inputs(W, count, "f32", seed=63)
