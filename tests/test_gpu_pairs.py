@@ -187,3 +187,26 @@ def test_tail_split_exact(op, W, M, N, K, grid):
             assert_exact(bits(single["out"][r]), want[r])
         if want_g is not None:
             assert_exact(bits(pair["gathered"]), want_g)
+
+
+# (op, W, M, N, K): empty M, empty K (the output is the bias alone: zeros + bias,
+# summed over the ranks for the reduce ops), a single row, and N = 8 per rank
+DEGENERATE = [
+    ("ag_mm", 4, 0, 256, 256), ("ag_mm", 4, 200, 136, 0), ("ag_mm", 2, 1, 8, 16),
+    ("mm_rs", 4, 0, 512, 128), ("mm_rs", 2, 130, 256, 0), ("mm_rs", 4, 1, 32, 64),
+    ("mm_ar", 3, 0, 256, 64), ("mm_ar", 2, 77, 264, 0), ("mm_ar", 2, 1, 8, 8),
+    ("mm_ag", 4, 0, 256, 64), ("mm_ag", 2, 2 * 100, 136, 0), ("mm_ag", 4, 4 * 1, 8, 24),
+]
+
+
+@pytest.mark.parametrize("op,W,M,N,K", DEGENERATE)
+@pytest.mark.parametrize("tile_m", [0, 128])   # 0: the default (pairs wherever they apply)
+def test_degenerate_shapes(op, W, M, N, K, tile_m):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "f16", seed=800 + M + N + K, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    outs = run(x, tile_m)
+    want, want_g = oracle_outputs(x)
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
+    if want_g is not None:
+        assert_exact(bits(outs["gathered"]), want_g)
