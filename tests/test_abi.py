@@ -119,6 +119,8 @@ def test_argument_checks_before_any_gpu_work():
     assert lib.iris_b200_concurrent_gemm_collective(None, None, None, 0, 0, 0, 0, 2, hp, 0, 0, 12, 2, None, None, 0, None) == N.IRIS_EALIGN
     # query_status needs a workspace
     assert lib.iris_b200_query_status(None, None, None, None, None) == N.IRIS_EINVAL
+    # the SM partition needs somewhere to put its streams
+    assert lib.iris_b200_sm_partition_streams(80, None, None, None, None) == N.IRIS_EINVAL
 
 
 def test_config_builder_rejects_unknown_keys():
