@@ -19,7 +19,7 @@ from typing import Callable, Dict, Iterable, List, Optional, Sequence
 ENV_CACHE = "IRIS_B200_CACHE"
 
 # knobs a cached entry may set (the rest stay at their defaults)
-TUNABLE = ("tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block")
+TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block")
 
 
 def cache_path() -> str:
@@ -82,12 +82,19 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     """Ranked candidate configs (the static default, {}, is always first).
 
     Ranking rule (from the measurements behind the defaults): the swizzle
-    group width matters most for operand reuse in L2, then the tile width for
-    small N, then -- per op -- the reduce schedule or the concurrent CTA
-    split.  The list is truncated to top_k."""
+    group width matters most for operand reuse in L2, then one CTA per tile
+    instead of a CTA pair where the pair tiles leave a wave badly filled,
+    then the tile width for small N, then -- per op -- the reduce schedule or
+    the concurrent CTA split.  The list is truncated to top_k."""
     out: List[dict] = [{}]
-    for gm in (32, 16, 64, 8):
+    for gm in (64, 16, 8):   # 32 is the default
         out.append({"group_m": gm})
+    pair_tiles = -(-M // 256) * -(-N // 256) * (W if op in ("matmul_reduce_scatter", "matmul_all_reduce") else 1)
+    pairs = max(1, sm_count // 2)
+    if pair_tiles % pairs and pair_tiles % pairs <= pairs // 2 or pair_tiles < pairs:
+        out.insert(1, {"tile_m": 128})   # a short last wave of pair tiles
+    else:
+        out.append({"tile_m": 128})
     if N <= 4096:
         out.append({"tile_n": 128})
     if op in ("matmul_reduce_scatter", "matmul_all_reduce"):
