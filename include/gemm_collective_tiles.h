@@ -319,9 +319,8 @@ IRIS_API int iris_b200_sm_partition_release(void);
  *     IRIS_NOALLOC_MAX_FLAGS; larger problems return IRIS_ENOWS and launch
  *     nothing.
  *   - The first call on a device looks up the array's device address and
- *     zero-fills it (cudaMemsetAsync on `stream`); make that first call before
- *     any stream capture.  Every call then clears the queue counters and the
- *     status word (one cudaMemsetAsync of 28 bytes on `stream`) and launches
+ *     zero-fills it (cudaMemsetAsync on `stream`).  Every call then clears
+ *     the queue counters and the status word (one cudaMemsetAsync of 28 bytes on `stream`) and launches
  *     the kernel.  No call allocates or frees memory.
  *   - All calls share the one array: calls whose kernels overlap on the GPU
  *     (different streams, or several host threads) race and must not be made.
