@@ -982,14 +982,32 @@ template <int BN, int STAGES, int CG>
 __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem,
                          uint32_t g, uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
+    const GemmCoord gc = decode_gemm(p, g);
+    const int blk = own_block<CG>(p, gc, ctl.half);
+    const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
+    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;  // accumulator columns this warp drains
+    // a column half of a split tail tile drains BN/2 columns, offset by coff;
+    // CTA pairs: nothing to store when this CTA's half lies below the last row
+    // (the accumulator is still released after acc_full, in step with the pair)
+    const int coff = gc.hn >= 0 ? gc.hn * (BN / 2) : 0;
+    const int colbase = gc.nb * BN + coff + wc.h * COLS;
+    const int cols_end = (CG == 2 && blk * BM >= p.M) ? 0 : (gc.hn >= 0 ? COLS / 2 : COLS);
+    const char* bias_base = nullptr;
+    if (p.has_bias) {
+        const int bias_region = reduce_op ? gc.rank : 0;
+        bias_base = p.heap + static_cast<size_t>(bias_region) * p.rank_stride + p.off_bias;
+    }
+    // per-column bias of the warp's columns, fetched while the MMAs still run:
+    // lane l holds the 8 values of columns colbase + 8l .. 8l + 7
+    uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
+    if (p.has_bias && !p.bias_on_m && wc.lane * 8 < cols_end && colbase + wc.lane * 8 < p.N)
+        bias8 = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(colbase + wc.lane * 8) * 2);
+
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
     tr.rec(EV_READY, g);
 
-    const GemmCoord gc = decode_gemm(p, g);
-    const int blk = own_block<CG>(p, gc, ctl.half);
     const int r_in_tile = wc.q * 32 + wc.lane;
-    const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
     // output row of this thread and whether it exists
     int row;        // row inside the op's output (or partial)
     int bias_row;   // index into a per-row bias
@@ -1004,21 +1022,21 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
         row_ok = row < p.M;
         bias_row = row;
     }
-    const char* bias_base = nullptr;
-    if (p.has_bias) {
-        const int bias_region = reduce_op ? gc.rank : 0;
-        bias_base = p.heap + static_cast<size_t>(bias_region) * p.rank_stride + p.off_bias;
-    }
+    (void)row;
     float row_bias = 0.f;
     if (p.has_bias && p.bias_on_m && row_ok)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[bias_row], p.bf16);
 
-    constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;  // accumulator columns this warp drains
     const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
     // Each 32 x 32 chunk (the warp's 32 rows, one per lane) goes registers ->
     // swizzled shared-memory staging -> TMA tensor store, so global memory
-    // sees whole 128-byte lines instead of 16-byte pieces of 32 rows.
-    uint8_t* stg = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
+    // sees whole 128-byte lines instead of 16-byte pieces of 32 rows.  The
+    // warp's 8 KB staging area rotates over 4 buffers (16-bit chunks, 2 KB)
+    // or 2 (fp32 chunks, 4 KB), so a chunk waits only for the store issued
+    // that many chunks earlier.
+    uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
+    const uint32_t chunk_bytes = reduce_op ? 32 * 32 * 4 : 32 * 32 * 2;
+    const uint32_t nbuf = Smem<BN, STAGES, CG>::STAGE_OUT_BYTES / chunk_bytes;
     // TMA coordinates of the warp's 32-row slab
     const int c_row = blk * BM + wc.q * 32;
     int c_blk, c_reg_lo = 0, c_reg_hi = 1;
@@ -1031,14 +1049,9 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
         c_blk = 0;
         if (p.replicate && p.op == OP_AG_MM) c_reg_hi = p.W;
     }
-    // CTA pairs: nothing to store when this CTA's half lies below the last
-    // row (the accumulator is still released after acc_full, in step with
-    // the pair)
-    // a column half of a split tail tile drains BN/2 columns, offset by coff
-    const int coff = gc.hn >= 0 ? gc.hn * (BN / 2) : 0;
-    const int cols_end = (CG == 2 && blk * BM >= p.M) ? 0 : (gc.hn >= 0 ? COLS / 2 : COLS);
+    uint32_t ci = 0;
 #pragma unroll 1
-    for (int cc = 0; cc < cols_end; cc += 32) {
+    for (int cc = 0; cc < cols_end; cc += 32, ++ci) {
         uint32_t r[32];
         if (p.k_blocks > 0) {
             tmem_ld_32x32b_x32(tbase + cc, r);
@@ -1047,10 +1060,14 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        const int col0 = gc.nb * BN + coff + wc.h * COLS + cc;
-        if (col0 >= p.N) continue;  // whole chunk right of the matrix (warp-uniform)
-        // the previous chunk's store must have read the staging buffer
-        if (wc.lane == 0) bulk_wait_read_all();
+        const int col0 = colbase + cc;
+        if (col0 >= p.N) continue;  // whole chunk right of the matrix (warp-uniform; so are all later ones)
+        uint8_t* stg = stg_base + (ci % nbuf) * chunk_bytes;
+        // the store issued nbuf chunks ago (from this buffer) must have read it
+        if (wc.lane == 0) {
+            if (reduce_op) bulk_wait_read<1>();
+            else bulk_wait_read<3>();
+        }
         __syncwarp();
 #pragma unroll
         for (int v = 0; v < 4; ++v) {  // 8 columns at a time: +bias, then into the staging row
@@ -1061,13 +1078,18 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
                 if (p.bias_on_m) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = x[i] + row_bias;
-                } else if (col0 + v * 8 < p.N) {
-                    const uint4 bb = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(col0 + v * 8) * 2);
-                    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+                } else {
+                    const int src = (cc >> 3) + v;  // the lane holding columns col0 + 8v ..
+                    const uint32_t bw[4] = {__shfl_sync(0xFFFFFFFFu, bias8.x, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.y, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.z, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.w, src)};
+                    if (col0 + v * 8 < p.N) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x[2 * i] = x[2 * i] + bits16_to_float(bw[i] & 0xFFFFu, p.bf16);
-                        x[2 * i + 1] = x[2 * i + 1] + bits16_to_float(bw[i] >> 16, p.bf16);
+                        for (int i = 0; i < 4; ++i) {
+                            x[2 * i] = x[2 * i] + bits16_to_float(bw[i] & 0xFFFFu, p.bf16);
+                            x[2 * i + 1] = x[2 * i + 1] + bits16_to_float(bw[i] >> 16, p.bf16);
+                        }
                     }
                 }
             }
@@ -1169,6 +1191,14 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         // L2 while the tile's MMAs still run
         for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, 0, 0);
     }
+    const int s = gc.rank;
+    const char* bias_base =
+        p.has_bias ? p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_bias : nullptr;
+    // per-column bias of the warp's columns, fetched while the MMAs still run:
+    // lane l holds the 8 values of columns colbase + 8l .. 8l + 7
+    uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
+    if (p.has_bias && !p.bias_on_m && wc.lane < nch * 4)
+        bias8 = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(colbase + wc.lane * 8) * 2);
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
     tr.rec(EV_READY, g);
@@ -1180,11 +1210,8 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         if (wc.lane == 0) release_acc(sm, buf);
         return true;
     }
-    const int s = gc.rank;
     const bool last = (s == p.W - 1);
     const int row = blk * BM + wc.q * 32 + wc.lane;
-    const char* bias_base =
-        p.has_bias ? p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_bias : nullptr;
     float row_bias = 0.f;
     if (p.has_bias && p.bias_on_m && row < p.M)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
@@ -1234,8 +1261,11 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
             } else {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 bb = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(col0 + v * 8) * 2);
-                    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+                    const int src = ci * 4 + v;  // the lane holding columns col0 + 8v ..
+                    const uint32_t bw[4] = {__shfl_sync(0xFFFFFFFFu, bias8.x, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.y, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.z, src),
+                                            __shfl_sync(0xFFFFFFFFu, bias8.w, src)};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         x[v * 8 + 2 * i] = x[v * 8 + 2 * i] + bits16_to_float(bw[i] & 0xFFFFu, p.bf16);
@@ -1263,7 +1293,8 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
             }
             __syncwarp();  // every lane has read its row before the buffer is rewritten
         } else {
-            if (wc.lane == 0) bulk_wait_read_all();
+            // the store issued two chunks ago (from this buffer) must have read it
+            if (wc.lane == 0) bulk_wait_read<1>();
             __syncwarp();
         }
         if (!last) {
