@@ -27,7 +27,7 @@ class Machine:
     sms: int = 152
     gemm_tflops_per_sm: float = 11.9      # CTA-pair GEMM 8192^3 bf16 at 1.81 PFLOP/s over 152 SMs
     comm_gbs_per_sm: float = 65.0         # one CTA's collective engine (all-reduce, linear up to ~96 CTAs)
-    hbm_gbs: float = 6774.0               # measured copy bandwidth
+    hbm_gbs: float = 6779.4               # measured copy bandwidth
     gemm_hbm_share: float = 0.12          # HBM fraction the GEMM operands use when all SMs run it
     tile_overhead_us: float = 1.0         # claim + pipeline fill per tile
 
