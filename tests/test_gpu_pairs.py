@@ -29,10 +29,11 @@ def assert_exact(got, want):
     assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
 
 
-def run(x, tile_m, extra=None):
+def run(x, tile_m, extra=None, bias_on_m=False):
     cfg = {"tile_m": tile_m}
     cfg.update(extra or {})
-    prob = FusedProblem(x.op, x.W, x.M, x.N, x.K, x.dtype, bias=x.bias is not None, config=cfg)
+    prob = FusedProblem(x.op, x.W, x.M, x.N, x.K, x.dtype, bias=x.bias is not None, bias_on_m=bias_on_m,
+                        config=cfg)
     prob.upload(x.A, x.B, x.bias)
     prob.poison_outputs()
     prob.run()
@@ -40,15 +41,15 @@ def run(x, tile_m, extra=None):
     return prob.outputs()
 
 
-def oracle_outputs(x):
+def oracle_outputs(x, bias_on_m=False):
     if x.op == "ag_mm":
-        out, g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+        out, g = oracle.all_gather_matmul(x.A, x.B[0], x.bias, bias_on_m=bias_on_m)
         return [out], g
     if x.op == "mm_rs":
-        return oracle.matmul_reduce_scatter(x.A, x.B, x.bias), None
+        return oracle.matmul_reduce_scatter(x.A, x.B, x.bias, bias_on_m=bias_on_m), None
     if x.op == "mm_ar":
-        return [oracle.matmul_all_reduce(x.A, x.B, x.bias)], None
-    return [oracle.matmul_all_gather(x.A, x.B[0], x.bias)], None
+        return [oracle.matmul_all_reduce(x.A, x.B, x.bias, bias_on_m=bias_on_m)], None
+    return [oracle.matmul_all_gather(x.A, x.B[0], x.bias, bias_on_m=bias_on_m)], None
 
 
 # (op, W, M, N, K): M (or M / W for matmul_all_gather) ends a pair tile with
@@ -210,3 +211,27 @@ def test_degenerate_shapes(op, W, M, N, K, tile_m):
         assert_exact(bits(outs["out"][r]), want[r])
     if want_g is not None:
         assert_exact(bits(outs["gathered"]), want_g)
+
+
+# Both bias layouts through every epilogue: a per-row bias on pair tiles (with
+# the split tail halves at `grid`) and on one-CTA tiles, and a per-column bias
+# on one-CTA 128 x 128 tiles, where a warp's 128 columns of bias sit in half
+# its lanes.  Small-integer inputs: every output must equal the oracle's bits.
+@pytest.mark.parametrize("op,W,M,N,K,grid", TAIL_CASES)
+@pytest.mark.parametrize("layout", ["row", "col_128x128"])
+def test_bias_layouts_exact(op, W, M, N, K, grid, layout):
+    bias_on_m = layout == "row"
+    bias_len = (M // W if op == "mm_ag" else M) if bias_on_m else N
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "f16", seed=1700 + M + N + K, dist="int", scale=2,
+                                    bias=True, bias_scale=3, bias_len=bias_len)
+    want, want_g = oracle_outputs(x, bias_on_m)
+    if bias_on_m:
+        runs = [(256, {"grid": grid}), (256, {}), (128, {"grid": grid})]
+    else:
+        runs = [(128, {"tile_n": 128}), (128, {"tile_n": 128, "grid": grid})]
+    for tile_m, extra in runs:
+        outs = run(x, tile_m, extra, bias_on_m=bias_on_m)
+        for r in range(W if op == "mm_rs" else 1):
+            assert_exact(bits(outs["out"][r]), want[r])
+        if want_g is not None:
+            assert_exact(bits(outs["gathered"]), want_g)
