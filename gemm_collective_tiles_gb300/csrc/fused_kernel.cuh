@@ -96,6 +96,9 @@ struct Params {
     CUtensorMap tmC;  // 4-D {n, row, row block, region} output, box {32, 32, 1, 1}:
                       // fp32 partials (128-byte swizzle) or 16-bit outputs (64-byte swizzle)
     CUtensorMap tmS;  // chained reduce: the fp32 running-sum tile buffer, box {32, 32, 1, 1}
+    CUtensorMap tmBc; // B as 64-column chunks: 4-D {64, k, n / 64, rank}, box {64, 64, BN / CG / 64, 1}
+                      // (one load per K-block fills a CTA's B columns; set when N % 64 == 0)
+    int b_chunked;    // tmBc is valid
     int op, W, bf16, coll;
     int M;            // rows of one GEMM (M_local for matmul_all_gather)
     int N, K;
@@ -648,10 +651,14 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             if (CG == 1) {
                 mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES, CG>::STAGE_BYTES);
                 tma_load_3d(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, &sm.full[stage]);
+                if (p.b_chunked) {
+                    tma_load_4d(sm.b_tile(stage), &p.tmBc, 0, kb * BK, gc.nb * (BN / 64), b_rank, &sm.full[stage]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                    tma_load_3d(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, gc.nb * BN + c * 64,
-                                kb * BK, b_rank, &sm.full[stage]);
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_3d(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, gc.nb * BN + c * 64,
+                                    kb * BK, b_rank, &sm.full[stage]);
+                }
             } else {
                 // both CTAs' boxes count on the even CTA's full barrier, which
                 // expects the pair's bytes (the odd CTA's may land first: the
@@ -664,9 +671,15 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 const uint32_t fb = mapa_shared(&sm.full[stage], 0);
                 tma_load_3d_pair(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, fb);
                 const int bcol = gc.nb * BN + (hn ? gc.hn * (BN / 2) + ctl.half * (BN / 4) : ctl.half * (BN / CG));
-                const int nbox = hn ? BN / 4 / 64 : BN / CG / 64;
-                for (int c = 0; c < nbox; ++c)
-                    tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, bcol + c * 64, kb * BK, b_rank, fb);
+                if (p.b_chunked && !hn) {
+                    // the CTA's BN / CG columns as one box of 64-column chunks
+                    tma_load_4d_pair(sm.b_tile(stage), &p.tmBc, 0, kb * BK, bcol / 64, b_rank, fb);
+                } else {
+                    const int nbox = hn ? BN / 4 / 64 : BN / CG / 64;
+                    for (int c = 0; c < nbox; ++c)
+                        tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, bcol + c * 64, kb * BK, b_rank,
+                                         fb);
+                }
             }
             issued_phase[stage] = phase;
             used_mask |= 1u << stage;
@@ -1746,6 +1759,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         if (p.n_gemm > 0 && p.k_blocks > 0) {
             tma_prefetch_desc(&p.tmA);
             tma_prefetch_desc(&p.tmB);
+            if (p.b_chunked) tma_prefetch_desc(&p.tmBc);
         }
         if (p.n_gemm > 0) tma_prefetch_desc(&p.tmC);
         if (p.n_gemm > 0 && p.reduce_mode == 3) tma_prefetch_desc(&p.tmS);

@@ -282,6 +282,29 @@ int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t d0, uint64_t d
     return r == CUDA_SUCCESS ? IRIS_OK : cuda_fail("cuTensorMapEncodeTiled (operand)", static_cast<int>(r));
 }
 
+// B as 64-column chunks: 4-D {64, k, n / 64, region} (strides N * 2, 128,
+// region), box {64, BK, tile_n / cg / 64, 1}.  One load fills all of a CTA's
+// B columns for a K-block, chunk after chunk 8 KB apart -- the layout the
+// 3-D map's per-chunk loads produce.  Only when N % 64 == 0, so that no
+// chunk runs past the end of a row; otherwise the 3-D map serves alone.
+int make_b_chunk_map(Params& p, const Cfg& c, const void* base, int64_t N, int64_t K, uint64_t regions,
+                     uint64_t region_stride) {
+    p.b_chunked = 0;
+    if (N % 64 != 0 || N <= 0 || K <= 0) return IRIS_OK;
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64), regions};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(N) * 2, 128, region_stride};
+    cuuint32_t box[4] = {64, BK, static_cast<cuuint32_t>(c.tile_n / c.cg / 64), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(&p.tmBc, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                     const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled (B chunks)", static_cast<int>(r));
+    p.b_chunked = 1;
+    return IRIS_OK;
+}
+
 // Output map: 4-D {n, row, row block, region} with a 32 x 32 box, written by
 // the epilogue's TMA stores.  fp32 (partials) use the 128-byte swizzle (one
 // 128-byte staging row), 16-bit outputs the 64-byte swizzle.
@@ -481,6 +504,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmA, g, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
             return rc;
+        if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
     if (p.n_gemm > 0 &&
         (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M, 1, W, N * 2, size_t(M) * N * 2, heap->rank_stride)))
@@ -538,6 +562,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64, BK))) return rc;
+        if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, W, heap->rank_stride))) return rc;
     }
     if (p.n_gemm > 0) {
         if (c.reduce_mode == 3) {
@@ -617,6 +642,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
             return rc;
+        if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
     if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M_l, W, W, N * 2,
                                            size_t(M_l) * N * 2, heap->rank_stride)))
@@ -717,6 +743,7 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, A, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
         if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK))) return rc;
+        if ((rc = make_b_chunk_map(p, c, B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
     if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, C, p.bf16, N, M, 1, 1, N * 2, size_t(M) * N * 2,
                                            size_t(M) * N * 2)))
