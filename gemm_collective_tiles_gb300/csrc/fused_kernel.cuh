@@ -40,7 +40,10 @@ enum : int { OP_AG_MM = 0, OP_MM_RS = 1, OP_MM_AG = 2, OP_MM_AR = 3, OP_CONC = 4
 enum : int { COLL_AG = 0, COLL_AR = 1, COLL_RS = 2, COLL_A2A = 3, COLL_BC = 4 };
 
 constexpr int BM = 128;           // tile rows (tcgen05 M for cta_group::1)
-constexpr int BK = 64;            // K per stage: 64 x 16-bit = one 128-byte swizzle row
+constexpr int BK = 64;            // K per block: 64 x 16-bit = one 128-byte swizzle row
+// K blocks per pipeline stage: CTA pairs take two (one A box and one B box
+// of 128 K rows per stage and CTA), one-CTA tiles one
+__host__ __device__ constexpr int k_per_stage(int cg) { return cg == 2 ? 2 : 1; }
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int NUM_WORKER_WARPS = 4;  // one per tensor-memory lane quadrant (or a multiple of 4)
 constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
@@ -96,9 +99,12 @@ struct Params {
     CUtensorMap tmC;  // 4-D {n, row, row block, region} output, box {32, 32, 1, 1}:
                       // fp32 partials (128-byte swizzle) or 16-bit outputs (64-byte swizzle)
     CUtensorMap tmS;  // chained reduce: the fp32 running-sum tile buffer, box {32, 32, 1, 1}
-    CUtensorMap tmBc; // B as 64-column chunks: 4-D {64, k, n / 64, rank}, box {64, 64, BN / CG / 64, 1}
-                      // (one load per K-block fills a CTA's B columns; set when N % 64 == 0)
+    CUtensorMap tmBc; // B as 64-column chunks: 4-D {64, k, n / 64, rank}, box {64, 64 KS, BN / CG / 64, 1}
+                      // (one load per stage fills a CTA's B columns; set when N % 64 == 0)
+    CUtensorMap tmAc; // A as 64-column K chunks: 4-D {64, row, k / 64, rank}, box {64, 128, KS, 1}
+                      // (CTA pairs: one load per stage; set when K % 64 == 0)
     int b_chunked;    // tmBc is valid
+    int a_chunked;    // tmAc is valid
     int op, W, bf16, coll;
     int M;            // rows of one GEMM (M_local for matmul_all_gather)
     int N, K;
@@ -378,8 +384,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
 // A and BN / 2 columns of B per stage.
 template <int BN, int STAGES, int CG>
 struct Smem {
-    static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = (BN / CG) * BK * 2;
+    static constexpr int KS = k_per_stage(CG);  // K blocks per stage
+    static constexpr uint32_t A_BYTES = BM * BK * KS * 2;  // KS chunks of 128 rows x 64 K, 16 KB apart
+    static constexpr uint32_t B_BYTES = (BN / CG) * BK * KS * 2;  // 64-column chunks of 64 KS K rows
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
@@ -633,9 +640,10 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 }
             }
         }
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        constexpr int KS = Smem<BN, STAGES, CG>::KS;
+        for (int kb = 0; kb < p.k_blocks; kb += KS) {
             if (p.op == OP_AG_MM && acquired < p.W) {
-                const int s_hi = min(p.W - 1, (kb * BK + BK - 1) / p.K_local);
+                const int s_hi = min(p.W - 1, ((kb + KS) * BK - 1) / p.K_local);
                 if (s_hi >= acquired) {
                     for (int s = acquired; s <= s_hi; ++s) {
                         const int fi = blk * p.W + s;
@@ -669,7 +677,16 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 if (ctl.half == 0)
                     mbar_arrive_expect_tx(&sm.full[stage], (hn ? HALF_BYTES : Smem<BN, STAGES, CG>::STAGE_BYTES) * CG);
                 const uint32_t fb = mapa_shared(&sm.full[stage], 0);
-                tma_load_3d_pair(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, fb);
+                // A: the stage's KS K-chunks of this CTA's 128 rows, 16 KB apart
+                if (p.a_chunked) {
+                    tma_load_4d_pair(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < KS; ++j)
+                        tma_load_3d_pair(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row, a_rank,
+                                         fb);
+                }
+                // B: 64-column chunks of KS x 64 K rows, 64 KS x 128 B apart
                 const int bcol = gc.nb * BN + (hn ? gc.hn * (BN / 2) + ctl.half * (BN / 4) : ctl.half * (BN / CG));
                 if (p.b_chunked && !hn) {
                     // the CTA's BN / CG columns as one box of 64-column chunks
@@ -677,8 +694,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 } else {
                     const int nbox = hn ? BN / 4 / 64 : BN / CG / 64;
                     for (int c = 0; c < nbox; ++c)
-                        tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * 2), &p.tmB, bcol + c * 64, kb * BK, b_rank,
-                                         fb);
+                        tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * KS * 2), &p.tmB, bcol + c * 64, kb * BK,
+                                         b_rank, fb);
                 }
             }
             issued_phase[stage] = phase;
@@ -755,23 +772,32 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         tr.rec(EV_BEGIN, item);
         const uint32_t d = tmem + buf * BN;
         bool ok = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        constexpr int KS = Smem<BN, STAGES, CG>::KS;
+        for (int kb = 0; kb < p.k_blocks; kb += KS) {
             if (!wait_bar(ctl, &sm.full[stage], phase, WAIT_SMEM_FULL)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // A: K-major, 128-byte swizzle, 8-row core groups 1024 B apart.
-            // B: MN-major, 128-byte swizzle: 64-column chunks 8 KB apart
-            //    (leading offset), 8-row K groups 1024 B apart (stride offset).
-            const uint64_t adesc = smem_desc(smem_u32(sm.a_tile(stage)), 16, 1024);
-            const uint64_t bdesc = smem_desc(smem_u32(sm.b_tile(stage)), 64 * BK * 2, 1024);
+            // A: K-major, 128-byte swizzle, 8-row core groups 1024 B apart;
+            //    K-chunk j of the stage 16 KB further.
+            // B: MN-major, 128-byte swizzle: 64-column chunks 64 KS x 128 B
+            //    apart (leading offset), 8-row K groups 1024 B apart (stride
+            //    offset); K-chunk j starts 64 rows (8 KB) further.
+            const uint32_t a_addr = smem_u32(sm.a_tile(stage));
+            const uint64_t bdesc = smem_desc(smem_u32(sm.b_tile(stage)), 64 * BK * KS * 2, 1024);
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-                // advance A by 16 columns (32 B inside the swizzled row) and
-                // B by 16 rows (2 KB); descriptors hold addresses >> 4
-                umma_f16<CG>(d, adesc + static_cast<uint64_t>(k * 2), bdesc + static_cast<uint64_t>(k * 128),
-                             idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int j = 0; j < KS; ++j) {
+                if (kb + j >= p.k_blocks) break;  // K tail: the chunk past K holds zeros
+                const uint64_t adesc = smem_desc(a_addr + j * (BM * BK * 2), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k) {
+                    // advance A by 16 columns (32 B inside the swizzled row) and
+                    // B by 16 rows (2 KB); descriptors hold addresses >> 4
+                    umma_f16<CG>(d, adesc + static_cast<uint64_t>(k * 2),
+                                 bdesc + static_cast<uint64_t>((j * (BK / UMMA_K) + k) * 128), idesc,
+                                 (kb | j | k) != 0 ? 1u : 0u);
+                }
             }
             // the stage is free again in both CTAs of a pair
             if (CG == 2)
@@ -1760,6 +1786,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
             tma_prefetch_desc(&p.tmA);
             tma_prefetch_desc(&p.tmB);
             if (p.b_chunked) tma_prefetch_desc(&p.tmBc);
+            if (p.a_chunked) tma_prefetch_desc(&p.tmAc);
         }
         if (p.n_gemm > 0) tma_prefetch_desc(&p.tmC);
         if (p.n_gemm > 0 && p.reduce_mode == 3) tma_prefetch_desc(&p.tmS);

@@ -24,7 +24,7 @@ constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
 // 128 x 64 of A and 64 x 128 of B (32 KB) per K-block, six deep
 // (measured: 6 stages ~ 5 stages > 4 stages by 6.5 %; 7 do not fit beside the
 // epilogue staging buffers)
-constexpr int STAGES_PAIR = 6;
+constexpr int STAGES_PAIR = 3;
 constexpr size_t WS_HEADER = 256;
 constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
 
@@ -283,10 +283,10 @@ int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t d0, uint64_t d
 }
 
 // B as 64-column chunks: 4-D {64, k, n / 64, region} (strides N * 2, 128,
-// region), box {64, BK, tile_n / cg / 64, 1}.  One load fills all of a CTA's
-// B columns for a K-block, chunk after chunk 8 KB apart -- the layout the
-// 3-D map's per-chunk loads produce.  Only when N % 64 == 0, so that no
-// chunk runs past the end of a row; otherwise the 3-D map serves alone.
+// region), box {64, BK * KS, tile_n / cg / 64, 1}.  One load fills all of a
+// CTA's B columns for a stage, chunk after chunk 64 KS x 128 B apart -- the
+// layout the 3-D map's per-chunk loads produce.  Only when N % 64 == 0, so
+// that no chunk runs past the end of a row; otherwise the 3-D map serves alone.
 int make_b_chunk_map(Params& p, const Cfg& c, const void* base, int64_t N, int64_t K, uint64_t regions,
                      uint64_t region_stride) {
     p.b_chunked = 0;
@@ -295,13 +295,37 @@ int make_b_chunk_map(Params& p, const Cfg& c, const void* base, int64_t N, int64
     if (!enc) return IRIS_ECUDA;
     cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64), regions};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(N) * 2, 128, region_stride};
-    cuuint32_t box[4] = {64, BK, static_cast<cuuint32_t>(c.tile_n / c.cg / 64), 1};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK * k_per_stage(c.cg)),
+                         static_cast<cuuint32_t>(c.tile_n / c.cg / 64), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = enc(&p.tmBc, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                      const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled (B chunks)", static_cast<int>(r));
     p.b_chunked = 1;
+    return IRIS_OK;
+}
+
+// A as 64-column K chunks (CTA pairs, whose stages hold KS > 1 K blocks):
+// 4-D {64, row, k / 64, region} (strides K * 2, 128, region), box {64, BM,
+// KS, 1}: one load fills a stage's KS chunks of the CTA's 128 rows, 16 KB
+// apart.  Only when K % 64 == 0, so that no chunk runs past the end of a row.
+int make_a_chunk_map(Params& p, const Cfg& c, const void* base, int64_t rows, int64_t K, uint64_t regions,
+                     uint64_t region_stride) {
+    p.a_chunked = 0;
+    const int ks = k_per_stage(c.cg);
+    if (ks == 1 || K % 64 != 0 || K <= 0 || rows <= 0) return IRIS_OK;
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64), regions};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(K) * 2, 128, region_stride};
+    cuuint32_t box[4] = {64, BM, static_cast<cuuint32_t>(ks), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(&p.tmAc, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                     const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled (A chunks)", static_cast<int>(r));
+    p.a_chunked = 1;
     return IRIS_OK;
 }
 
@@ -502,7 +526,9 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     if (p.n_gemm > 0 && K > 0) {
         char* g = p.heap + off_gathered;
         if ((rc = make_map(&p.tmA, g, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
-        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
+        if ((rc = make_a_chunk_map(p, c, g, M, K, 1, round_up(size_t(M) * K * 2, 16)))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
+                           BK * k_per_stage(c.cg))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
@@ -561,7 +587,10 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
-        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64, BK))) return rc;
+        if ((rc = make_a_chunk_map(p, c, p.heap + off_A, M, K, W, heap->rank_stride))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64,
+                           BK * k_per_stage(c.cg))))
+            return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, W, heap->rank_stride))) return rc;
     }
     if (p.n_gemm > 0) {
@@ -640,7 +669,9 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_MATMUL_ALL_GATHER, 0, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
-        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK)))
+        if ((rc = make_a_chunk_map(p, c, p.heap + off_A, M_l, K, W, heap->rank_stride))) return rc;
+        if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
+                           BK * k_per_stage(c.cg))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
@@ -742,7 +773,10 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_CONCURRENT, 0, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, A, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
-        if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64, BK))) return rc;
+        if ((rc = make_a_chunk_map(p, c, A, M, K, 1, round_up(size_t(M) * K * 2, 16)))) return rc;
+        if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
+                           BK * k_per_stage(c.cg))))
+            return rc;
         if ((rc = make_b_chunk_map(p, c, B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
     if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, C, p.bf16, N, M, 1, 1, N * 2, size_t(M) * N * 2,
