@@ -41,9 +41,11 @@ enum : int { COLL_AG = 0, COLL_AR = 1, COLL_RS = 2, COLL_A2A = 3, COLL_BC = 4 };
 
 constexpr int BM = 128;           // tile rows (tcgen05 M for cta_group::1)
 constexpr int BK = 64;            // K per block: 64 x 16-bit = one 128-byte swizzle row
-// K blocks per pipeline stage: CTA pairs take two (one A box and one B box
-// of 128 K rows per stage and CTA), one-CTA tiles one
-__host__ __device__ constexpr int k_per_stage(int cg) { return cg == 2 ? 2 : 1; }
+// K blocks per pipeline stage: the three-stage CTA-pair pipeline takes two
+// (one A box and one B box of 128 K rows per stage and CTA); the six-stage
+// one (operands streaming from DRAM: more, smaller stages in flight) and
+// one-CTA tiles take one
+__host__ __device__ constexpr int k_per_stage(int cg, int stages) { return (cg == 2 && stages <= 3) ? 2 : 1; }
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int NUM_WORKER_WARPS = 4;  // one per tensor-memory lane quadrant (or a multiple of 4)
 constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
@@ -384,7 +386,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
 // A and BN / 2 columns of B per stage.
 template <int BN, int STAGES, int CG>
 struct Smem {
-    static constexpr int KS = k_per_stage(CG);  // K blocks per stage
+    static constexpr int KS = k_per_stage(CG, STAGES);  // K blocks per stage
     static constexpr uint32_t A_BYTES = BM * BK * KS * 2;  // KS chunks of 128 rows x 64 K, 16 KB apart
     static constexpr uint32_t B_BYTES = (BN / CG) * BK * KS * 2;  // 64-column chunks of 64 KS K rows
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;

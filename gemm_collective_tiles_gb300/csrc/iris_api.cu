@@ -21,10 +21,13 @@ namespace {
 constexpr int BN_WIDE = 256, STAGES_WIDE = 4;
 constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
 // CTA pairs (tile_m 256): 256 x 256 tiles over two SMs; each SM stages
-// 128 x 64 of A and 64 x 128 of B (32 KB) per K-block, six deep
-// (measured: 6 stages ~ 5 stages > 4 stages by 6.5 %; 7 do not fit beside the
-// epilogue staging buffers)
+// 128 x 64 of A and 64 x 128 of B (32 KB) per K-block.  Three stages of two
+// K-blocks (one A and one B box per stage: half the TMA instructions and
+// barrier hand-offs), or six stages of one K-block when the operands stream
+// from DRAM (long K), where more, smaller stages keep more bytes in flight.
 constexpr int STAGES_PAIR = 3;
+constexpr int STAGES_PAIR_STREAM = 6;
+constexpr int64_t STREAM_K = 98304;  // K above which the six-stage pipeline is the default
 constexpr size_t WS_HEADER = 256;
 constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
 
@@ -72,12 +75,13 @@ constexpr size_t smem_bytes() {
 
 int g_pair_clusters[64] = {0};  // co-resident CTA pairs of the pair kernel, per device
 
-cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
+                                      size_t smem = smem_bytes<BN_WIDE, STAGES_PAIR, 2>()) {
     cudaLaunchConfig_t lc;
     std::memset(&lc, 0, sizeof(lc));
     lc.gridDim = dim3(grid, 1, 1);
     lc.blockDim = dim3(NUM_THREADS, 1, 1);
-    lc.dynamicSmemBytes = smem_bytes<BN_WIDE, STAGES_PAIR, 2>();
+    lc.dynamicSmemBytes = smem;
     lc.stream = stream;
     attr->id = cudaLaunchAttributeClusterDimension;
     attr->val.clusterDim.x = 2;
@@ -104,6 +108,10 @@ int ensure_attrs(int dev) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes<BN_WIDE, STAGES_PAIR, 2>()));
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_m 256)", static_cast<int>(e));
+    e = cudaFuncSetAttribute(fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR_STREAM, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN_WIDE, STAGES_PAIR_STREAM, 2>()));
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (tile_m 256, 6 stages)", static_cast<int>(e));
     // how many CTA pairs fit at once (one CTA per SM; a pair needs two SMs of
     // one GPC): the persistent pair grid is twice that
     int sms = 0;
@@ -147,6 +155,7 @@ struct Cfg {
     int trace_cap;
     int reduce_mode;  // resolved by the reduce ops (resolve_reduce_mode)
     int rank_inner;
+    int stages;       // CTA pairs: requested 0 / 3 / 6, resolved by resolve_stages; one-CTA tiles: 0
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -158,6 +167,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     out.tile_m = c->tile_m;
     out.cg = 1;
     if (c->tile_k != 0 && c->tile_k != BK) return IRIS_EINVAL;
+    if (c->stages != 0 && c->stages != STAGES_PAIR && c->stages != STAGES_PAIR_STREAM) return IRIS_EINVAL;
+    out.stages = c->stages;
     if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256) return IRIS_EINVAL;
     out.tile_n = c->tile_n ? c->tile_n : (N <= 128 ? 128 : 256);
     if (c->group_m < 0) return IRIS_EINVAL;
@@ -211,15 +222,25 @@ int resolve_reduce_mode(const iris_b200_config* c, iris_op op, int64_t N, int W)
 // launch of the concurrent mode keeps one CTA per item).  The default is
 // pairs; tile_m 128 keeps one CTA per tile.  The pair grid is every
 // co-resident pair (at most grid / 2).
+// CTA pairs: the pipeline by K unless the config chose one
+void resolve_stages(Cfg& c, int64_t K) {
+    if (c.cg != 2) {
+        c.stages = 0;
+        return;
+    }
+    if (c.stages == 0) c.stages = K > STREAM_K ? STAGES_PAIR_STREAM : STAGES_PAIR;
+}
+
 int resolve_pair(Cfg& c, iris_op op, bool has_gemm = true) {
     const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
     const bool applies = has_gemm && c.tile_n == BN_WIDE && (!reduce_op || c.reduce_mode == 3);
     if (c.tile_m == 2 * BM && !applies && has_gemm) return IRIS_EINVAL;
     c.cg = (c.tile_m == BM || !applies) ? 1 : 2;
+    if (c.cg == 1 && c.stages != 0 && has_gemm) return IRIS_EINVAL;  // the pipeline choice is the pairs'
     if (c.cg == 2) {
         const int pairs = std::min(pair_clusters(), c.grid / 2);
         if (pairs < 1) {
-            if (c.tile_m == 2 * BM) return c.grid < 2 ? IRIS_EINVAL : IRIS_ECUDA;
+            if (c.tile_m == 2 * BM || c.stages != 0) return c.grid < 2 ? IRIS_EINVAL : IRIS_ECUDA;
             c.cg = 1;
             return IRIS_OK;
         }
@@ -295,7 +316,7 @@ int make_b_chunk_map(Params& p, const Cfg& c, const void* base, int64_t N, int64
     if (!enc) return IRIS_ECUDA;
     cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64), regions};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(N) * 2, 128, region_stride};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK * k_per_stage(c.cg)),
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK * k_per_stage(c.cg, c.stages)),
                          static_cast<cuuint32_t>(c.tile_n / c.cg / 64), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = enc(&p.tmBc, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -313,7 +334,7 @@ int make_b_chunk_map(Params& p, const Cfg& c, const void* base, int64_t N, int64
 int make_a_chunk_map(Params& p, const Cfg& c, const void* base, int64_t rows, int64_t K, uint64_t regions,
                      uint64_t region_stride) {
     p.a_chunked = 0;
-    const int ks = k_per_stage(c.cg);
+    const int ks = k_per_stage(c.cg, c.stages);
     if (ks == 1 || K % 64 != 0 || K <= 0 || rows <= 0) return IRIS_OK;
     EncodeTiledFn enc = encoder();
     if (!enc) return IRIS_ECUDA;
@@ -382,8 +403,12 @@ int launch(Params& p, const Cfg& c, cudaStream_t stream) {
     if (rc != IRIS_OK) return rc;
     if (c.cg == 2) {
         cudaLaunchAttribute attr;
-        const cudaLaunchConfig_t lc = pair_launch_config(c.grid, stream, &attr);
-        const cudaError_t e = cudaLaunchKernelEx(&lc, fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR, 2>, p);
+        const bool stream_k = c.stages == STAGES_PAIR_STREAM;
+        const cudaLaunchConfig_t lc =
+            pair_launch_config(c.grid, stream, &attr,
+                               stream_k ? smem_bytes<BN_WIDE, STAGES_PAIR_STREAM, 2>() : smem_bytes<BN_WIDE, STAGES_PAIR, 2>());
+        const cudaError_t e = stream_k ? cudaLaunchKernelEx(&lc, fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR_STREAM, 2>, p)
+                                       : cudaLaunchKernelEx(&lc, fused_gemm_coll_kernel<BN_WIDE, STAGES_PAIR, 2>, p);
         if (e != cudaSuccess) return cuda_fail("kernel launch (CTA pairs)", static_cast<int>(e));
     } else if (c.tile_n == BN_WIDE) {
         fused_gemm_coll_kernel<BN_WIDE, STAGES_WIDE, 1>
@@ -464,6 +489,7 @@ int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int wo
     if (!bytes || !dims_ok(M, N, K) || world < 1 || world > IRIS_MAX_WORLD) return IRIS_EINVAL;
     if (op < IRIS_OP_ALL_GATHER_MATMUL || op > IRIS_OP_CONCURRENT) return IRIS_EINVAL;
     (void)dtype;
+    if (cfg && cfg->stages != 0 && cfg->stages != STAGES_PAIR && cfg->stages != STAGES_PAIR_STREAM) return IRIS_EINVAL;
     int tile_n = 256;
     if (cfg && cfg->tile_n) {
         if (cfg->tile_n != 128 && cfg->tile_n != 256) return IRIS_EINVAL;
@@ -496,6 +522,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_ALL_GATHER_MATMUL, N, c))) return rc;
     if ((rc = resolve_pair(c, IRIS_OP_ALL_GATHER_MATMUL))) return rc;
+    resolve_stages(c, K);
     if ((rc = check_region(heap, off_A, size_t(M) * K_l * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -528,7 +555,7 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmA, g, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
         if ((rc = make_a_chunk_map(p, c, g, M, K, 1, round_up(size_t(M) * K * 2, 16)))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
-                           BK * k_per_stage(c.cg))))
+                           BK * k_per_stage(c.cg, c.stages))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
@@ -557,6 +584,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     c.reduce_mode = resolve_reduce_mode(cfg, op, N, W);
     if (c.reduce_mode < 0) return IRIS_EINVAL;
     if ((rc = resolve_pair(c, op))) return rc;
+    resolve_stages(c, K);
     if ((rc = check_region(heap, off_A, size_t(M) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N_l * 2))) return rc;
@@ -589,7 +617,7 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_a_chunk_map(p, c, p.heap + off_A, M, K, W, heap->rank_stride))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, W, N * 2, heap->rank_stride, 64,
-                           BK * k_per_stage(c.cg))))
+                           BK * k_per_stage(c.cg, c.stages))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, W, heap->rank_stride))) return rc;
     }
@@ -643,6 +671,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_MATMUL_ALL_GATHER, N, c))) return rc;
     if ((rc = resolve_pair(c, IRIS_OP_MATMUL_ALL_GATHER))) return rc;
+    resolve_stages(c, K);
     if ((rc = check_region(heap, off_A, size_t(M_l) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -671,7 +700,7 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_a_chunk_map(p, c, p.heap + off_A, M_l, K, W, heap->rank_stride))) return rc;
         if ((rc = make_map(&p.tmB, p.heap + off_B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
-                           BK * k_per_stage(c.cg))))
+                           BK * k_per_stage(c.cg, c.stages))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, p.heap + off_B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }
@@ -724,6 +753,7 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
     }
     const bool launch_gemm = has_gemm && part != 2;
     if ((rc = resolve_pair(c, IRIS_OP_CONCURRENT, launch_gemm))) return rc;
+    resolve_stages(c, K);
     if (count > 0) {
         if (size_t(c.comm_block) * esz % 16 != 0) return IRIS_EALIGN;
         const size_t in_bytes = size_t(count) * esz;
@@ -775,7 +805,7 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
         if ((rc = make_map(&p.tmA, A, p.bf16, K, M, 1, K * 2, round_up(size_t(M) * K * 2, 16), BK, BM))) return rc;
         if ((rc = make_a_chunk_map(p, c, A, M, K, 1, round_up(size_t(M) * K * 2, 16)))) return rc;
         if ((rc = make_map(&p.tmB, B, p.bf16, N, K, 1, N * 2, round_up(size_t(K) * N * 2, 16), 64,
-                           BK * k_per_stage(c.cg))))
+                           BK * k_per_stage(c.cg, c.stages))))
             return rc;
         if ((rc = make_b_chunk_map(p, c, B, N, K, 1, round_up(size_t(K) * N * 2, 16)))) return rc;
     }

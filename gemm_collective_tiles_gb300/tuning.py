@@ -19,7 +19,7 @@ from typing import Callable, Dict, Iterable, List, Optional, Sequence
 ENV_CACHE = "IRIS_B200_CACHE"
 
 # knobs a cached entry may set (the rest stay at their defaults)
-TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block")
+TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block", "stages")
 
 
 def cache_path() -> str:
@@ -87,6 +87,9 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     then the tile width for small N, then -- per op -- the reduce schedule or
     the concurrent CTA split.  The list is truncated to top_k."""
     out: List[dict] = [{}]
+    # the CTA-pair pipeline the default does not pick for this K (three
+    # 128-deep stages up to K = 98304, six 64-deep stages beyond)
+    out.append({"stages": 3 if K > 98304 else 6})
     for gm in (64, 16, 8):   # 32 is the default
         out.append({"group_m": gm})
     pair_tiles = -(-M // 256) * -(-N // 256) * (W if op in ("matmul_reduce_scatter", "matmul_all_reduce") else 1)

@@ -110,7 +110,13 @@ typedef struct {
                               (concurrent: 65% of the grid; the dependent ops: all
                               CTAs); -1 = balanced (every CTA draws from both queues
                               so that both finish together). */
-    int stages;            /* reserved: pipeline depth is fixed per tile_n */
+    int stages;            /* CTA-pair tiles: shared-memory pipeline (192 KB either
+                              way).  0 = by K: 3 stages of two 64-deep K blocks
+                              (one A and one B TMA box per stage), or, when
+                              K > 98304 and the operands stream from DRAM, 6
+                              stages of one K block (more, smaller loads in
+                              flight); 3 or 6 choose.  Other values, or a
+                              nonzero value with one-CTA tiles: IRIS_EINVAL. */
     int comm_block;        /* concurrent mode: elements per comm tile (default 65536) */
     int replicate_outputs; /* 1: also write the W-1 identical copies of replicated
                               outputs into the other heap regions */

@@ -78,6 +78,12 @@ def test_workspace_size_layout():
     assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, None, None) == N.IRIS_EINVAL
     bad = gct.make_config(tile_n=96)
     assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, ctypes.byref(bad), ctypes.byref(out)) == N.IRIS_EINVAL
+    for stages in (1, 4, 5, 7):   # CTA-pair pipelines: 3 or 6 stages (0 = by K)
+        bad = gct.make_config(stages=stages)
+        assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, ctypes.byref(bad), ctypes.byref(out)) == N.IRIS_EINVAL
+    for stages in (0, 3, 6):
+        ok = gct.make_config(stages=stages)
+        assert lib.iris_b200_workspace_size(0, 8, 8, 8, 1, 0, ctypes.byref(ok), ctypes.byref(out)) == N.IRIS_OK
 
 
 def _heap(world=2, stride=1 << 20, base=1 << 20):

@@ -235,3 +235,52 @@ def test_bias_layouts_exact(op, W, M, N, K, grid, layout):
             assert_exact(bits(outs["out"][r]), want[r])
         if want_g is not None:
             assert_exact(bits(outs["gathered"]), want_g)
+
+
+# Both CTA-pair pipelines (3 stages of two K blocks, 6 stages of one) on
+# small-integer inputs: K not a multiple of 64 (A loaded chunk by chunk), an
+# odd number of K blocks (the last 3-stage slot half past K), a single K
+# block, N not a multiple of 64 (B loaded chunk by chunk) and split tails.
+STAGE_CASES = [
+    ("ag_mm", 2, 300, 512, 208, 0), ("ag_mm", 4, 256, 256, 192, 0),
+    ("mm_rs", 4, 300, 512, 64, 0), ("mm_rs", 2, 640, 768, 192, 8),
+    ("mm_ar", 2, 260, 256, 320, 0), ("mm_ag", 2, 2 * 200, 520, 136, 0),
+    ("mm_ag", 4, 4 * 256, 768, 512, 10),
+]
+
+
+@pytest.mark.parametrize("op,W,M,N,K,grid", STAGE_CASES)
+@pytest.mark.parametrize("stages", [3, 6])
+def test_pair_pipelines_exact(op, W, M, N, K, grid, stages):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=2100 + M + N + K, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    want, want_g = oracle_outputs(x)
+    extra = {"stages": stages}
+    if grid:
+        extra["grid"] = grid
+    outs = run(x, 256, extra)
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
+    if want_g is not None:
+        assert_exact(bits(outs["gathered"]), want_g)
+
+
+@pytest.mark.parametrize("stages", [3, 6])
+def test_pair_pipelines_concurrent_gemm(stages):
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem
+    M, N, K = 520, 776, 328
+    A, B = synthetic.make_gemm_inputs(M, N, K, "f16", seed=2200, dist="int", scale=2)
+    prob = ConcurrentProblem(M, N, K, "f16", "all_reduce", 2, 0, config={"stages": stages})
+    prob.upload(A, B)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    assert_exact(bits(prob.outputs()["C"]), oracle.gemm(A, B))
+
+
+def test_pair_pipeline_choice_rejected_for_one_cta_tiles():
+    from gemm_collective_tiles_gb300 import _native
+    x = synthetic.make_fused_inputs("mm_ag", 2, 256, 256, 64, "bf16", seed=2300, dist="int", scale=2)
+    with pytest.raises(_native.IrisError) as e:
+        run(x, 128, {"stages": 6})
+    assert e.value.code == _native.IRIS_EINVAL
