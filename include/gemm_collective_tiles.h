@@ -102,7 +102,9 @@ typedef struct {
                               per pair: the pair whose even CTA is below gemm_ctas
                               prefers the GEMM queue. */
     int tile_n;            /* GEMM tile columns: 128 or 256 (default 256) */
-    int tile_k;            /* K step per pipeline stage: 64 (only value) */
+    int tile_k;            /* K block: 64 (only value); a pipeline stage holds one
+                              K block, or two in the three-stage CTA-pair
+                              pipeline (see stages) */
     int group_m;           /* GROUP_M tile swizzle width in M blocks (default 32) */
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
