@@ -67,6 +67,11 @@ def test_candidates():
     r = tuning.candidates("matmul_reduce_scatter", 4, 4096, 4096, 4096, 152, top_k=50)
     assert {"reduce_mode": 1} in r and {"reduce_mode": 2} in r
     assert len(tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)) == 3
+    # the CTA-pair pipeline the default does not pick for this K is tried early
+    short_k = tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)
+    long_k = tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152, top_k=3)
+    assert {"stages": 6} in short_k and {"stages": 3} not in short_k
+    assert {"stages": 3} in long_k and {"stages": 6} not in long_k
 
 
 def test_all_tuned_knobs_exist_in_the_config_struct():
