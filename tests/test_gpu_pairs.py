@@ -284,3 +284,16 @@ def test_pair_pipeline_choice_rejected_for_one_cta_tiles():
     with pytest.raises(_native.IrisError) as e:
         run(x, 128, {"stages": 6})
     assert e.value.code == _native.IRIS_EINVAL
+
+
+# K > 98304: the default config runs the six-stage pipeline.  Inputs in
+# {-1, 0, 1} keep every fp32 sum exact (|sum| <= K < 2^24).
+@pytest.mark.parametrize("op,W,M,N,K", [("ag_mm", 2, 300, 256, 131072), ("mm_rs", 2, 256, 512, 106496)])
+def test_long_k_default_pipeline_exact(op, W, M, N, K):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=2400 + M, dist="int", scale=1)
+    want, want_g = oracle_outputs(x)
+    outs = run(x, 0)
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
+    if want_g is not None:
+        assert_exact(bits(outs["gathered"]), want_g)
