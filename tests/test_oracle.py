@@ -325,6 +325,38 @@ def test_sampled_variants_match_full():
     assert np.array_equal(oracle.gemm_at(A, B, ii.numpy(), jj.numpy()), c[ii.numpy(), jj.numpy()])
 
 
+# ---------------------------------------------------------- the independent GEMM
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_gemm_golden(dt):
+    g = _load("gemm_small.json")
+    C = oracle.gemm(_t(g["A"], dt), _t(g["B"], dt))
+    assert C.dtype == np.uint16 and C.shape == (2, 4)
+    assert np.array_equal(C, _hex_bits(g[dt]["C_bits"]))
+    ii, jj = np.array([0, 1, 0, 1]), np.array([0, 3, 3, 1])
+    assert np.array_equal(oracle.gemm_at(_t(g["A"], dt), _t(g["B"], dt), ii, jj),
+                          _hex_bits(g[dt]["C_bits"])[ii, jj])
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(5, 7, 9), (3, 11, 4), (8, 2, 13)])
+def test_gemm_exact_integer_brute_force(dt, shape):
+    """C = A @ B on integers in [-8, 8]: every dot product is an exact integer
+    (|C| <= 13 * 64), computed here with Python ints, so the only rounding is
+    the final one to the 16-bit type, taken from torch's own conversion of the
+    exact value (exact in fp32).  bf16 results above 256 do round."""
+    M, N, K = shape
+    A, B = synthetic.make_gemm_inputs(M, N, K, dt, seed=17 + M, dist="int", scale=8)
+    exact = _brute_int(A, B)
+    want = torch.tensor(exact, dtype=torch.float32).to(synthetic.DTYPES[dt]).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.gemm(A, B)
+    assert got.dtype == np.uint16 and got.shape == (M, N)
+    assert np.array_equal(got, want)
+    ii = np.array([i for i in range(M) for _ in range(N)])
+    jj = np.array([j for _ in range(M) for j in range(N)])
+    assert np.array_equal(oracle.gemm_at(A, B, ii, jj), want[ii, jj])
+
+
 # ---------------------------------------------------------- planted mistakes
 
 def test_pins_catch_planted_mistakes(monkeypatch):
@@ -375,6 +407,18 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         return ((u + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
     monkeypatch.setattr(ref, "round_bf16_bits", away)
     assert fails(test_rne16_golden_cases)
+    monkeypatch.undo()
+
+    # 6. fp16 GEMM inputs taken as bf16: the output rounded to the wrong type
+    monkeypatch.setattr(ref, "_dtype_name", lambda t: "bf16")
+    assert fails(lambda: test_gemm_golden("f16"))
+    assert fails(lambda: test_gemm_exact_integer_brute_force("f16", (5, 7, 9)))
+    monkeypatch.undo()
+
+    # 7. the last term of every dot product dropped (an off-by-one K loop)
+    monkeypatch.setattr(ref, "accumulate", lambda X, Y: orig_acc(X[:, :-1], Y[:-1, :]))
+    assert fails(lambda: test_gemm_golden("bf16"))
+    assert fails(lambda: test_gemm_exact_integer_brute_force("bf16", (5, 7, 9)))
     monkeypatch.undo()
 
 
