@@ -5,13 +5,21 @@ One step = one call of the fused op over one batch of synthetic input: by
 default matmul_reduce_scatter, W=4 emulated ranks, A_r and B_r 4096 x 4096
 fp16, bias fp16 (N = 4096), uniform inputs (seed 1) -- all W ranks' GEMMs,
 the fp32 partials, the rank-order reduction and the scatter run inside the
-one persistent kernel.  Prints one JSON line (rank 0).
+one persistent kernel.  Prints one JSON line (rank 0), last.
+
+Before that line, the default single-GPU run also measures every other
+workload of the family, one compact JSON line each (and a summary of them
+inside the last line): all_gather_matmul and matmul_all_gather W=8 4096 x
+14336 x 4096 bf16, the concurrent bf16 GEMM 8192^3 beside an all-reduce of
+8 x 64Mi fp32 (with the sequential arms and a gemm_ctas sweep from 25 % to
+90 % of the SMs), all_gather_matmul W=8 131072 x 16384 x 16384 bf16,
+matmul_all_reduce W=8 8192^3 bf16 and the small all_gather_matmul W=2 256^3.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--config '{"gemm_ctas": 100}']
+                  [--workload NAME] [--config '{"gemm_ctas": 100}'] [--headline-only]
 
 --impl reference times the CPU oracle (the plain definition of the same op)
-on this machine's host cores, each step a bounded sample of the workload.
+on this machine's host cores, each step a bounded row slice of the workload.
 Under torchrun every rank runs an independent replica (the emulated ranks all
 live on one GPU; there is no data-path collective between GPUs).
 """
@@ -224,33 +232,11 @@ def oracle_rows(wl: dict, x, rows: int):
     return 2.0 * W * rows * wl["N"] * wl["K"]
 
 
-def oracle_sampled(wl: dict, x, n: int, seed: int):
-    """Oracle on n sampled output elements: returns the flops they represent."""
-    import oracle
-    op, W, M, N, K = wl["op"], wl["W"], wl["M"], wl["N"], wl["K"]
-    if op == "mm_rs":
-        ii, jj = synthetic.sample_indices(M, N // W, seed, n=n, tile_m=1, tile_n=1)
-        ii, jj = ii[:n].numpy(), jj[:n].numpy()
-        oracle.matmul_reduce_scatter_at(x.A, x.B, x.bias, seed % W, ii, jj)
-        return 2.0 * W * K * len(ii)
-    ii, jj = synthetic.sample_indices(M, N, seed, n=n, tile_m=1, tile_n=1)
-    ii, jj = ii[:n].numpy(), jj[:n].numpy()
-    if op == "mm_ar":
-        oracle.matmul_all_reduce_at(x.A, x.B, x.bias, ii, jj)
-        return 2.0 * W * K * len(ii)
-    if op == "ag_mm":
-        oracle.all_gather_matmul_at(x.A, x.B[0], x.bias, ii, jj)
-        return 2.0 * K * len(ii)
-    oracle.matmul_all_gather_at(x.A, x.B[0], x.bias, ii, jj)
-    return 2.0 * K * len(ii)
-
-
-def cpu_baseline(wl: dict, x, target_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the workload: a row
-    slice sized to about target_s, or -- when the host finishes every row
-    sooner -- whole passes over all rows, repeated up to about target_s."""
+def size_oracle_sample(wl: dict, x, target_s: float):
+    """Rows of every rank whose oracle run takes about target_s on this host,
+    from two probes that separate the per-call cost (operand conversion) from
+    the per-row cost.  Returns (rows, max_rows, seconds per pass over all rows)."""
     max_rows = wl["M"] if wl["op"] != "mm_ag" else wl["M"] // wl["W"]
-    # two probes separate the per-call cost (operand conversion) from the per-row cost
     probe = [min(32, max_rows), min(128, max_rows)]
     times = []
     for r in probe:
@@ -259,11 +245,23 @@ def cpu_baseline(wl: dict, x, target_s: float = 12.0):
         times.append(time.perf_counter() - t0)
     per_row = max((times[1] - times[0]) / max(probe[1] - probe[0], 1), 1e-7)
     fixed = max(times[0] - probe[0] * per_row, 0.0)
+    rows = int(min(max_rows, max(probe[0], (target_s - fixed) / per_row)))
+    return rows, max_rows, fixed + max_rows * per_row
+
+
+def host_threads() -> dict:
+    return {"cores": blas_threads(), "nproc": os.cpu_count() or 1}
+
+
+def cpu_baseline(wl: dict, x, target_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the workload: a row
+    slice sized to about target_s, or -- when the host finishes every row
+    sooner -- whole passes over all rows, repeated up to about target_s."""
     budget = target_s * 0.8
-    rows = int(min(max_rows, max(probe[0], (budget - fixed) / per_row)))
+    rows, max_rows, full_s = size_oracle_sample(wl, x, budget)
     passes = 1
     if rows == max_rows:
-        passes = int(max(1, min(20, budget / max(fixed + max_rows * per_row, 1e-3))))
+        passes = int(max(1, min(20, budget / max(full_s, 1e-3))))
     flops = 0.0
     t0 = time.perf_counter()
     for _ in range(passes):
@@ -271,42 +269,41 @@ def cpu_baseline(wl: dict, x, target_s: float = 12.0):
     dt = time.perf_counter() - t0
     what = (f"{passes} passes over all {rows} output rows of every rank" if passes > 1
             else f"first {rows} output rows of every rank")
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+    th = host_threads()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": th["cores"], "nproc": th["nproc"],
+            "kind": "oracle",
             "sample": f"{what} (full N={wl['N']}, K={wl['K']}), {flops:.3g} flop in {dt:.2f} s "
-                      f"(fp64 dot products, numpy BLAS)"}
+                      f"(fp64 dot products, numpy BLAS on {th['cores']} threads of {th['nproc']} cores)"}
 
 
-def run_reference(args, wl, name):
+def run_reference(args, wl, name, cfg):
+    """The reference arm: the CPU oracle, as it stands, on the host cores.
+    Each step runs the oracle on the first `rows` output rows of every rank
+    (all of N and K), the same sample kind as the cpu_baseline leg, sized so
+    that the whole --steps/--warmup run takes about two minutes."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     x = synthetic.make_fused_inputs(**wl)
     steps, warm = args.steps, args.warmup
-    budget = 150.0
-    t0 = time.perf_counter()
-    oracle_sampled(wl, x, 16, 0)
-    t16 = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle_sampled(wl, x, 64, 0)
-    t64 = time.perf_counter() - t0
-    per = max((t64 - t16) / 48, 1e-6)
-    fixed = max(t16 - 16 * per, 0.0)
-    n = int(max(1, min(4096, (budget / (steps + warm) - fixed) / per)))
-    for i in range(warm):
-        oracle_sampled(wl, x, n, 1 + i)
+    rows, _max_rows, _ = size_oracle_sample(wl, x, 120.0 / (steps + warm))
+    for _ in range(warm):
+        oracle_rows(wl, x, rows)
     flops = 0.0
     t0 = time.perf_counter()
-    for i in range(steps):
-        flops += oracle_sampled(wl, x, n, 1000 + i)
+    for _ in range(steps):
+        flops += oracle_rows(wl, x, rows)
     dt = time.perf_counter() - t0
     val = flops / dt / 1e12
-    cores = blas_threads()
+    th = host_threads()
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(wl, name, {}),
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{n} sampled output elements per step (fp64 dot products over all W ranks)"},
+            "config": bench_config(wl, name, cfg, args.gpus),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": th["cores"], "nproc": th["nproc"],
+                             "kind": "oracle",
+                             "sample": f"first {rows} output rows of every rank per step (full N={wl['N']}, "
+                                       f"K={wl['K']}; fp64 dot products, numpy BLAS)"},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -320,6 +317,14 @@ def workload_config(wl, name, cfg):
          "op": OP_NAMES[wl["op"]], "world_size_emulated": wl["W"], "M": wl["M"], "N": wl["N"],
          "K": wl["K"], "seed": wl["seed"], "dist": wl["dist"]}
     d.update({k: v for k, v in cfg.items()})
+    return d
+
+
+def bench_config(wl, name, cfg, world):
+    """The `config` object of a bench line; both arms print the same one."""
+    d = workload_config(wl, name, cfg)
+    d["l2"] = "flushed before every step (258 MB memset outside the step's events)"
+    d["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU"
     return d
 
 
@@ -367,13 +372,16 @@ def library_reference(prob, wl, stream, flush):
     return {"what": what, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "reps": reps}
 
 
-def run_concurrent(args, cfg):
+def concurrent_measure(cfg, steps, warm, sweep=False, two_stream=False):
     """Independent GEMM (bf16 8192^3, normal(0,1), seed 3) sharing the SMs with
-    an all-reduce of W=8 fp32 buffers of 64Mi elements (uniform[-1,1], seed 4).
-    value = GEMM TFLOP/s over the whole step; the roofline is
-    max(GEMM flop / tensor peak, collective bytes / HBM bandwidth).  The
-    all-reduce writes a separate output (the same bytes as in place, and the
-    inputs stay unchanged across steps)."""
+    an all-reduce of W=8 fp32 buffers of 64Mi elements (uniform[-1,1], seed 4),
+    in one launch.  Also times the sequential arms (the GEMM alone on every
+    SM, then the all-reduce alone on every SM); optionally the gemm_ctas
+    sweep and the two-stream modes.  The roofline is max(GEMM flop / tensor
+    peak, all bytes / HBM bandwidth), the bytes counting the collective's
+    W reads and W writes and the GEMM's A, B and C once.  The all-reduce
+    writes a separate output (the same bytes as in place, and the inputs stay
+    unchanged across steps)."""
     from gemm_collective_tiles_gb300 import query_status
     from gemm_collective_tiles_gb300.runner import ConcurrentProblem
     cw = synthetic.CONCURRENT_WORKLOAD
@@ -390,15 +398,15 @@ def run_concurrent(args, cfg):
         pr.upload(A if gemm else None, B if gemm else None, X if coll else None)
         return pr
 
-    def timeit(probs, steps, warm):
+    def timeit(probs, n, w):
         stream = torch.cuda.current_stream()
-        for _ in range(warm):
+        for _ in range(w):
             for pr in probs:
                 pr.run(stream)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
+        for _ in range(n):
             for pr in probs:
                 pr.run(stream)
         e1.record(stream)
@@ -407,100 +415,98 @@ def run_concurrent(args, cfg):
             rc = query_status(pr.ws, stream)
             if rc[0] != 0:
                 raise RuntimeError(f"device status {rc}")
-        return e0.elapsed_time(e1) / steps
+        return e0.elapsed_time(e1) / n
 
     flops = 2.0 * cw["M"] * cw["N"] * cw["K"]
     coll_bytes = 2.0 * cw["W"] * cw["count"] * 4
-    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), coll_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    steps = max(3, min(args.steps, 200))
-    warm = max(3, args.warmup)
+    gemm_bytes = 2.0 * (cw["M"] * cw["K"] + cw["K"] * cw["N"] + cw["M"] * cw["N"])
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+    t_hbm = (coll_bytes + gemm_bytes) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_roof = max(t_tensor, t_hbm)
     fused = make(cfg)
     sampler = ClockSampler(0)
     sampler.start()
     ms = timeit([fused], steps, warm)
     clocks = sampler.stop()
     del fused
-    # the two-stream mode: GEMM kernel and collective kernel side by side
-    two = make(cfg)
-    s_g, s_c = torch.cuda.Stream(), torch.cuda.Stream()
-    sms_all = torch.cuda.get_device_properties(0).multi_processor_count
-
-    def time_two(gemm_ctas):
-        conf = dict(cfg)
-        conf["gemm_ctas"] = gemm_ctas
-        from gemm_collective_tiles_gb300 import make_config
-        two.config = make_config(**conf)
-        for _ in range(2):
-            two.run_two_stream(s_g, s_c)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(steps):
-            two.run_two_stream(s_g, s_c)
-        torch.cuda.synchronize()
-        return (time.perf_counter() - t0) * 1e3 / steps
-    two_stream = {str(g): time_two(g) for g in (sms_all // 2, int(sms_all * 0.55), int(sms_all * 0.45))}
-
-    # the same on two green contexts with disjoint SM sets (the split enforced
-    # by the driver): GEMM streams get at least g SMs, the collective the rest
-    from gemm_collective_tiles_gb300 import make_config, sm_partition_release, sm_partition_streams
-
-    def time_green(g):
-        s_gemm, s_comm, gs, cs = sm_partition_streams(g)
-        try:
-            conf = dict(cfg)
-            conf.update(gemm_ctas=gs, grid=gs + cs)
-            two.config = make_config(**conf)
-            for _ in range(2):
-                two.run_two_stream(s_gemm, s_comm)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for _ in range(steps):
-                two.run_two_stream(s_gemm, s_comm)
-            torch.cuda.synchronize()
-            return gs, (time.perf_counter() - t0) * 1e3 / steps
-        finally:
-            torch.cuda.synchronize()
-            sm_partition_release()
-    green = {}
-    for g in (72, 80, 88, 96):
-        gs, t = time_green(g)
-        green[str(gs)] = t
-    del two
+    res = {"flops": flops, "ms": ms, "clocks": clocks, "peak_kind": peak_kind,
+           "roofline": {"bound": "hbm" if t_hbm >= t_tensor else "tensor", "roofline_ms": t_roof,
+                        "frac": t_roof / ms, "bytes": coll_bytes + gemm_bytes,
+                        "peak_source": f"{peak_kind} bf16 burst and HBM copy"}}
     g_only = make(cfg, coll=False)
-    c_only = make(cfg, gemm=False)
     ms_g = timeit([g_only], steps, warm)
+    del g_only
+    c_only = make(cfg, gemm=False)
     ms_c = timeit([c_only], steps, warm)
-    del g_only, c_only
-    line = {"metric": "concurrent GEMM + all-reduce step: GEMM TFLOPS over the step; % of max(tensor, HBM) roofline",
-            "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warm,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": "concurrent: bf16 GEMM 8192^3 || all_reduce W=8 x 64Mi fp32 (concurrent_ar_w8)",
-                       **cfg},
-            "roofline": {"bound": "hbm" if coll_bytes / peaks["hbm_gbs"] > flops / peaks["bf16_tflops"] / 1e3 else "tensor",
-                         "roofline_ms": t_roof, "frac": t_roof / ms, "peak_source": peak_kind},
-            "sequential": {"gemm_ms": ms_g, "all_reduce_ms": ms_c, "sum_ms": ms_g + ms_c,
-                           "speedup_concurrent_vs_sequential": (ms_g + ms_c) / ms,
-                           "gemm_tflops_alone": flops / (ms_g * 1e-3) / 1e12,
-                           "all_reduce_gbs_alone": coll_bytes / (ms_c * 1e-3) / 1e9},
-            "two_stream_ms_by_gemm_ctas": two_stream,
-            "two_stream_green_ctx_ms_by_gemm_sms": green,
-            "gpu_launches": steps, "clocks": clocks}
-    if args.sweep:
+    del c_only
+    res["sequential"] = {"gemm_ms": ms_g, "all_reduce_ms": ms_c, "sum_ms": ms_g + ms_c,
+                         "speedup_concurrent_vs_sequential": (ms_g + ms_c) / ms,
+                         "gemm_tflops_alone": flops / (ms_g * 1e-3) / 1e12,
+                         "all_reduce_gbs_alone": coll_bytes / (ms_c * 1e-3) / 1e9}
+    if sweep:
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        sweep = []
+        pts = {}
         for frac in (0.25, 0.35, 0.45, 0.55, 0.65, 0.75, 0.85, 0.9):
             conf = dict(cfg)
             conf["gemm_ctas"] = max(1, int(round(frac * sms)))
             pr = make(conf)
-            t = timeit([pr], max(3, steps // 4), 2)
-            sweep.append({"gemm_ctas": conf["gemm_ctas"], "ms": t})
+            pts[str(conf["gemm_ctas"])] = timeit([pr], max(3, steps // 2), 2)
             del pr
         conf = dict(cfg)
         conf["gemm_ctas"] = -1
         pr = make(conf)
-        sweep.append({"gemm_ctas": "balanced", "ms": timeit([pr], max(3, steps // 4), 2)})
-        line["gemm_ctas_sweep"] = sweep
+        pts["balanced"] = timeit([pr], max(3, steps // 2), 2)
+        del pr
+        res["gemm_ctas_sweep_ms"] = pts
+    if two_stream:
+        from gemm_collective_tiles_gb300 import make_config, sm_partition_release, sm_partition_streams
+        two = make(cfg)
+        sms_all = torch.cuda.get_device_properties(0).multi_processor_count
+
+        def time_two(conf, s_g, s_c):
+            two.config = make_config(**conf)
+            for _ in range(2):
+                two.run_two_stream(s_g, s_c)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                two.run_two_stream(s_g, s_c)
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) * 1e3 / steps
+        s_g, s_c = torch.cuda.Stream(), torch.cuda.Stream()
+        res["two_stream_ms_by_gemm_ctas"] = {
+            str(g): time_two({**cfg, "gemm_ctas": g}, s_g, s_c)
+            for g in (sms_all // 2, int(sms_all * 0.55), int(sms_all * 0.45))}
+        # the same on two green contexts with disjoint SM sets (the split
+        # enforced by the driver): the GEMM stream gets at least g SMs
+        green = {}
+        for g in (72, 80, 88, 96):
+            s_gemm, s_comm, gs, cs = sm_partition_streams(g)
+            try:
+                green[str(gs)] = time_two({**cfg, "gemm_ctas": gs, "grid": gs + cs}, s_gemm, s_comm)
+            finally:
+                torch.cuda.synchronize()
+                sm_partition_release()
+        res["two_stream_green_ctx_ms_by_gemm_sms"] = green
+        del two
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_concurrent(args, cfg):
+    steps = max(3, min(args.steps, 200))
+    warm = max(3, args.warmup)
+    r = concurrent_measure(cfg, steps, warm, sweep=args.sweep, two_stream=True)
+    line = {"metric": "concurrent GEMM + all-reduce step: GEMM TFLOPS over the step; % of max(tensor, HBM) roofline",
+            "value": r["flops"] / (r["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+            "warmup": warm, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "concurrent: bf16 GEMM 8192^3 || all_reduce W=8 x 64Mi fp32 (concurrent_ar_w8)",
+                       **cfg},
+            "roofline": r["roofline"], "sequential": r["sequential"], "gpu_launches": steps, "clocks": r["clocks"]}
+    for k in ("gemm_ctas_sweep_ms", "two_stream_ms_by_gemm_ctas", "two_stream_green_ctx_ms_by_gemm_sms"):
+        if k in r:
+            line[k] = r[k]
     print(json.dumps(line), flush=True)
     return 0
 
@@ -593,11 +599,164 @@ def run_shape_sweep(args, cfg):
     return 0
 
 
+# the workloads measured beside the headline in the default run: (name,
+# inputs drawn on the host by the recipe or -- for the multi-GB ones -- on
+# the device, steps multiplier)
+OTHER_CONFIGS = [
+    ("ag_mm_w8_4096x14336x4096", "host", 1),
+    ("mm_ag_w8_4096x14336x4096", "host", 1),
+    ("ag_mm_w8_131072x16384x16384", "device", 1),
+    ("mm_ar_w8_8192", "device", 1),
+    ("ag_mm_w2_256", "host", 10),
+]
+
+
+def make_problem(name, cfg, inputs="host"):
+    """The fused problem of workload `name` with its inputs in the heap:
+    drawn on the host by the workload's recipe (seed, distribution, draw
+    order), or for timing-only runs of multi-GB workloads drawn on the device
+    from the same seed and distribution (synthetic.fill_device_)."""
+    from gemm_collective_tiles_gb300.runner import FusedProblem
+    wl = dict(synthetic.WORKLOADS[name])
+    prob = FusedProblem(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"], wl["dtype"], bias=wl.get("bias", False),
+                        config=cfg)
+    x = None
+    if inputs == "host":
+        x = synthetic.make_fused_inputs(**wl)
+        prob.upload(x.A, x.B, x.bias)
+    else:
+        seed = wl["seed"] * 1000
+        for r in range(wl["W"]):
+            synthetic.fill_device_(prob.heap.view(prob.A, r), seed + r, wl["dist"], wl["scale"])
+            if prob.per_rank_b() or r == 0:
+                synthetic.fill_device_(prob.heap.view(prob.B, r), seed + 100 + r, wl["dist"], wl["scale"])
+        if prob.bias is not None:
+            for r in range(wl["W"] if prob.per_rank_b() else 1):
+                synthetic.fill_device_(prob.heap.view(prob.bias, r), seed + 200, "uniform", wl.get("bias_scale", 0.1))
+    return wl, prob, x
+
+
+def time_steps(prob, steps, warm, stream, flush, pg=None, sample_gpu=0):
+    """Warm-up, then `steps` timed calls, each bracketed by its own events
+    with an L2 flush before it (outside the events).  Returns (per-step ms,
+    clocks sampled during the timed region, host wall seconds)."""
+    from gemm_collective_tiles_gb300 import query_status
+    for _ in range(warm):
+        prob.run(stream)
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after warm-up: {rc}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(sample_gpu)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()                      # evict L2 between steps (outside the step events)
+        starts[i].record(stream)
+        prob.run(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after timed steps: {rc}")
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], clocks, wall
+
+
+def short_clocks(c):
+    if not c:
+        return None
+    return {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"), "samples": c.get("samples"),
+            "reasons": c.get("reasons")}
+
+
+def run_other_configs(args, cfg, stream, flush):
+    """Every other workload of the family on this GPU, one compact JSON line
+    each; returns {name: summary} for the headline line."""
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    summary = {}
+    for name, inputs, mult in OTHER_CONFIGS:
+        wl, prob, _x = make_problem(name, cfg, inputs)
+        steps = max(3, args.steps * mult)
+        step_ms, clocks, _wall = time_steps(prob, steps, args.warmup, stream, flush)
+        flops = prob.flops()
+        mean_ms = statistics.mean(step_ms)
+        tf = flops / (mean_ms * 1e-3) / 1e12
+        base = pages_tflops(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"])
+        line = {"config_line": name, "workload": workload_config(wl, name, {})["workload"], "value": tf,
+                "unit": "TFLOP/s", "ms_per_step": mean_ms, "median_ms": statistics.median(step_ms),
+                "steps": steps, "inputs": inputs,
+                "roofline": {"bound": "tensor", "frac": tf / peak, "peak": peak,
+                             "peak_source": f"{peak_kind} bf16 burst"},
+                "pages_mi300x_tflops": base, "gpu_launches": steps, "clocks": short_clocks(clocks)}
+        print(json.dumps(line), flush=True)
+        summary[name] = {"value": round(tf, 1), "ms": round(mean_ms, 4), "frac": round(tf / peak, 4),
+                         "steps": steps}
+        del prob
+        torch.cuda.empty_cache()
+    steps = max(3, args.steps)
+    r = concurrent_measure(cfg, steps, args.warmup, sweep=True)
+    sweep = r.get("gemm_ctas_sweep_ms", {})
+    best = min(sweep.items(), key=lambda kv: kv[1]) if sweep else (None, None)
+    line = {"config_line": "concurrent_ar_w8",
+            "workload": "concurrent: bf16 GEMM 8192^3 || all_reduce W=8 x 64Mi fp32 (default split)",
+            "value": r["flops"] / (r["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": r["ms"],
+            "steps": steps, "roofline": {"bound": r["roofline"]["bound"], "frac": r["roofline"]["frac"],
+                                         "roofline_ms": r["roofline"]["roofline_ms"]},
+            "sequential_ms": r["sequential"]["sum_ms"],
+            "speedup_concurrent_vs_sequential": r["sequential"]["speedup_concurrent_vs_sequential"],
+            "gemm_ms_alone": r["sequential"]["gemm_ms"], "all_reduce_ms_alone": r["sequential"]["all_reduce_ms"],
+            "gemm_ctas_sweep_ms": {k: round(v, 4) for k, v in sweep.items()}, "best_gemm_ctas": best[0],
+            "gpu_launches": steps, "clocks": short_clocks(r["clocks"])}
+    print(json.dumps(line), flush=True)
+    summary["concurrent_ar_w8"] = {"ms": round(r["ms"], 4), "frac": round(r["roofline"]["frac"], 4),
+                                   "speedup_vs_sequential": round(r["sequential"]["speedup_concurrent_vs_sequential"], 3),
+                                   "best_gemm_ctas": best[0]}
+    return summary
+
+
+def sustained(prob, stream, peak_sustained, seconds=2.5):
+    """The headline op back to back for about `seconds` (no flush between
+    calls: the working set is several times the L2), one event pair around
+    the whole loop, against the measured sustained peak."""
+    for _ in range(20):
+        prob.run(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(50):
+        prob.run(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = max(50, int(seconds * 1e3 / max(e0.elapsed_time(e1) / 50, 1e-3)))
+    sampler = ClockSampler(0)
+    sampler.start()
+    e0.record(stream)
+    for _ in range(n):
+        prob.run(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / n
+    tf = prob.flops() / (ms * 1e-3) / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n, "peak": peak_sustained,
+            "frac": tf / peak_sustained, "l2": "not flushed (back to back; working set > L2)",
+            "clocks": short_clocks(clocks)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(synthetic.WORKLOADS) + ["concurrent_ar_w8", "ag_mm_shape_sweep"])
@@ -606,6 +765,8 @@ def main():
                     help="concurrent workload: also time gemm_ctas from 25%% to 90%% of the SMs")
     ap.add_argument("--config", default="{}", help="JSON dict of iris_b200_config fields")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads measured before the headline line")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -623,7 +784,7 @@ def main():
     wl = dict(synthetic.WORKLOADS[args.workload])
 
     if args.impl == "reference":
-        return run_reference(args, wl, args.workload)
+        return run_reference(args, wl, args.workload, cfg)
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -636,42 +797,15 @@ def main():
     from gemm_collective_tiles_gb300 import query_status
     from gemm_collective_tiles_gb300.runner import FusedProblem
 
-    x = synthetic.make_fused_inputs(**wl)
-    prob = FusedProblem(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"], wl["dtype"], bias=wl.get("bias", False),
-                        config=cfg)
-    prob.upload(x.A, x.B, x.bias)
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    others = None
+    if world == 1 and not args.headline_only and args.workload == DEFAULT_WORKLOAD:
+        others = run_other_configs(args, cfg, stream, flush)
 
-    for _ in range(args.warmup):
-        prob.run(stream)
-    rc = query_status(prob.ws, stream)
-    if rc[0] != 0:
-        raise RuntimeError(f"device status after warm-up: {rc}")
-
+    wl, prob, x = make_problem(args.workload, cfg, "host")
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    sampler = ClockSampler(local)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush.zero_()                      # evict L2 between steps (outside the step events)
-        starts[i].record(stream)
-        prob.run(stream)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if pg:
-        pg.barrier()
-    clocks = sampler.stop()
-    rc = query_status(prob.ws, stream)
-    if rc[0] != 0:
-        raise RuntimeError(f"device status after timed steps: {rc}")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms, clocks, wall = time_steps(prob, K, args.warmup, stream, flush, pg, local)
     total_ms = max_over_ranks(sum(step_ms), pg)
     flops = prob.flops()
     value = job_throughput(flops, world, K, total_ms)
@@ -686,6 +820,9 @@ def main():
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json) x 1.0 fp16/bf16 nominal ratio",
                 "kernel": KERNEL_NAME, "median_ms": statistics.median(step_ms)}
+    sus = None
+    if world == 1 and not args.headline_only:
+        sus = sustained(prob, stream, float(peaks.get("bf16_tflops_sustained", peak)))
 
     # end to end: pinned host inputs -> heap, fused op, outputs -> pinned host,
     # every step.  Two problem instances alternate so that step i's uploads
@@ -752,16 +889,17 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         del flush
         cpu = cpu_baseline(wl, x)
-    cfg_out = workload_config(wl, args.workload, cfg)
-    cfg_out["l2"] = "flushed before every step (258 MB memset outside the step's events)"
-    cfg_out["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU"
     base = pages_tflops(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"])
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / world / base) if base else None, "dtype": wl["dtype"], "data": "synthetic",
-            "config": cfg_out,
+            "config": bench_config(wl, args.workload, cfg, world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K,
             "clocks": clocks, "wall_s_timed_region": wall, "library_reference": lib_ref}
+    if sus is not None:
+        line["sustained"] = sus
+    if others is not None:
+        line["other_configs"] = others
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
