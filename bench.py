@@ -706,6 +706,7 @@ def run_other_configs(args, cfg, stream, flush):
     r = concurrent_measure(cfg, steps, args.warmup, sweep=True)
     sweep = r.get("gemm_ctas_sweep_ms", {})
     best = min(sweep.items(), key=lambda kv: kv[1]) if sweep else (None, None)
+    pred = predictor_vs_sweep(sweep)
     line = {"config_line": "concurrent_ar_w8",
             "workload": "concurrent: bf16 GEMM 8192^3 || all_reduce W=8 x 64Mi fp32 (default split)",
             "value": r["flops"] / (r["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": r["ms"],
@@ -715,12 +716,38 @@ def run_other_configs(args, cfg, stream, flush):
             "speedup_concurrent_vs_sequential": r["sequential"]["speedup_concurrent_vs_sequential"],
             "gemm_ms_alone": r["sequential"]["gemm_ms"], "all_reduce_ms_alone": r["sequential"]["all_reduce_ms"],
             "gemm_ctas_sweep_ms": {k: round(v, 4) for k, v in sweep.items()}, "best_gemm_ctas": best[0],
-            "gpu_launches": steps, "clocks": short_clocks(r["clocks"])}
+            "predictor": pred, "gpu_launches": steps, "clocks": short_clocks(r["clocks"])}
     print(json.dumps(line), flush=True)
     summary["concurrent_ar_w8"] = {"ms": round(r["ms"], 4), "frac": round(r["roofline"]["frac"], 4),
                                    "speedup_vs_sequential": round(r["sequential"]["speedup_concurrent_vs_sequential"], 3),
                                    "best_gemm_ctas": best[0]}
     return summary
+
+
+def predictor_vs_sweep(sweep):
+    """The split predictor's makespans for the measured gemm_ctas points (the
+    default tile kind), its best split against the measured best, and the
+    rank correlation of the two orders."""
+    from gemm_collective_tiles_gb300 import predictor
+    cw = synthetic.CONCURRENT_WORKLOAD
+    pts = {k: v for k, v in sweep.items() if k.isdigit()}
+    if len(pts) < 3:
+        return None
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = predictor.Workload(M=cw["M"], N=cw["N"], K=cw["K"], coll="all_reduce", W=cw["W"], count=cw["count"])
+    tk = next(t for t in predictor.TILE_KINDS if t.name == predictor.PREFERRED_TILE)
+    pred = {k: predictor.simulate(wl, int(k), predictor.Machine(sms=sms), tk) / 1e3 for k in pts}
+    keys = sorted(pts)
+
+    def ranks(d):
+        order = sorted(keys, key=lambda k: d[k])
+        return {k: i for i, k in enumerate(order)}
+    rp, rm = ranks(pred), ranks(pts)
+    n = len(keys)
+    rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
+    return {"predicted_ms": {k: round(v, 4) for k, v in pred.items()},
+            "predicted_best": min(pred, key=pred.get), "measured_best": min(pts, key=pts.get),
+            "rank_correlation": round(rho, 3)}
 
 
 def sustained(prob, stream, peak_sustained, seconds=2.5):

@@ -126,15 +126,22 @@ def make_config(**kw) -> iris_b200_config:
     return c
 
 
-def _resolve(cfg, op: str, W: int, M: int, N: int, K: int, dtype: torch.dtype):
-    """config="auto": the measured winner cached for this device and shape
-    (see tuning.py), else the static default."""
+_DTN = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
+
+
+def _resolve(cfg, op: str, W: int, M: int, N: int, K: int, dtype: torch.dtype, coll: Optional[str] = None,
+             count: int = 0, coll_dtype: Optional[torch.dtype] = None):
+    """config="auto": the measured winner cached for this device and shape,
+    else the winner of the nearest cached shape, else the static default
+    (see tuning.py)."""
     if isinstance(cfg, str):
         if cfg != "auto":
             raise ValueError(f"unknown config {cfg!r}")
         from . import tuning
-        name = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[dtype]
-        hit = tuning.select(tuning.device_arch(), tuning.shape_key(op, W, M, N, K, name))
+        cdt = _DTN[coll_dtype] if coll_dtype is not None else "f32"
+        key = tuning.shape_key(op, W, M, N, K, _DTN[dtype], coll, count, cdt)
+        shape = tuning.shape_info(op, W, M, N, K, _DTN[dtype], coll, count, cdt)
+        hit = tuning.select(tuning.device_arch(), key, shape=shape)
         return hit or None
     return cfg
 
@@ -261,7 +268,8 @@ def concurrent_gemm_collective(A: Optional[torch.Tensor], B: Optional[torch.Tens
         dev = heap.buf.device
     W = heap.world if heap is not None else 1
     count = x_in.nbytes // torch.empty((), dtype=x_in.dtype).element_size() if x_in is not None else 0
-    config = _resolve(config, "concurrent", W, M, N, K, gdt)
+    config = _resolve(config, "concurrent", W, M, N, K, gdt, coll if count else None, count,
+                      x_in.dtype if x_in is not None else None)
     ws = _ws(workspace, workspace_size("concurrent", M, N, K, W, gdt, config), dev)
     hp = ctypes.byref(heap.c_heap()) if heap is not None else None
     _native.check("iris_b200_concurrent_gemm_collective",

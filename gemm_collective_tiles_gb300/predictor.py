@@ -13,6 +13,14 @@ the other collectives move fewer bytes per tile.
 Constants are calibrated on GB300 measurements of this library (the GEMM and
 the all-reduce of the concurrent path, each timed alone on 8 to 152 CTAs);
 they can be replaced by the caller.
+
+The GEMM tile is ranked together with the split (PR #544 review excerpt of
+predict_split: tile candidates, a preferred tile and a margin): each tile
+kind of this library -- 256 x 256 tiles on CTA pairs with the six- or the
+three-stage pipeline, or 128 x 256 tiles on one CTA -- has its own measured
+per-CTA rate and its own cost for lending the pipeline stages to a
+collective tile, and a tile other than the preferred one ranks above it only
+when its predicted makespan is shorter by more than the margin.
 """
 from __future__ import annotations
 
@@ -25,11 +33,36 @@ from typing import Dict, List, Optional, Sequence
 @dataclasses.dataclass
 class Machine:
     sms: int = 152
-    gemm_tflops_per_sm: float = 11.9      # CTA-pair GEMM 8192^3 bf16 at 1.81 PFLOP/s over 152 SMs
-    comm_gbs_per_sm: float = 65.0         # one CTA's collective engine (all-reduce, linear up to ~96 CTAs)
-    hbm_gbs: float = 6779.4               # measured copy bandwidth
+    gemm_tflops_per_sm: float = 11.3      # CTA-pair GEMM 8192^3 bf16 (six-stage pipeline) over 152 SMs
+    comm_gbs_per_sm: float = 61.0         # one CTA's collective engine, reads + writes (all-reduce on 38 CTAs)
+    hbm_gbs: float = 5500.0               # reads + writes the all-reduce reaches alone on every SM
     gemm_hbm_share: float = 0.12          # HBM fraction the GEMM operands use when all SMs run it
     tile_overhead_us: float = 1.0         # claim + pipeline fill per tile
+
+
+@dataclasses.dataclass
+class TileKind:
+    """One GEMM tile / pipeline of the kernel, with its measured rate."""
+    name: str
+    tile_m: int                  # rows of one tile
+    tile_n: int
+    ctas: int                    # CTAs that compute one tile together (2 = a CTA pair)
+    gemm_tflops_per_cta: float   # GEMM rate per CTA with every SM on the GEMM
+    lease_us: float              # pipeline drain before a collective tile borrows the stages
+    config: Dict[str, int]       # the iris_b200_config fields that select it
+
+
+# Per-CTA rates measured on GB300 (bf16 8192^3 GEMM alone on 152 SMs:
+# 0.640 ms six-stage pairs, 0.607 ms three-stage pairs, 0.694 ms one CTA per
+# tile).  The lease cost is the pipeline's drain: the stages' bytes (192 KB
+# either way) consumed at the tile's rate, about a third longer for the
+# three-stage pipeline's deeper stages.
+TILE_KINDS = (
+    TileKind("pair6", 256, 256, 2, 11.30, 1.0, {"tile_m": 256, "stages": 6}),
+    TileKind("pair3", 256, 256, 2, 11.91, 1.33, {"tile_m": 256, "stages": 3}),
+    TileKind("cta128", 128, 256, 1, 10.43, 1.0, {"tile_m": 128}),
+)
+PREFERRED_TILE = "pair6"   # the library's default beside a collective
 
 
 @dataclasses.dataclass
@@ -80,24 +113,40 @@ def comm_floor(coll: str, base: int = 8, sms: int = 152) -> int:
     return 1
 
 
-def simulate(wl: Workload, gemm_ctas: int, m: Optional[Machine] = None) -> float:
+def simulate(wl: Workload, gemm_ctas: int, m: Optional[Machine] = None, tile: Optional[TileKind] = None) -> float:
     """Makespan (microseconds) of one launch with `gemm_ctas` CTAs preferring
-    the GEMM queue and the rest the comm queue, both spilling when dry."""
+    the GEMM queue and the rest the comm queue, both spilling when dry.
+
+    Without `tile`, every CTA is a worker with the workload's tile at the
+    machine's per-SM rate.  With a TileKind, the workers are its units (a CTA
+    pair computes one tile and runs each collective tile on both CTAs), a
+    unit prefers the GEMM when its first CTA is below gemm_ctas, and a unit
+    that turns from GEMM to collective work first drains its pipeline."""
     m = m or Machine()
-    grid = m.sms
-    gemm_ctas = max(0, min(grid, gemm_ctas))
-    n_g, n_c = wl.gemm_tiles(), wl.comm_tiles()
-    t_gemm = wl.gemm_tile_flops() / (m.gemm_tflops_per_sm * 1e12) * 1e6 + m.tile_overhead_us
+    ctas = tile.ctas if tile else 1
+    units = max(1, m.sms // ctas)
+    gemm_ctas = max(0, min(m.sms, gemm_ctas))
+    if tile:
+        tiles = math.ceil(wl.M / tile.tile_m) * math.ceil(wl.N / tile.tile_n) if wl.M and wl.N else 0
+        t_gemm = 2.0 * tile.tile_m * tile.tile_n * wl.K / (tile.gemm_tflops_per_cta * ctas * 1e12) * 1e6
+        lease = tile.lease_us
+    else:
+        tiles = wl.gemm_tiles() if wl.M and wl.N else 0
+        t_gemm = wl.gemm_tile_flops() / (m.gemm_tflops_per_sm * 1e12) * 1e6
+        lease = 0.0
+    t_gemm += m.tile_overhead_us
+    n_g, n_c = tiles, wl.comm_tiles()
     bytes_c = wl.comm_tile_bytes()
-    # event queue of (time free, cta); greedy claims in time order
-    free = [(0.0, c) for c in range(grid)]
+    # event queue of (time free, unit); greedy claims in time order
+    free = [(0.0, u) for u in range(units)]
     heapq.heapify(free)
+    last_gemm = [False] * units
     g_next = c_next = 0
     active_comm: List[float] = []   # end times of collective tiles in flight
     end = 0.0
     while g_next < n_g or c_next < n_c:
-        t, cta = heapq.heappop(free)
-        prefer_gemm = cta < gemm_ctas
+        t, u = heapq.heappop(free)
+        prefer_gemm = u * ctas < gemm_ctas
         take_gemm = (prefer_gemm and g_next < n_g) or (not prefer_gemm and c_next >= n_c)
         if take_gemm:
             g_next += 1
@@ -106,20 +155,29 @@ def simulate(wl: Workload, gemm_ctas: int, m: Optional[Machine] = None) -> float
             c_next += 1
             active_comm = [x for x in active_comm if x > t]
             running = len(active_comm) + 1
-            gemm_running = min(gemm_ctas, grid - running) if g_next < n_g else 0
-            hbm_left = m.hbm_gbs * (1.0 - m.gemm_hbm_share * gemm_running / grid)
-            bw = min(m.comm_gbs_per_sm, hbm_left / running)
-            done = t + bytes_c / (bw * 1e9) * 1e6 + m.tile_overhead_us
+            gemm_running = min(gemm_ctas // ctas, units - running) if g_next < n_g else 0
+            hbm_left = m.hbm_gbs * (1.0 - m.gemm_hbm_share * gemm_running / units)
+            bw = min(m.comm_gbs_per_sm * ctas, hbm_left / running)
+            done = t + bytes_c / (bw * 1e9) * 1e6 + m.tile_overhead_us + (lease if last_gemm[u] else 0.0)
             active_comm.append(done)
+        last_gemm[u] = take_gemm
         end = max(end, done)
-        heapq.heappush(free, (done, cta))
+        heapq.heappush(free, (done, u))
     return end
 
 
 def predict_split(wl: Workload, candidates: Optional[Sequence[int]] = None, m: Optional[Machine] = None,
-                  top_k: int = 4) -> List[Dict[str, float]]:
+                  top_k: int = 4, tiles: Optional[Sequence[TileKind]] = None, prefer: str = PREFERRED_TILE,
+                  margin: float = 0.20) -> List[Dict[str, object]]:
     """Rank GEMM/comm CTA splits by simulated makespan; the collective keeps
-    at least comm_floor() CTAs.  Returns the top_k as dicts."""
+    at least comm_floor() CTAs.  Returns the top_k as dicts with "gemm_ctas"
+    and "us".
+
+    With `tiles`, each (tile kind, split) pair is simulated and ranked
+    jointly; a tile other than `prefer` counts as if its makespan were
+    1 / (1 - margin) times longer, so it wins only when it is faster by more
+    than the margin.  Those dicts also hold "tile" (the kind's name), "key"
+    (the ranking value) and "config" (the iris_b200_config fields)."""
     m = m or Machine()
     floor = comm_floor(wl.coll, sms=m.sms)
     if candidates is None:
@@ -129,8 +187,15 @@ def predict_split(wl: Workload, candidates: Optional[Sequence[int]] = None, m: O
     for g in candidates:
         if wl.comm_tiles() > 0 and m.sms - g < floor:
             continue
-        ranked.append({"gemm_ctas": int(g), "us": simulate(wl, g, m)})
-    ranked.sort(key=lambda d: d["us"])
+        if tiles is None:
+            ranked.append({"gemm_ctas": int(g), "us": simulate(wl, g, m)})
+            continue
+        for tk in tiles:
+            us = simulate(wl, g, m, tk)
+            key = us if tk.name == prefer else us / (1.0 - margin)
+            ranked.append({"gemm_ctas": int(g), "us": us, "tile": tk.name, "key": key,
+                           "config": {**tk.config, "gemm_ctas": int(g)}})
+    ranked.sort(key=lambda d: d.get("key", d["us"]))
     return ranked[:max(1, top_k)]
 
 

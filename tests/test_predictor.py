@@ -50,8 +50,9 @@ def test_best_split_beats_sequential_and_respects_the_floor():
 
 
 def test_calibration_close_to_measurements():
-    """GB300 measurements of this library: GEMM 8192^3 alone 0.69-0.70 ms,
-    all-reduce 8 x 64Mi fp32 alone 0.72-0.75 ms."""
+    """GB300 measurements of this library: GEMM 8192^3 alone 0.61-0.70 ms
+    (three- and six-stage pair pipelines), all-reduce 8 x 64Mi fp32 alone
+    0.76-0.78 ms."""
     wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
     g = P.simulate(P.Workload(M=8192, N=8192, K=8192, count=0), 152)
     c = P.simulate(P.Workload(M=0, N=0, K=0, coll="all_reduce", W=8, count=64 * 1024 * 1024), 0)
@@ -65,3 +66,34 @@ def test_tuning_candidates_use_the_predictor():
                           count=64 * 1024 * 1024)
     assert c[0] == {}
     assert sum("gemm_ctas" in x for x in c) >= 3
+
+
+def test_joint_tile_ranking_and_margin_rule():
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    r = P.predict_split(wl, top_k=100, tiles=P.TILE_KINDS)
+    assert {d["tile"] for d in r} == {t.name for t in P.TILE_KINDS}
+    assert r == sorted(r, key=lambda d: d["key"])
+    for d in r:
+        tk = next(t for t in P.TILE_KINDS if t.name == d["tile"])
+        assert d["key"] == pytest.approx(d["us"] if tk.name == P.PREFERRED_TILE else d["us"] / 0.8)
+        assert d["config"]["gemm_ctas"] == d["gemm_ctas"] and d["config"]["tile_m"] == tk.tile_m
+    # a tile that is faster by less than the margin does not displace the
+    # preferred one; faster by more than the margin, it does
+    pref = next(t for t in P.TILE_KINDS if t.name == P.PREFERRED_TILE)
+    a_bit = P.TileKind("fast10", 256, 256, 2, pref.gemm_tflops_per_cta * 1.1, pref.lease_us, {"tile_m": 256})
+    wl_g = P.Workload(M=8192, N=8192, K=8192, count=0)
+    best = P.predict_split(wl_g, candidates=[152], tiles=[pref, a_bit], top_k=1)[0]
+    assert best["tile"] == P.PREFERRED_TILE
+    much = P.TileKind("fast50", 256, 256, 2, pref.gemm_tflops_per_cta * 1.5, pref.lease_us, {"tile_m": 256})
+    best = P.predict_split(wl_g, candidates=[152], tiles=[pref, much], top_k=1)[0]
+    assert best["tile"] == "fast50"
+
+
+def test_pair_tile_simulation_matches_closed_form():
+    """A CTA pair computes one 256 x 256 tile at twice the per-CTA rate; with
+    no collective the makespan is the number of waves of pair tiles."""
+    m = P.Machine(sms=20, tile_overhead_us=0.0)
+    tk = P.TileKind("p", 256, 256, 2, 10.0, 0.0, {})
+    wl = P.Workload(M=256 * 4, N=256 * 7, K=2048, count=0)                  # 28 tiles on 10 pairs
+    t_tile = 2 * 256 * 256 * 2048 / (10.0 * 2 * 1e12) * 1e6
+    assert P.simulate(wl, 20, m, tk) == pytest.approx(3 * t_tile)

@@ -78,3 +78,67 @@ def test_all_tuned_knobs_exist_in_the_config_struct():
     from gemm_collective_tiles_gb300 import _native
     names = {f[0] for f in _native.iris_b200_config._fields_}
     assert set(tuning.TUNABLE) <= names
+
+
+def test_concurrent_key_names_the_collective_and_its_size():
+    k1 = tuning.shape_key("concurrent", 8, 8192, 8192, 8192, "bf16", "all_reduce", 64 << 20, "f32")
+    k2 = tuning.shape_key("concurrent", 8, 8192, 8192, 8192, "bf16", "all_gather", 1 << 20, "f32")
+    k3 = tuning.shape_key("concurrent", 8, 8192, 8192, 8192, "bf16", "all_reduce", 1 << 20, "f32")
+    assert k1 == "concurrent|W8|8192x8192x8192|bf16|all_reduce|count67108864|f32"
+    assert len({k1, k2, k3}) == 3
+    # the fused ops' keys are unchanged
+    assert tuning.shape_key("all_gather_matmul", 8, 4096, 14336, 4096, "bf16") == \
+        "all_gather_matmul|W8|4096x14336x4096|bf16"
+
+
+def _rec(path, op, M, N, K, cfg, ms, dms, W=8, dtype="bf16", **kw):
+    shape = tuning.shape_info(op, W, M, N, K, dtype, **kw)
+    key = tuning.shape_key(op, W, M, N, K, dtype, **kw)
+    assert tuning.record("a", key, cfg, ms, dms, path, shape)
+
+
+def test_nearest_shape_exact_nearest_and_none(tmp_path):
+    path = str(tmp_path / "t.json")
+    _rec(path, "all_gather_matmul", 4096, 14336, 4096, {"group_m": 16}, 1.0, 1.2)   # beat its default
+    _rec(path, "all_gather_matmul", 8192, 8192, 8192, {"group_m": 64}, 2.0, 2.0)    # default won: no info
+    _rec(path, "all_gather_matmul", 65536, 16384, 16384, {"stages": 6}, 30.0, 31.0)
+
+    def sel(M, N, K, W=8, dtype="bf16", op="all_gather_matmul"):
+        return tuning.select("a", tuning.shape_key(op, W, M, N, K, dtype), path=path,
+                             shape=tuning.shape_info(op, W, M, N, K, dtype))
+
+    assert sel(4096, 14336, 4096) == {"group_m": 16}                # exact
+    assert sel(4096, 11008, 4096) == {"group_m": 16}                # 0.38 log2 away
+    assert sel(131072, 16384, 16384) == {"stages": 6}               # one size x2
+    assert sel(8192, 8192, 8192) == {"group_m": 64}                 # exact match is not filtered
+    assert sel(8192, 8192, 16384) == {}                             # nearest lost to its default
+    assert sel(1024, 1024, 1024) == {}                              # nothing close
+    assert sel(4096, 14336, 4096, W=4) == {}                        # other world size
+    assert sel(4096, 14336, 4096, dtype="f16") == {}                # other dtype
+    assert sel(4096, 14336, 4096, op="matmul_all_gather") == {}     # other op
+    # explicit wins over everything
+    assert tuning.select("a", "x", {"tile_n": 128}, path, tuning.shape_info("all_gather_matmul", 8, 4096,
+                                                                            14336, 4096, "bf16")) == {"tile_n": 128}
+
+
+def test_nearest_shape_concurrent_needs_the_same_collective(tmp_path):
+    path = str(tmp_path / "t.json")
+    _rec(path, "concurrent", 8192, 8192, 8192, {"gemm_ctas": 90}, 1.0, 1.1, coll="all_reduce", count=64 << 20,
+         coll_dtype="f32")
+    info = tuning.shape_info("concurrent", 8, 8192, 8192, 8192, "bf16", "all_reduce", 48 << 20, "f32")
+    assert tuning.lookup_nearest("a", info, path) == {"gemm_ctas": 90}
+    info = tuning.shape_info("concurrent", 8, 8192, 8192, 8192, "bf16", "all_gather", 64 << 20, "f32")
+    assert tuning.lookup_nearest("a", info, path) is None
+    assert tuning.shape_distance(tuning.shape_info("concurrent", 8, 1, 1, 1, "bf16", "all_reduce", 4, "f32"),
+                                 tuning.shape_info("concurrent", 8, 2, 1, 1, "bf16", "all_reduce", 8, "f32")) == \
+        pytest.approx(2 ** 0.5)
+
+
+def test_concurrent_candidates_rank_tiles_and_splits():
+    c = tuning.concurrent_candidates(8192, 8192, 8192, "all_reduce", 8, 64 << 20, 152, top_k=6)
+    assert c[0] == {} and len(c) == 6
+    assert all("gemm_ctas" in x and "tile_m" in x for x in c[1:])
+    assert len({json.dumps(x, sort_keys=True) for x in c}) == len(c)
+    # the fused-op candidate helper hands the concurrent mode to it
+    assert tuning.candidates("concurrent", 8, 8192, 8192, 8192, 152, top_k=6, coll="all_reduce",
+                             count=64 << 20) == c
