@@ -67,6 +67,9 @@ class iris_b200_config(ctypes.Structure):
         ("reduce_mode", ctypes.c_int),
         ("root", ctypes.c_int),
         ("rank_inner", ctypes.c_int),
+        ("coll_ring", ctypes.c_int),
+        ("coll_l2_hint", ctypes.c_int),
+        ("coll_path", ctypes.c_int),
     ]
 
 

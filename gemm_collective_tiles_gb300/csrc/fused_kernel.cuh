@@ -105,6 +105,8 @@ struct Params {
                       // (one load per stage fills a CTA's B columns; set when N % 64 == 0)
     CUtensorMap tmAc; // A as 64-column K chunks: 4-D {64, row, k / 64, rank}, box {64, 128, KS, 1}
                       // (CTA pairs: one load per stage; set when K % 64 == 0)
+    CUtensorMap tmX;  // concurrent all-reduce / reduce-scatter input (coll_path 3): 3-D fp32
+                      // {256, count / 256, W} (1 KB rows; regions rank_stride apart), box {256, R, W}
     int b_chunked;    // tmBc is valid
     int a_chunked;    // tmAc is valid
     int op, W, bf16, coll;
@@ -134,6 +136,11 @@ struct Params {
     unsigned long long wait_ns;
     uint32_t debug_skip;               // flag index + 1 that is never released (0 = none)
     int reduce_mode;                   // reduce ops: 1 = comm queue, 2 = distributed parts, 3 = chained
+    int coll_ring;                     // concurrent collectives: buffers per worker warp (2..4)
+    int coll_evict_first;              // concurrent collectives: bulk copies with an L2 evict-first policy
+    int coll_path;                     // concurrent collectives: 1 TMA, 2 TMA loads + register stores,
+                                       // 3 one 3-D TMA box per sub-chunk for all W sources
+    int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
     int rank_inner;                    // reduce ops: 1 = rank index fastest in the GEMM item order
     unsigned long long* trace;         // optional per-CTA event trace (nullptr = off)
     int trace_cap;                     // events per (CTA, role)
@@ -143,7 +150,10 @@ struct Params {
 // workers) of trace_cap (event, globaltimer ns) pairs; slot 0 of a stream
 // holds its event count.
 enum : int { TR_SCHED = 0, TR_MMA = 1, TR_TMA = 2, TR_WORK = 3 };
-enum : unsigned long long { EV_CLAIM = 1, EV_BEGIN = 2, EV_END = 3, EV_READY = 4 };
+// EV_KERNEL_BEGIN / EV_KERNEL_END (scheduler stream, thread 0 of every CTA):
+// entry into the kernel and the end of its teardown
+enum : unsigned long long { EV_CLAIM = 1, EV_BEGIN = 2, EV_END = 3, EV_READY = 4, EV_KERNEL_BEGIN = 5,
+                            EV_KERNEL_END = 6 };
 struct Tracer {
     unsigned long long* buf = nullptr;
     int cap = 0, n = 0;
@@ -384,6 +394,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
 // ============================================================ shared state
 // CG = 2: the CTA pair computes a (2 BM) x BN tile; this CTA holds BM rows of
 // A and BN / 2 columns of B per stage.
+constexpr int SBARS = 4;  // per worker warp: running-sum loads (2) or collective buffers (1 to 4)
+constexpr int MAX_COLL_RING = SBARS;
+
 template <int BN, int STAGES, int CG>
 struct Smem {
     static constexpr int KS = k_per_stage(CG, STAGES);  // K blocks per stage
@@ -392,7 +405,7 @@ struct Smem {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + 2 * NUM_WORKER_WARPS + 2;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + SBARS * NUM_WORKER_WARPS + 2;
     static constexpr int READY_BITS = 4096;  // all_gather_matmul: m-blocks whose gathers this CTA has seen complete
     static constexpr uint32_t BYTES = 1024 /*align slack*/ + TILES_BYTES +
                                       NUM_WORKER_WARPS * STAGE_OUT_BYTES + NUM_BARS * 8 + (RING + 4) * 4 +
@@ -400,7 +413,7 @@ struct Smem {
     uint8_t* tiles;
     uint8_t* stage_out;
     uint64_t *full, *empty, *acc_full, *acc_empty, *item_full, *item_empty, *wbar, *final_bar;
-    uint64_t* sbar;  // per worker warp: 2 barriers for running-sum / collective chunk loads
+    uint64_t* sbar;  // per worker warp: SBARS barriers for running-sum / collective chunk loads
     uint64_t* lease;       // TMA producer -> workers: pipeline stages lent for a collective tile
     uint64_t* lease_done;  // workers -> TMA producer: stages returned
     volatile uint32_t* ring;
@@ -423,7 +436,7 @@ struct Smem {
         wbar = item_empty + RING;
         final_bar = wbar + 1;
         sbar = final_bar + 1;
-        lease = sbar + 2 * NUM_WORKER_WARPS;
+        lease = sbar + SBARS * NUM_WORKER_WARPS;
         lease_done = lease + 1;
         uint32_t* u = reinterpret_cast<uint32_t*>(lease_done + 1);
         ring = u;
@@ -443,9 +456,7 @@ struct Smem {
 // every CTA is a topological order of the dependency graph and no CTA can wait
 // on work that nobody will run.
 template <int BN, int STAGES, int CG>
-__device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm) {
-    Tracer tr;
-    tr.init(p, TR_SCHED);
+__device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, Tracer& tr) {
     uint32_t ring_n = 0;
     bool gemm_dry = (p.n_gemm == 0), comm_dry = (p.n_comm == 0);
     const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
@@ -590,7 +601,6 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         }
     }
     if (ok) publish(ITEM_END);
-    tr.finish();
 }
 
 // A consumer is done with ring slot `slot` (CTA pairs: the even CTA's
@@ -1267,7 +1277,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     }
     const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
     uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
-    uint64_t* lbar = sm.sbar + 2 * wc.w;
+    uint64_t* lbar = sm.sbar + SBARS * wc.w;
     auto issue_load = [&](int ci) {
         // the staging half must be free: earlier stores have read it
         bulk_wait_read_all();
@@ -1526,25 +1536,19 @@ __device__ __noinline__ void reduce_body(const Params& p, uint32_t c, WorkerCtx&
     }
 }
 
-// Concurrent-mode collective tile through the TMA engine, run while the TMA
-// producer lends the CTA's pipeline stages (STAGES x STAGE_BYTES bytes of
-// shared memory) to the workers.  Worker warp w owns 1/4 of that space as two
-// buffers; for each sub-chunk of its slice of tile c it bulk-loads the sources
-// (all W ranks for all-reduce / reduce-scatter, rank s for all-gather) into one
-// buffer while the other is summed in rank order (fp32) and bulk-stored to the
-// destinations.  Bytes in flight per SM: about half the stage area.
-template <int BN, int STAGES, int CG>
-__device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c, WorkerCtx& wc) {
-    constexpr uint32_t AREA = STAGES * Smem<BN, STAGES, CG>::STAGE_BYTES / NUM_WORKER_WARPS;
-    constexpr uint32_t HALF = AREA / 2;
-    uint8_t* area = sm.tiles + wc.w * AREA;
-    uint64_t* bar = sm.sbar + 2 * wc.w;
+// Concurrent-mode collective item c: bytes [b0, b1) of a source range.
+// Sources: src_n regions starting at src_lo, at src_base + (b - b0).
+// Destinations: every region (dst_all), the owning rank's slice
+// (reduce-scatter), or region dst_region, at dst_base + (b - b0).
+struct CollRange {
+    size_t b0, b1, src_base, dst_base;
+    int src_lo, src_n, dst_region;
+    bool dst_all;
+};
+__device__ __forceinline__ CollRange coll_range(const Params& p, uint32_t c) {
     const size_t esz = static_cast<size_t>(p.elem_bytes);
     const size_t bytes_per_rank = static_cast<size_t>(p.count) * esz;
     const size_t chunk = static_cast<size_t>(p.comm_block) * esz;
-    // Item c covers bytes [b0, b1) of a source range.  Sources: src_n regions
-    // starting at src_lo, at src_base + (b - b0).  Destinations: every region
-    // (dst_all), the owning rank's slice (reduce-scatter), or one region.
     size_t b0, b1, src_base, dst_base;
     int src_lo, src_n, dst_region = -1;
     bool dst_all = false;
@@ -1588,36 +1592,140 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         dst_base = p.off_cout + b0;
         dst_all = (p.coll == COLL_AR);
     }
+    CollRange r;
+    r.b0 = b0;
+    r.b1 = b1;
+    r.src_base = src_base;
+    r.dst_base = dst_base;
+    r.src_lo = src_lo;
+    r.src_n = src_n;
+    r.dst_region = dst_region;
+    r.dst_all = dst_all;
+    return r;
+}
+
+// Concurrent-mode collective tile through the TMA engine, run while the TMA
+// producer lends the CTA's pipeline stages (STAGES x STAGE_BYTES bytes of
+// shared memory) to the workers.  Worker warp w owns 1/4 of that space as a
+// ring of p.coll_ring buffers; for each sub-chunk of its slice of tile c it
+// bulk-loads the sources (all W ranks for all-reduce / reduce-scatter, rank s
+// for all-gather) into the next buffer while earlier ones are summed in rank
+// order (fp32) and bulk-stored to the destinations.  While a warp waits for
+// a sub-chunk, up to coll_ring loads are in flight.  With p.coll_evict_first the copies carry an L2
+// evict-first policy, so the streamed collective data does not push the
+// concurrent GEMM's operands out of the L2.
+template <int BN, int STAGES, int CG>
+__device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c, WorkerCtx& wc) {
+    constexpr uint32_t AREA = STAGES * Smem<BN, STAGES, CG>::STAGE_BYTES / NUM_WORKER_WARPS;
+    const int nb = p.coll_ring;
+    const uint32_t BUF = (AREA / static_cast<uint32_t>(nb)) & ~15u;
+    uint8_t* area = sm.tiles + wc.w * AREA;
+    uint64_t* bar = sm.sbar + SBARS * wc.w;
+    const CollRange cr = coll_range(p, c);
+    const size_t b0 = cr.b0, b1 = cr.b1, src_base = cr.src_base, dst_base = cr.dst_base;
+    const int src_lo = cr.src_lo, src_n = cr.src_n, dst_region = cr.dst_region;
+    const bool dst_all = cr.dst_all;
     // the warp's contiguous slice (16-byte granules) of [b0, b1), as offsets
     // from b0; a CTA pair runs the item together, one slice per worker warp
     // of either CTA
-    const size_t g_tot = (b1 - b0) / 16;
+    // coll_path 3 loads whole 1 KB rows of all W sources with one box: the
+    // slice and the sub-chunks are then counted in rows
+    const bool box = p.coll_path == 3;
+    const size_t gran = box ? 1024 : 16;
+    const size_t g_tot = (b1 - b0) / gran;
     const size_t ww = static_cast<size_t>(ctl.half * NUM_WORKER_WARPS + wc.w), nww = CG * NUM_WORKER_WARPS;
     const size_t g_lo = g_tot * ww / nww, g_hi = g_tot * (ww + 1) / nww;
-    const uint32_t sub = (HALF / src_n) & ~15u;  // bytes per source per sub-chunk
-    const size_t s_lo = g_lo * 16, s_hi = g_hi * 16;
+    const uint32_t sub = box ? static_cast<uint32_t>(p.coll_box_rows) * 1024u
+                             : (BUF / src_n) & ~15u;  // bytes per source per sub-chunk
+    const size_t s_lo = g_lo * gran, s_hi = g_hi * gran;
     const int nsub = static_cast<int>((s_hi - s_lo + sub - 1) / sub);
     const size_t cw_bytes = static_cast<size_t>(p.count / p.W) * 4;  // reduce-scatter slice per rank
+    const bool hint = p.coll_evict_first != 0;
+    const uint64_t pol = hint ? l2_policy_evict_first() : 0ull;
+    auto store = [&](void* g, const void* s, uint32_t n) {
+        if (hint) bulk_store_hint(g, s, n, pol);
+        else bulk_store(g, s, n);
+    };
+    // load sub-chunk i into buffer i % nb (whose earlier store has read it)
     auto issue = [&](int i) {
         const size_t o = s_lo + static_cast<size_t>(i) * sub;
         const uint32_t n = static_cast<uint32_t>(min(static_cast<size_t>(sub), s_hi - o));
-        uint8_t* buf = area + (i & 1) * HALF;
-        bulk_wait_read_all();  // earlier stores have read this buffer
-        mbar_arrive_expect_tx(&bar[i & 1], n * src_n);
-        for (int r = 0; r < src_n; ++r)
-            bulk_load(buf + r * sub, p.heap + static_cast<size_t>(src_lo + r) * p.rank_stride + src_base + o, n,
-                      &bar[i & 1]);
+        uint8_t* buf = area + (i % nb) * BUF;
+        if (box) {
+            // rows [(b0 + o) / 1 KB, + R) of every region in one box (rows
+            // past the tensor read as zeros; rows past this warp's slice
+            // are loaded but not used)
+            mbar_arrive_expect_tx(&bar[i % nb], sub * src_n);
+            if (hint) tma_load_3d_hint(buf, &p.tmX, 0, static_cast<int>((b0 + o) / 1024), 0, &bar[i % nb], pol);
+            else tma_load_3d(buf, &p.tmX, 0, static_cast<int>((b0 + o) / 1024), 0, &bar[i % nb]);
+            return;
+        }
+        mbar_arrive_expect_tx(&bar[i % nb], n * src_n);
+        for (int r = 0; r < src_n; ++r) {
+            const char* src = p.heap + static_cast<size_t>(src_lo + r) * p.rank_stride + src_base + o;
+            if (hint) bulk_load_hint(buf + r * sub, src, n, &bar[i % nb], pol);
+            else bulk_load(buf + r * sub, src, n, &bar[i % nb]);
+        }
     };
-    if (nsub > 0 && wc.lane == 0) issue(0);
-    for (int i = 0; i < nsub; ++i) {
-        if (i + 1 < nsub && wc.lane == 0) issue(i + 1);
-        int ok = 1;
-        if (wc.lane == 0) ok = wait_bar(ctl, &bar[i & 1], (wc.sphase >> (i & 1)) & 1u, WAIT_COLL_LOAD) ? 1 : 0;
-        wc.sphase ^= 1u << (i & 1);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+    int issued = 0;  // lane 0: sub-chunks whose loads were issued
+    if (wc.lane == 0)
+        for (; issued < min(nb - 1, nsub); ++issued) issue(issued);
+    int i = 0;
+    bool ok = true;
+    for (; i < nsub; ++i) {
+        int got = 1;
+        if (wc.lane == 0) {
+            // keep nb loads in flight: the next one goes into the buffer of
+            // sub-chunk i - 1, whose store (the newest group) must have read it
+            if (issued < nsub) {
+                bulk_wait_read_all();
+                issue(issued);
+                ++issued;
+            }
+            got = wait_bar(ctl, &bar[i % nb], (wc.sphase >> (i % nb)) & 1u, WAIT_COLL_LOAD) ? 1 : 0;
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+            ok = false;
+            break;
+        }
+        wc.sphase ^= 1u << (i % nb);
         const size_t o = s_lo + static_cast<size_t>(i) * sub;
         const uint32_t n = static_cast<uint32_t>(min(static_cast<size_t>(sub), s_hi - o));
-        uint8_t* buf = area + (i & 1) * HALF;
+        uint8_t* buf = area + (i % nb) * BUF;
+        if (p.coll_path == 2) {
+            // every lane stores its 16-byte granules straight from registers
+            // (consecutive lanes, consecutive granules: 512 B per warp store)
+            for (uint32_t q = wc.lane; q < n / 16; q += 32) {
+                uint4 v = *reinterpret_cast<const uint4*>(buf + q * 16);
+                if (src_n > 1) {
+                    // rank-order fp32 sum
+                    float4 a = *reinterpret_cast<const float4*>(&v);
+                    for (int r = 1; r < src_n; ++r) {
+                        const float4 u = *reinterpret_cast<const float4*>(buf + r * sub + q * 16);
+                        a.x = a.x + u.x;
+                        a.y = a.y + u.y;
+                        a.z = a.z + u.z;
+                        a.w = a.w + u.w;
+                    }
+                    v = *reinterpret_cast<const uint4*>(&a);
+                }
+                const size_t og = o + static_cast<size_t>(q) * 16;  // byte offset from the item start
+                if (p.coll == COLL_RS) {
+                    const size_t e = b0 + og;
+                    const int rr = static_cast<int>(e / cw_bytes);
+                    *reinterpret_cast<uint4*>(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout +
+                                              (e - rr * cw_bytes)) = v;
+                } else if (dst_all) {
+                    for (int r = 0; r < p.W; ++r)
+                        *reinterpret_cast<uint4*>(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + og) = v;
+                } else {
+                    *reinterpret_cast<uint4*>(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base +
+                                              og) = v;
+                }
+            }
+            __syncwarp();  // the buffer is free for the next load once every lane has read it
+            continue;
+        }
         if (src_n > 1) {
             // rank-order fp32 sum into the rank-0 slot
             for (uint32_t q = wc.lane; q < n / 16; q += 32) {
@@ -1642,23 +1750,31 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
                     const size_t e = b0 + o + done;  // byte index into the summed vector
                     const int rr = static_cast<int>(e / cw_bytes);
                     const size_t piece = min(static_cast<size_t>(n) - done, (rr + 1) * cw_bytes - e);
-                    bulk_store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
-                               buf + done, static_cast<uint32_t>(piece));
+                    store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
+                          buf + done, static_cast<uint32_t>(piece));
                     done += piece;
                 }
             } else if (dst_all) {
-                for (int r = 0; r < p.W; ++r)
-                    bulk_store(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + o, buf, n);
+                for (int r = 0; r < p.W; ++r) store(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + o, buf, n);
             } else {
-                bulk_store(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base + o, buf, n);
+                store(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base + o, buf, n);
             }
             bulk_commit();
+        }
+        __syncwarp();
+    }
+    if (!ok && wc.lane == 0) {
+        // stopped early: the loads still in flight land in the leased stages,
+        // so wait (bounded) for each before the stages can be returned
+        for (int j = i; j < issued; ++j) {
+            drain_bar(ctl, &bar[j % nb], (wc.sphase >> (j % nb)) & 1u, WAIT_COLL_LOAD);
+            wc.sphase ^= 1u << (j % nb);
         }
     }
     // the stages go back to the TMA producer once every store has read them
     if (wc.lane == 0) bulk_wait_read_all();
     __syncwarp();
-    return true;
+    return ok;
 }
 
 template <int BN, int STAGES, int CG>
@@ -1759,6 +1875,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
     // MMAs for both; each CTA loads its halves of A and B and drains its own
     // half of the accumulator
     const int half = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+    Tracer ktr;  // thread 0: the scheduler stream (kernel entry, claims, teardown end)
+    if (threadIdx.x == 0) {
+        ktr.init(p, TR_SCHED);
+        ktr.rec(EV_KERNEL_BEGIN, blockIdx.x);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -1776,7 +1897,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         }
         mbar_init(sm.wbar, NUM_WORKER_WARPS);
         mbar_init(sm.final_bar, 1);
-        for (int i = 0; i < 2 * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
+        for (int i = 0; i < SBARS * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
         mbar_init(sm.lease, 1);
         mbar_init(sm.lease_done, NUM_WORKER_WARPS);
         for (int i = 0; i < Smem<BN, STAGES, CG>::READY_BITS / 32; ++i) sm.ready_bits[i] = 0u;
@@ -1791,6 +1912,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
             if (p.a_chunked) tma_prefetch_desc(&p.tmAc);
         }
         if (p.n_gemm > 0) tma_prefetch_desc(&p.tmC);
+        if (p.n_comm > 0 && p.coll_path == 3) tma_prefetch_desc(&p.tmX);
         if (p.n_gemm > 0 && p.reduce_mode == 3) tma_prefetch_desc(&p.tmS);
     }
     if (warp == 1) tmem_alloc<TMEM_COLS, CG>(sm.tmem_slot);
@@ -1803,7 +1925,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
     const Ctl ctl{p.ws, *sm.epoch_slot, p.wait_ns, half};
 
     if (warp == 0) {
-        if (lane == 0 && half == 0) run_scheduler<BN, STAGES, CG>(p, ctl, sm);
+        if (lane == 0 && half == 0) run_scheduler<BN, STAGES, CG>(p, ctl, sm, ktr);
         __syncwarp();
     } else if (warp == 2) {
         if (lane == 0) run_tma<BN, STAGES, CG>(p, ctl, sm);
@@ -1837,6 +1959,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
             __threadfence();
             atomicExch(&p.ws->epoch, ctl.epoch);
         }
+        ktr.rec(EV_KERNEL_END, blockIdx.x);
+        ktr.finish();
     }
 }
 

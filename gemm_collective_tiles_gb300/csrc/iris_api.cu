@@ -73,6 +73,13 @@ constexpr size_t smem_bytes() {
     return Smem<BN, STAGES, CG>::BYTES;
 }
 
+// Every kernel variant lends the same pipeline bytes to a collective tile.
+constexpr uint32_t LEASE_BYTES = Smem<BN_WIDE, STAGES_PAIR, 2>::TILES_BYTES;
+static_assert(Smem<BN_WIDE, STAGES_PAIR_STREAM, 2>::TILES_BYTES == LEASE_BYTES &&
+                  Smem<BN_WIDE, STAGES_WIDE, 1>::TILES_BYTES == LEASE_BYTES &&
+                  Smem<BN_NARROW, STAGES_NARROW, 1>::TILES_BYTES == LEASE_BYTES,
+              "collective tiles assume one lease size for every kernel variant");
+
 int g_pair_clusters[64] = {0};  // co-resident CTA pairs of the pair kernel, per device
 
 cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
@@ -156,6 +163,9 @@ struct Cfg {
     int reduce_mode;  // resolved by the reduce ops (resolve_reduce_mode)
     int rank_inner;
     int stages;       // CTA pairs: requested 0 / 3 / 6, resolved by resolve_stages; one-CTA tiles: 0
+    int coll_ring;    // concurrent collectives: buffers per worker warp
+    int coll_evict_first;
+    int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 registers only
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -174,8 +184,10 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->group_m < 0) return IRIS_EINVAL;
     // 32 m-blocks per swizzle group (measured best on the reduce ops, where it
     // also keeps one rank's operands in L2 per group phase and spaces a
-    // tile's W ranks several waves apart, and on all_gather_matmul)
-    out.group_m = c->group_m ? c->group_m : 32;
+    // tile's W ranks several waves apart, and on all_gather_matmul); 16 for
+    // the concurrent mode, whose GEMM shares the L2 with a streaming
+    // collective (8192^3 beside an 8 x 64Mi all-reduce: 1.144 against 1.180 ms)
+    out.group_m = c->group_m ? c->group_m : (op == IRIS_OP_CONCURRENT ? 16 : 32);
     out.comm_block = c->comm_block ? c->comm_block : 65536;
     if (out.comm_block < 0 || out.comm_block % 8 != 0) return IRIS_EINVAL;
     out.replicate = c->replicate_outputs ? 1 : 0;
@@ -200,6 +212,12 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->reduce_mode < 0 || c->reduce_mode > 3) return IRIS_EINVAL;
     out.reduce_mode = c->reduce_mode;
     out.rank_inner = c->rank_inner ? 1 : 0;
+    if (c->coll_ring != 0 && (c->coll_ring < 1 || c->coll_ring > MAX_COLL_RING)) return IRIS_EINVAL;
+    out.coll_ring = c->coll_ring ? c->coll_ring : 2;
+    if (c->coll_l2_hint < 0 || c->coll_l2_hint > 2) return IRIS_EINVAL;
+    out.coll_evict_first = c->coll_l2_hint == 1 ? 1 : 0;
+    if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
+    out.coll_path = c->coll_path;  // 0: chosen per collective (resolve_coll_path)
     return IRIS_OK;
 }
 
@@ -350,6 +368,22 @@ int make_a_chunk_map(Params& p, const Cfg& c, const void* base, int64_t rows, in
     return IRIS_OK;
 }
 
+// Concurrent all-reduce / reduce-scatter input for coll_path 3: 3-D fp32
+// {256, count / 256, W} (1 KB rows, regions rank_stride apart), box {256, R,
+// W}: one load brings R rows of every source.
+int make_coll_map(Params& p, const void* base, int64_t count, int W, uint64_t region_stride, int R) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    cuuint64_t dims[3] = {256, static_cast<cuuint64_t>(count / 256), static_cast<cuuint64_t>(W)};
+    cuuint64_t strides[2] = {1024, region_stride};
+    cuuint32_t box[3] = {256, static_cast<cuuint32_t>(R), static_cast<cuuint32_t>(W)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(&p.tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? IRIS_OK : cuda_fail("cuTensorMapEncodeTiled (collective input)", static_cast<int>(r));
+}
+
 // Output map: 4-D {n, row, row block, region} with a 32 x 32 box, written by
 // the epilogue's TMA stores.  fp32 (partials) use the 128-byte swizzle (one
 // 128-byte staging row), 16-bit outputs the 64-byte swizzle.
@@ -394,6 +428,9 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.trace_cap = c.trace_cap;
     p.reduce_mode = c.reduce_mode;
     p.rank_inner = c.rank_inner;
+    p.coll_ring = c.coll_ring;
+    p.coll_evict_first = c.coll_evict_first;
+    p.coll_path = c.coll_path;
 }
 
 int launch(Params& p, const Cfg& c, cudaStream_t stream) {
@@ -803,6 +840,21 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
                                                               : chunks;
         if (items >= 0x7FFFFFFF) return IRIS_EINVAL;
         p.n_comm = static_cast<uint32_t>(items);
+        // one 3-D box of all W sources per sub-chunk (path 3) applies to the
+        // summing collectives over whole 1 KB rows when R rows of all W
+        // sources fit one ring buffer; measured faster than one copy per
+        // source (fewer, larger TMA requests), so it is their default
+        const int area = static_cast<int>(LEASE_BYTES / NUM_WORKER_WARPS);  // leased bytes per worker warp
+        const int R = area / c.coll_ring / (1024 * W);
+        const bool box_ok = (coll == IRIS_COLL_ALL_REDUCE || coll == IRIS_COLL_REDUCE_SCATTER) && count % 256 == 0 &&
+                            c.comm_block % 256 == 0 && R >= 1;
+        if (c.coll_path == 3 && !box_ok) return IRIS_EINVAL;
+        if (c.coll_path == 0) c.coll_path = box_ok ? 3 : 1;
+        p.coll_path = c.coll_path;
+        if (c.coll_path == 3) {
+            p.coll_box_rows = std::min(R, 256);
+            if ((rc = make_coll_map(p, p.heap + off_in, count, W, heap->rank_stride, p.coll_box_rows))) return rc;
+        }
     }
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_CONCURRENT, 0, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
@@ -883,39 +935,28 @@ int iris_b200_query_status(void* workspace, cudaStream_t stream, int* device_sta
 // is a static device array of this translation unit instead of caller memory.
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[IRIS_NOALLOC_SCRATCH_BYTES];
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
-
-// Device address of the static scratch on the current device; the first call
-// per device looks it up and zero-fills it on `stream`.
-int noalloc_scratch(cudaStream_t stream, void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IRIS_ECUDA;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return IRIS_ECUDA;
-        if (cudaMemsetAsync(p, 0, IRIS_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return IRIS_ECUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
-    return IRIS_OK;
-}
 }  // namespace
 
 extern "C" int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, size_t off_A, size_t off_B,
                                                    size_t off_bias, size_t off_out, size_t off_gathered,
                                                    int64_t M, int64_t N, int64_t K, iris_dtype dtype,
                                                    const iris_b200_config* cfg, cudaStream_t stream) {
-    if (!heap || heap->world < 1 || heap->world > IRIS_MAX_WORLD || M < 0) return IRIS_EINVAL;
-    const int64_t flags = int64_t(heap->world) * ((M + BM - 1) / BM);
+    if (!heap || heap->world < 1 || heap->world > IRIS_MAX_WORLD || !dims_ok(M, N, K)) return IRIS_EINVAL;
+    // M <= INT32_MAX here, so the flag count cannot overflow
+    const int64_t flags = int64_t(heap->world) * cdiv(M, BM);
     if (flags > IRIS_NOALLOC_MAX_FLAGS) return IRIS_ENOWS;
+    // The array's device address on the current device, looked up on every
+    // call: a lookup allocates nothing, and an address cached across a device
+    // reset (which reloads the module) could be stale.
     void* scratch = nullptr;
-    int rc = noalloc_scratch(stream, &scratch);
-    if (rc != IRIS_OK) return rc;
-    // queue counters and status start at zero for this call; the epoch (first
-    // 4 bytes) carries over so flags left by earlier calls never match
-    if (cudaMemsetAsync(static_cast<char*>(scratch) + 4, 0, 28, stream) != cudaSuccess) return IRIS_ECUDA;
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || !scratch) return cuda_fail("cudaGetSymbolAddress (no-alloc scratch)", static_cast<int>(e));
+    // Every call starts from zeroed state: the header (queue counters, epoch,
+    // status) and the ready-flags this problem uses, so nothing left by an
+    // earlier call -- finished or stopped by a bounded wait -- can match.
+    const size_t used = WS_HEADER + size_t(flags) * 4;
+    e = cudaMemsetAsync(scratch, 0, used, stream);
+    if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync (no-alloc scratch)", static_cast<int>(e));
     return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, cfg,
                                        scratch, IRIS_NOALLOC_SCRATCH_BYTES, stream);
 }

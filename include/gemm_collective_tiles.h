@@ -105,7 +105,8 @@ typedef struct {
     int tile_k;            /* K block: 64 (only value); a pipeline stage holds one
                               K block, or two in the three-stage CTA-pair
                               pipeline (see stages) */
-    int group_m;           /* GROUP_M tile swizzle width in M blocks (default 32) */
+    int group_m;           /* GROUP_M tile swizzle width in 128-row M blocks
+                              (default 32; 16 in the concurrent mode) */
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
                               other queue when its own runs dry.  0 = op default
@@ -135,7 +136,9 @@ typedef struct {
     unsigned long long trace_buf; /* optional device buffer (as an address) for a
                               per-CTA timeline: 4 streams per CTA (scheduler, MMA,
                               TMA, workers) of trace_cap (event, ns) u64 pairs,
-                              pair 0 holding the count; 0 = off */
+                              pair 0 holding the count; the scheduler stream also
+                              records each CTA's kernel entry and the end of
+                              its teardown; 0 = off */
     int trace_cap;         /* pairs per stream (>= 2 when trace_buf is set) */
     int reduce_mode;       /* matmul_reduce_scatter / matmul_all_reduce reduce schedule:
                               0 = auto (3 when every rank's output slice is whole
@@ -155,6 +158,28 @@ typedef struct {
     int rank_inner;        /* reduce ops: 1 = order GEMM tiles with the rank index
                               fastest; 0 (default) = rank by rank inside each GROUP_M
                               group, so one rank's operands share the L2 at a time */
+    int coll_ring;         /* concurrent collectives: shared-memory buffers per
+                              worker warp (1 to 4; 0 = default 2).  With more
+                              than one, a warp's next loads are in flight
+                              while it sums and stores a sub-chunk; with one,
+                              each load is a whole 48 KB buffer and the four
+                              worker warps overlap each other instead. */
+    int coll_l2_hint;      /* concurrent collectives: L2 policy of their bulk
+                              copies.  0 = default (none), 1 = evict first (the
+                              streamed collective data does not push the
+                              concurrent GEMM's operands out of the L2),
+                              2 = none. */
+    int coll_path;         /* concurrent collectives: how their data moves.
+                              0 = default (3 where it applies, else 1);
+                              1 = TMA bulk loads into the CTA's pipeline
+                                  stages (lent by the GEMM for the tile) and
+                                  TMA bulk stores;
+                              2 = as 1, but the results are stored from the
+                                  worker threads' registers;
+                              3 = all-reduce and reduce-scatter with count and
+                                  comm_block multiples of 256: one 3-D TMA box
+                                  brings the same rows of all W sources (fewer,
+                                  larger requests); IRIS_EINVAL elsewhere. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */
@@ -329,12 +354,19 @@ IRIS_API int iris_b200_sm_partition_release(void);
  *   - Limit: W * ceil(M / 128) ready-flags must fit, i.e. W * ceil(M/128) <=
  *     IRIS_NOALLOC_MAX_FLAGS; larger problems return IRIS_ENOWS and launch
  *     nothing.
- *   - The first call on a device looks up the array's device address and
- *     zero-fills it (cudaMemsetAsync on `stream`).  Every call then clears
- *     the queue counters and the status word (one cudaMemsetAsync of 28 bytes on `stream`) and launches
- *     the kernel.  No call allocates or frees memory.
- *   - All calls share the one array: calls whose kernels overlap on the GPU
- *     (different streams, or several host threads) race and must not be made.
+ *   - `stream` must belong to the current device: the array used is the
+ *     current device's copy.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, which allocates nothing; no address is cached,
+ *     so a device reset cannot leave a stale one), zeroes the part of it this
+ *     problem uses -- the 256-byte header and W * ceil(M / 128) flags -- with
+ *     one cudaMemsetAsync on `stream`, and launches the kernel.  No call
+ *     allocates or frees memory.  The first call on a device may load the
+ *     library's GPU code (lazy module loading), so make it before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents:
+ *     calls whose kernels overlap on the GPU (different streams, or several
+ *     host threads) race and must not be made.
  *   - A bounded device wait that gives up is recorded in the array and
  *     cleared by the next call; it is not reported to the caller (use the
  *     workspace entry point and iris_b200_query_status when that is needed).

@@ -297,3 +297,53 @@ def test_long_k_default_pipeline_exact(op, W, M, N, K):
         assert_exact(bits(outs["out"][r]), want[r])
     if want_g is not None:
         assert_exact(bits(outs["gathered"]), want_g)
+
+
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter", "all_gather", "all_to_all", "broadcast"])
+@pytest.mark.parametrize("ring,hint,store", [(3, 0, 1), (4, 1, 0), (2, 1, 0), (4, 2, 0), (2, 0, 2), (3, 1, 2),
+                                             (0, 0, 3), (3, 1, 3), (1, 0, 1), (1, 1, 3)])
+def test_concurrent_collective_paths(coll, ring, hint, store):
+    """The collective tiles' buffer ring (1-4 buffers per worker warp), the
+    L2 evict-first policy on their bulk copies, the way results leave the SM
+    (TMA bulk stores or stores from registers) and the way sources arrive
+    (one 1-D copy per source, or one 3-D box of all sources for the summing
+    collectives) change only the schedule of the copies: the collective stays
+    bit-exact against the oracle and the GEMM exact on integer inputs, with
+    CTA pairs and with one CTA per tile."""
+    from gemm_collective_tiles_gb300 import _native
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem
+    W, count = 8, 3 * 16384 + 4096 + 256   # a ragged last item of 17 one-KB rows
+    M, N, K = 392, 512, 192
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=97, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=98)
+    if store == 3 and coll not in ("all_reduce", "reduce_scatter"):
+        # one box of all W sources per sub-chunk is a summing collective's path
+        prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count,
+                                 config={"comm_block": 16384, "coll_path": 3})
+        with pytest.raises(_native.IrisError) as e:
+            prob.run()
+        assert e.value.code == _native.IRIS_EINVAL
+        return
+    if coll == "all_reduce":
+        want = [oracle.all_reduce(X)] * W
+    elif coll == "reduce_scatter":
+        want = oracle.reduce_scatter(X)
+    elif coll == "all_gather":
+        want = [oracle.all_gather(X)] * W
+    elif coll == "all_to_all":
+        want = oracle.all_to_all(X)
+    else:
+        want = oracle.broadcast(X, 0)
+    for tile_m in (256, 128):
+        prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count,
+                                 config={"tile_m": tile_m, "comm_block": 16384, "gemm_ctas": 50,
+                                         "coll_ring": ring, "coll_l2_hint": hint, "coll_path": store})
+        prob.upload(A, B, X)
+        prob.poison_outputs()
+        prob.run()
+        assert query_status(prob.ws)[0] == 0
+        out = prob.outputs()
+        assert_exact(bits(out["C"]), oracle.gemm(A, B))
+        for r in range(W):
+            got = out["x"][r].contiguous().view(torch.uint8).numpy()
+            assert np.array_equal(got, np.ascontiguousarray(want[r]).view(np.uint8).reshape(-1)), f"rank {r}"
