@@ -70,6 +70,7 @@ class iris_b200_config(ctypes.Structure):
         ("coll_ring", ctypes.c_int),
         ("coll_l2_hint", ctypes.c_int),
         ("coll_path", ctypes.c_int),
+        ("gather_parts", ctypes.c_int),
     ]
 
 

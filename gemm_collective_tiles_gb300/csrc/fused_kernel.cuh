@@ -51,7 +51,9 @@ constexpr int NUM_WORKER_WARPS = 4;  // one per tensor-memory lane quadrant (or 
 constexpr int FIRST_WORKER_WARP = 3;   // warps 0..2: scheduler, MMA issuer, TMA producer
 constexpr int NUM_THREADS = 32 * (FIRST_WORKER_WARP + NUM_WORKER_WARPS);
 constexpr int RING = 8;           // work-item ring depth
-constexpr int GATHER_AHEAD = 2;   // all_gather_matmul: look-ahead gathers claimed per GEMM item
+// all_gather_matmul: look-ahead gather blocks claimed per GEMM item (times
+// the gather parts per block)
+constexpr int GATHER_AHEAD = 2;
 constexpr uint32_t ITEM_END = 0xFFFFFFFFu;
 constexpr uint32_t ITEM_COMM = 0x80000000u;
 constexpr int DEV_TIMEOUT = 1;
@@ -141,6 +143,7 @@ struct Params {
     int coll_path;                     // concurrent collectives: 1 TMA, 2 TMA loads + register stores,
                                        // 3 one 3-D TMA box per sub-chunk for all W sources
     int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
+    int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int rank_inner;                    // reduce ops: 1 = rank index fastest in the GEMM item order
     unsigned long long* trace;         // optional per-CTA event trace (nullptr = off)
     int trace_cap;                     // events per (CTA, role)
@@ -254,6 +257,24 @@ __device__ __forceinline__ bool wait_flag(const Ctl& c, const uint32_t* flag, in
     }
 }
 
+// Bounded wait for a 64-bit counter to hold `want` (acquire).
+__device__ __forceinline__ bool wait_count(const Ctl& c, const unsigned long long* ctr, unsigned long long want,
+                                           int where, int index) {
+    if (ld_acquire_gpu_u64(ctr) == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu_u64(ctr) == want) return true;
+        if ((i & 7) == 0) {
+            if (launch_aborted(c)) return false;
+            if (global_timer_ns() - t0 > c.limit) {
+                raise_timeout(c, where, index);
+                return false;
+            }
+        }
+    }
+}
+
 // Teardown wait: same as wait_bar but ignores the abort flag (the async work
 // it waits for always completes); still bounded.
 __device__ __forceinline__ bool drain_bar(const Ctl& c, uint64_t* bar, uint32_t parity, int where) {
@@ -347,35 +368,50 @@ __device__ __forceinline__ int own_block(const Params& p, const GemmCoord& gc, i
 
 // all_gather_matmul gather items are numbered swizzle group by swizzle group
 // (the groups of group_m m-blocks the GEMM order walks through) and, inside a
-// group, shard-major: item = first_m * W + s * gsz + (mb - first_m).  Every
-// m-block's shard 0 comes before any shard 1, so with the gathers spread over
-// all CTAs the first K-blocks of the group's tiles arrive first.
+// group, shard-major, the p.gather_parts row parts of one (m-block, shard)
+// consecutive: item = (first_m * W + s * gsz + (mb - first_m)) * parts + part.
+// Parts let the copies of one shard spread over many CTAs, so the shards of
+// a block land in order while its first tiles already run.
+// Every m-block's shard 0 comes before any shard 1, so with the gathers
+// spread over all CTAs the first K-blocks of the group's tiles arrive first.
 struct GatherCoord {
-    int mb, s;
+    int mb, s, part;
 };
 __device__ __forceinline__ GatherCoord decode_gather(const Params& p, uint32_t c) {
+    const uint32_t blk = c / static_cast<uint32_t>(p.gather_parts);  // (m-block, shard) copy
     const uint32_t per_group = static_cast<uint32_t>(p.group_m) * p.W;
-    const int first_m = static_cast<int>(c / per_group) * p.group_m;
+    const int first_m = static_cast<int>(blk / per_group) * p.group_m;
     const int gsz = min(p.m_blocks - first_m, p.group_m);
-    const int local = static_cast<int>(c - static_cast<uint32_t>(first_m) * p.W);
+    const int local = static_cast<int>(blk - static_cast<uint32_t>(first_m) * p.W);
     GatherCoord gc;
     gc.s = local / gsz;
     gc.mb = first_m + (local - gc.s * gsz);
+    gc.part = static_cast<int>(c % static_cast<uint32_t>(p.gather_parts));
     return gc;
 }
 
 // Number of gather items that must be claimed before GEMM item x may be
 // published: every item of the groups before x's, and in x's group the items
-// up to shard W-1 of x's m-block.  Inside a group the GEMM order first visits
-// its m-blocks in order, so the need grows by one per item there and stays at
-// the whole group afterwards (monotonic in x).
+// up to shard W-1 of x's m-block (all its parts).  Inside a group the GEMM
+// order first visits its m-blocks in order, so the need grows by one block
+// per item there and stays at the whole group afterwards (monotonic in x).
 __device__ __forceinline__ uint32_t gather_need(const Params& p, uint32_t x) {
     const uint32_t group_size = static_cast<uint32_t>(p.group_m) * p.n_blocks;
     const uint32_t group = x / group_size;
     const int first_m = static_cast<int>(group) * p.group_m;
     const int gsz = min(p.m_blocks - first_m, p.group_m);
     const int local = static_cast<int>(x - group * group_size);
-    return static_cast<uint32_t>(first_m) * p.W + static_cast<uint32_t>((p.W - 1) * gsz + min(local, gsz - 1) + 1);
+    return static_cast<uint32_t>(p.gather_parts) * (static_cast<uint32_t>(first_m) * p.W +
+                           static_cast<uint32_t>((p.W - 1) * gsz + min(local, gsz - 1) + 1));
+}
+
+// all_gather_matmul ready counters: one epoch-tagged 64-bit arrival counter
+// per (128-row block, shard), complete when all its parts are in
+__device__ __forceinline__ unsigned long long* gather_ctr(const Params& p, int fi) {
+    return reinterpret_cast<unsigned long long*>(p.flags) + fi;
+}
+__device__ __forceinline__ unsigned long long gather_done(const Params& p, uint32_t epoch) {
+    return (static_cast<unsigned long long>(epoch) << 32) | static_cast<uint32_t>(p.gather_parts);
 }
 
 __device__ __forceinline__ float bits16_to_float(uint32_t b, int bf16) {
@@ -525,7 +561,7 @@ __device__ void run_scheduler(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
             int ahead = 0;
             while (!comm_dry) {
                 const uint32_t head = ld_relaxed_gpu(&p.ws->comm_ctr);
-                if (head >= need && (head >= need_ahead || ahead >= GATHER_AHEAD)) break;
+                if (head >= need && (head >= need_ahead || ahead >= GATHER_AHEAD * p.gather_parts)) break;
                 const uint32_t c = atomicAdd(&p.ws->comm_ctr, 1u);
                 if (c >= p.n_comm) {
                     comm_dry = true;
@@ -644,7 +680,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 acquired = p.W;
             } else {
                 uint32_t seen = 0;
-                for (int s = 0; s < p.W; ++s) seen += ld_acquire_gpu(&p.flags[blk * p.W + s]) == ctl.epoch ? 1u : 0u;
+                for (int s = 0; s < p.W; ++s)
+                    seen += ld_acquire_gpu_u64(gather_ctr(p, blk * p.W + s)) == gather_done(p, ctl.epoch) ? 1u : 0u;
                 if (seen == static_cast<uint32_t>(p.W)) {
                     acquired = p.W;
                     fence_proxy_async_global();
@@ -659,7 +696,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 if (s_hi >= acquired) {
                     for (int s = acquired; s <= s_hi; ++s) {
                         const int fi = blk * p.W + s;
-                        if (!wait_flag(ctl, &p.flags[fi], WAIT_FLAG_GATHER, fi)) return false;
+                        if (!wait_count(ctl, gather_ctr(p, fi), gather_done(p, ctl.epoch), WAIT_FLAG_GATHER, fi))
+                            return false;
                     }
                     acquired = s_hi + 1;
                     fence_proxy_async_global();
@@ -1196,24 +1234,6 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
     return true;
 }
 
-// Bounded wait for a 64-bit counter to hold `want` (acquire).
-__device__ __forceinline__ bool wait_count(const Ctl& c, const unsigned long long* ctr, unsigned long long want,
-                                           int where, int index) {
-    if (ld_acquire_gpu_u64(ctr) == want) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        __nanosleep(64);
-        if (ld_acquire_gpu_u64(ctr) == want) return true;
-        if ((i & 7) == 0) {
-            if (launch_aborted(c)) return false;
-            if (global_timer_ns() - t0 > c.limit) {
-                raise_timeout(c, where, index);
-                return false;
-            }
-        }
-    }
-}
-
 // Chained reduce epilogue (reduce ops, reduce_mode 3): rank s of output tile t
 // waits until ranks 0..s-1 have folded their partials into the fp32 running
 // sum S[t] (tile counter = s), then folds in its own partial P_s = acc + bias_s,
@@ -1408,12 +1428,15 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
     const GatherCoord gq = decode_gather(p, c);
     const int mb = gq.mb * CG + ctl.half, s = gq.s;
     if (mb * BM >= p.M) return true;  // below the last row: nothing to copy, no consumer
-    const int rows = min(BM, p.M - mb * BM);
+    const int block_rows = min(BM, p.M - mb * BM);
+    // this item's row part of the block
+    const int r_lo = gq.part * block_rows / p.gather_parts, r_hi = (gq.part + 1) * block_rows / p.gather_parts;
+    const int rows = r_hi - r_lo;
     const int vpr = p.K_local / 8;  // 16-byte vectors per shard row
     const int Kv = p.K / 8;         // vectors per gathered row
     const uint4* src = reinterpret_cast<const uint4*>(p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_A) +
-                       static_cast<size_t>(mb) * BM * vpr;
-    uint4* dst = reinterpret_cast<uint4*>(p.heap + p.off_gathered) + static_cast<size_t>(mb) * BM * Kv +
+                       (static_cast<size_t>(mb) * BM + r_lo) * vpr;
+    uint4* dst = reinterpret_cast<uint4*>(p.heap + p.off_gathered) + (static_cast<size_t>(mb) * BM + r_lo) * Kv +
                  static_cast<size_t>(s) * vpr;
     // The shard block (rows x vpr vectors, contiguous) is copied as one flat
     // range: thread t takes vectors t, t + 128, ...; U loads per thread are in
@@ -1442,8 +1465,13 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
     fence_proxy_async_global();
     __threadfence();
     if (!worker_sync(ctl, sm, wc)) return false;
+    // count this part in; the block's counter completes with the last part
+    // (the test hook drops part 0's arrival of one block)
     const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
-    if (wc.w == 0 && wc.lane == 0 && p.debug_skip != fi + 1) st_release_gpu(&p.flags[fi], ctl.epoch);
+    if (wc.w == 0 && wc.lane == 0 && !(p.debug_skip == fi + 1 && gq.part == 0)) {
+        __threadfence();
+        arrive_count(gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
+    }
     return true;
 }
 

@@ -165,7 +165,8 @@ struct Cfg {
     int stages;       // CTA pairs: requested 0 / 3 / 6, resolved by resolve_stages; one-CTA tiles: 0
     int coll_ring;    // concurrent collectives: buffers per worker warp
     int coll_evict_first;
-    int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 registers only
+    int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 one box of all sources
+    int gather_parts;    // all_gather_matmul: gather items per (row block, shard)
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -216,6 +217,11 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     out.coll_ring = c->coll_ring ? c->coll_ring : 2;
     if (c->coll_l2_hint < 0 || c->coll_l2_hint > 2) return IRIS_EINVAL;
     out.coll_evict_first = c->coll_l2_hint == 1 ? 1 : 0;
+    if (c->gather_parts < 0 || c->gather_parts > 16) return IRIS_EINVAL;
+    // one gather item per (128-row block, shard) copy: splitting it in row
+    // parts measured slower on every shape tried (more claims contending on
+    // the comm queue counter and more per-item synchronisation)
+    out.gather_parts = c->gather_parts ? c->gather_parts : 1;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
     out.coll_path = c->coll_path;  // 0: chosen per collective (resolve_coll_path)
     return IRIS_OK;
@@ -279,7 +285,7 @@ WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n, int redu
     const int64_t mb = cdiv(M, BM), nb = cdiv(N, tile_n);
     const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
     if (op == IRIS_OP_ALL_GATHER_MATMUL)
-        L.n_flags = static_cast<size_t>(W) * mb;
+        L.n_flags = 2 * static_cast<size_t>(W) * mb;  // 8-byte ready counters per (128-row block, shard)
     else if (reduce_op)
         L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte tile counters
     L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
@@ -584,7 +590,9 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     p.off_bias = has_bias ? off_bias : 0;
     p.has_bias = has_bias;
     p.n_gemm = (M > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
-    p.n_comm = static_cast<uint32_t>(mblocks) * W;
+    p.gather_parts = c.gather_parts;
+    if (int64_t(mblocks) * W * c.gather_parts >= 0x7FFFFFFF) return IRIS_EINVAL;
+    p.n_comm = static_cast<uint32_t>(mblocks) * W * c.gather_parts;
     tail_split(p, c, false);
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_ALL_GATHER_MATMUL, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
@@ -954,7 +962,7 @@ extern "C" int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, s
     // Every call starts from zeroed state: the header (queue counters, epoch,
     // status) and the ready-flags this problem uses, so nothing left by an
     // earlier call -- finished or stopped by a bounded wait -- can match.
-    const size_t used = WS_HEADER + size_t(flags) * 4;
+    const size_t used = WS_HEADER + size_t(flags) * 8;
     e = cudaMemsetAsync(scratch, 0, used, stream);
     if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync (no-alloc scratch)", static_cast<int>(e));
     return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, cfg,

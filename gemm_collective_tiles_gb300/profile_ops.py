@@ -1,0 +1,50 @@
+"""Run one benchmark workload's fused kernel a few times (for an ncu capture).
+
+    python -m gemm_collective_tiles_gb300.profile_ops WORKLOAD [LAUNCHES]
+
+WORKLOAD is a fused-op workload name of ``synthetic.WORKLOADS`` or
+``concurrent_ar_w8``; inputs are drawn as the benchmark draws them.  Used by
+the profiling commands recorded under ``profiles/``.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+def main(argv):
+    import torch
+
+    import synthetic
+    from gemm_collective_tiles_gb300 import query_status
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem, FusedProblem
+    name = argv[0]
+    launches = int(argv[1]) if len(argv) > 1 else 6
+    torch.cuda.set_device(0)
+    if name == "concurrent_ar_w8":
+        cw = synthetic.CONCURRENT_WORKLOAD
+        A, B = synthetic.make_gemm_inputs(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], cw["gemm_seed"],
+                                          dist="normal", scale=1.0)
+        X = synthetic.make_coll_inputs(cw["W"], cw["count"], cw["coll_dtype"], cw["coll_seed"])
+        prob = ConcurrentProblem(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], "all_reduce", cw["W"], cw["count"],
+                                 coll_dtype=cw["coll_dtype"])
+        prob.upload(A, B, X)
+    else:
+        wl = synthetic.WORKLOADS[name]
+        x = synthetic.make_fused_inputs(**wl)
+        prob = FusedProblem(wl["op"], wl["W"], wl["M"], wl["N"], wl["K"], wl["dtype"], bias=wl.get("bias", False))
+        prob.upload(x.A, x.B, x.bias)
+    for _ in range(launches):
+        prob.run()
+    torch.cuda.synchronize()
+    rc = query_status(prob.ws)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status {rc}")
+    print(f"{name}: {launches} launches ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv[1:]))

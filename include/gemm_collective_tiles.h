@@ -180,6 +180,11 @@ typedef struct {
                                   comm_block multiples of 256: one 3-D TMA box
                                   brings the same rows of all W sources (fewer,
                                   larger requests); IRIS_EINVAL elsewhere. */
+    int gather_parts;      /* all_gather_matmul: gather items per (128-row block,
+                              shard) copy, each a row part of the block
+                              (1..16; 0 = default 1).  More parts spread a
+                              shard's copies over more CTAs at the cost of
+                              more claims and synchronisation per byte. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */
@@ -209,9 +214,10 @@ IRIS_API int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t 
  *                (with replicate_outputs, every region receives the same bits).
  *   off_gathered region 0 receives the gathered A: M x K, shard s in columns
  *                [s*K/W, (s+1)*K/W) -- bit-exact copies of the shards.
- * Comm tiles copy each shard's row block into the gathered buffer and release
- * a per-(shard, row block) flag; GEMM tiles acquire the flags of the shards
- * they consume just before loading them.
+ * Comm tiles copy each shard's row block into the gathered buffer, a row part
+ * at a time (cfg->gather_parts parts per 128-row block), and count themselves into a
+ * per-(shard, row block) ready counter (epoch-tagged, release); GEMM tiles
+ * acquire the counters of the shards they consume just before loading them.
  * Requires K % W == 0, (K/W) % 8 == 0, N % 8 == 0.
  */
 IRIS_API int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t off_B,
@@ -351,7 +357,8 @@ IRIS_API int iris_b200_sm_partition_release(void);
  * status word and ready-flags live instead in a fixed static device array of
  * IRIS_NOALLOC_SCRATCH_BYTES bytes inside this library (every GPU that loads
  * the library holds it until the process exits).
- *   - Limit: W * ceil(M / 128) ready-flags must fit, i.e. W * ceil(M/128) <=
+ *   - Limit: W * ceil(M / 128) ready counters (8 bytes each, one per
+ *     128-row block and shard) must fit, i.e. W * ceil(M/128) <=
  *     IRIS_NOALLOC_MAX_FLAGS; larger problems return IRIS_ENOWS and launch
  *     nothing.
  *   - `stream` must belong to the current device: the array used is the
@@ -359,7 +366,7 @@ IRIS_API int iris_b200_sm_partition_release(void);
  *   - Every call looks up the array's device address on the current device
  *     (cudaGetSymbolAddress, which allocates nothing; no address is cached,
  *     so a device reset cannot leave a stale one), zeroes the part of it this
- *     problem uses -- the 256-byte header and W * ceil(M / 128) flags -- with
+ *     problem uses -- the 256-byte header and W * ceil(M / 128) counters -- with
  *     one cudaMemsetAsync on `stream`, and launches the kernel.  No call
  *     allocates or frees memory.  The first call on a device may load the
  *     library's GPU code (lazy module loading), so make it before any stream
@@ -372,7 +379,7 @@ IRIS_API int iris_b200_sm_partition_release(void);
  *     workspace entry point and iris_b200_query_status when that is needed).
  */
 #define IRIS_NOALLOC_MAX_FLAGS 16384
-#define IRIS_NOALLOC_SCRATCH_BYTES (256 + 4 * IRIS_NOALLOC_MAX_FLAGS)
+#define IRIS_NOALLOC_SCRATCH_BYTES (256 + 8 * IRIS_NOALLOC_MAX_FLAGS)
 IRIS_API int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, size_t off_A,
                                                  size_t off_B, size_t off_bias, size_t off_out,
                                                  size_t off_gathered, int64_t M, int64_t N,

@@ -40,10 +40,10 @@ def test_strerror_and_codes():
 def test_workspace_size_layout():
     lib = N.load()
     out = ctypes.c_size_t(0)
-    # all_gather_matmul: header + W * m_blocks flags
+    # all_gather_matmul: header + W * m_blocks 8-byte ready counters
     assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 4096, 14336, 4096, 8, N.IRIS_BF16,
                                         None, ctypes.byref(out)) == 0
-    assert out.value == 256 + ((8 * 32 * 4 + 255) // 256) * 256
+    assert out.value == 256 + ((8 * 32 * 8 + 255) // 256) * 256
     # reduce-scatter, default (chained) schedule: flags / tile counters + one
     # fp32 running sum of M x N
     assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_REDUCE_SCATTER, 4096, 4096, 4096, 4, N.IRIS_F16,

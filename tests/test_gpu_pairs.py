@@ -347,3 +347,24 @@ def test_concurrent_collective_paths(coll, ring, hint, store):
         for r in range(W):
             got = out["x"][r].contiguous().view(torch.uint8).numpy()
             assert np.array_equal(got, np.ascontiguousarray(want[r]).view(np.uint8).reshape(-1)), f"rank {r}"
+
+
+@pytest.mark.parametrize("parts", [1, 3, 4, 16])
+@pytest.mark.parametrize("tile_m", [256, 128])
+def test_ag_mm_gather_parts_exact(parts, tile_m):
+    """all_gather_matmul with each (row block, shard) copy cut into `parts`
+    row parts (ragged: 392 rows leave a last block of 8 rows, fewer rows than
+    parts): the gathered A is bit-exact and the output exact on integer
+    inputs, for CTA pairs and one CTA per tile."""
+    W, M, N, K = 4, 392, 520, 256
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=99, dist="int", scale=2, bias=True,
+                                    bias_scale=2)
+    prob = FusedProblem("ag_mm", W, M, N, K, "bf16", bias=True, config={"gather_parts": parts, "tile_m": tile_m})
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    outs = prob.outputs()
+    want_out, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    assert_exact(bits(outs["gathered"]), want_g)
+    assert_exact(bits(outs["out"][0]), want_out)
