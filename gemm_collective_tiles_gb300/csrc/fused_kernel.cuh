@@ -80,6 +80,7 @@ enum : int {
     WAIT_LEASE_DONE = 18,
     WAIT_COLL_LOAD = 19,
     WAIT_DRAIN = 20,
+    WAIT_GATHER_TMA = 21,
 };
 
 // First 256 bytes of the workspace.
@@ -107,6 +108,8 @@ struct Params {
                       // (one load per stage fills a CTA's B columns; set when N % 64 == 0)
     CUtensorMap tmAc; // A as 64-column K chunks: 4-D {64, row, k / 64, rank}, box {64, 128, KS, 1}
                       // (CTA pairs: one load per stage; set when K % 64 == 0)
+    CUtensorMap tmGs; // all_gather_matmul start-up gathers: the shards, 3-D {K_l, M, W}, box {gather_box, 128, 1}
+    CUtensorMap tmGd; // ... and the gathered buffer, 3-D {K, M, 1}, box {gather_box, 128, 1} (no swizzle)
     CUtensorMap tmX;  // concurrent all-reduce / reduce-scatter input (coll_path 3): 3-D fp32
                       // {256, count / 256, W} (1 KB rows; regions rank_stride apart), box {256, R, W}
     int b_chunked;    // tmBc is valid
@@ -144,6 +147,9 @@ struct Params {
                                        // 3 one 3-D TMA box per sub-chunk for all W sources
     int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
+    int startup_gather;                // all_gather_matmul: the TMA producer copies the gathers claimed
+                                       // before its CTA's first GEMM item (TMA boxes through its idle stages)
+    int gather_box;                    // ... columns per box
     int rank_inner;                    // reduce ops: 1 = rank index fastest in the GEMM item order
     unsigned long long* trace;         // optional per-CTA event trace (nullptr = off)
     int trace_cap;                     // events per (CTA, role)
@@ -441,7 +447,7 @@ struct Smem {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr uint32_t STAGE_OUT_BYTES = 2 * 32 * 32 * 4;  // per worker warp: 2 x (32 rows x 32 fp32)
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + SBARS * NUM_WORKER_WARPS + 2;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * RING + 2 + SBARS * NUM_WORKER_WARPS + 3;
     static constexpr int READY_BITS = 4096;  // all_gather_matmul: m-blocks whose gathers this CTA has seen complete
     static constexpr uint32_t BYTES = 1024 /*align slack*/ + TILES_BYTES +
                                       NUM_WORKER_WARPS * STAGE_OUT_BYTES + NUM_BARS * 8 + (RING + 4) * 4 +
@@ -452,6 +458,7 @@ struct Smem {
     uint64_t* sbar;  // per worker warp: SBARS barriers for running-sum / collective chunk loads
     uint64_t* lease;       // TMA producer -> workers: pipeline stages lent for a collective tile
     uint64_t* lease_done;  // workers -> TMA producer: stages returned
+    uint64_t* gbar;        // TMA producer: its start-up gather loads
     volatile uint32_t* ring;
     uint32_t* tmem_slot;
     uint32_t* epoch_slot;
@@ -474,7 +481,8 @@ struct Smem {
         sbar = final_bar + 1;
         lease = sbar + SBARS * NUM_WORKER_WARPS;
         lease_done = lease + 1;
-        uint32_t* u = reinterpret_cast<uint32_t*>(lease_done + 1);
+        gbar = lease_done + 1;
+        uint32_t* u = reinterpret_cast<uint32_t*>(gbar + 1);
         ring = u;
         tmem_slot = u + RING;
         epoch_slot = u + RING + 1;
@@ -649,6 +657,48 @@ __device__ __forceinline__ void release_item(Smem<BN, STAGES, CG>& sm, uint32_t 
         mbar_arrive(&sm.item_empty[slot]);
 }
 
+// all_gather_matmul start-up gather, run by the TMA producer (startup_gather):
+// the gathers a CTA pair claims before its first GEMM item arrive while its
+// pipeline stages are still idle, so the producer copies this CTA's 128 rows
+// of (m-block, shard) with TMA boxes of gather_box columns (up to 64 KB each)
+// through the stages -- as many boxes in flight as the stages hold -- instead
+// of leaving them to the worker threads' 16-byte copies.  Then the stores
+// complete, the proxy fence orders them before the release, and the copy
+// counts itself into the block's ready counter.
+template <int BN, int STAGES, int CG>
+__device__ bool tma_gather(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c,
+                           uint32_t& gphase) {
+    const GatherCoord gq = decode_gather(p, c);
+    const int mb = gq.mb * CG + ctl.half, s = gq.s;
+    if (mb * BM >= p.M) return true;  // below the last row: nothing to copy, no consumer
+    const uint32_t box_bytes = static_cast<uint32_t>(p.gather_box) * 2u * BM;
+    const int slots = static_cast<int>(Smem<BN, STAGES, CG>::TILES_BYTES / box_bytes);
+    const int nbox = p.K_local / p.gather_box;
+    bool ok = true;
+    for (int j0 = 0; j0 < nbox && ok; j0 += slots) {
+        const int nb = min(slots, nbox - j0);
+        // rows past M read as zeros and are not stored
+        mbar_arrive_expect_tx(sm.gbar, box_bytes * static_cast<uint32_t>(nb));
+        for (int j = 0; j < nb; ++j)
+            tma_load_3d(sm.tiles + j * box_bytes, &p.tmGs, (j0 + j) * p.gather_box, mb * BM, s, sm.gbar);
+        ok = wait_bar(ctl, sm.gbar, gphase, WAIT_GATHER_TMA);
+        if (!ok) drain_bar(ctl, sm.gbar, gphase, WAIT_GATHER_TMA);  // the loads land before the stages are reused
+        gphase ^= 1u;
+        if (!ok) break;
+        for (int j = 0; j < nb; ++j)
+            tma_store_3d(&p.tmGd, sm.tiles + j * box_bytes, s * p.K_local + (j0 + j) * p.gather_box, mb * BM, 0);
+        bulk_commit();
+        bulk_wait_read_all();  // the next boxes (or the GEMM's loads) may overwrite the stages
+    }
+    bulk_wait_all();
+    if (!ok) return false;
+    fence_proxy_async_global();
+    __threadfence();
+    const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
+    if (p.debug_skip != fi + 1) arrive_count(gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
+    return true;
+}
+
 // ============================================================ TMA producer
 // Follows the item ring; for every GEMM item streams its K-blocks of A and B
 // into the STAGES-deep shared-memory pipeline (acquiring the gather flags of
@@ -759,6 +809,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
     };
 
     uint32_t leases = 0;
+    bool seen_gemm = false;  // a GEMM item has passed (start-up gathers are the comm items before it)
+    uint32_t gphase = 0;
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
         if (!wait_bar(ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_TMA, CG == 2)) break;
@@ -767,6 +819,10 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         ++ring_n;
         if (item == ITEM_END) break;
         if (item & ITEM_COMM) {
+            if (p.op == OP_AG_MM && p.startup_gather && !seen_gemm) {
+                if (!tma_gather(p, ctl, sm, item & ~ITEM_COMM, gphase)) break;
+                continue;
+            }
             if (p.op != OP_CONC) continue;
             // lend the pipeline stages to the workers for this collective
             // tile: every load issued so far must have been consumed first
@@ -779,6 +835,7 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             ++leases;
             continue;
         }
+        seen_gemm = true;
         tr.rec(EV_BEGIN, item);
         if (!load_gemm(item)) break;
         tr.rec(EV_END, item);
@@ -1824,6 +1881,7 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
     ps.ready = false;
     uint32_t ring_n = 0, acc_i = 0;
     bool ok = true;
+    bool seen_gemm = false;  // as the TMA producer tracks it
     while (true) {
         const uint32_t slot = ring_n % RING, use = ring_n / RING;
         ok = wait_bar_working<BN>(p, ctl, &sm.item_full[slot], use & 1, WAIT_ITEM_FULL_WORKER, ps, wc, CG == 2);
@@ -1838,7 +1896,9 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
         tr.rec(EV_BEGIN, item);
         if (item & ITEM_COMM) {
             const uint32_t c = item & ~ITEM_COMM;
-            if (p.op == OP_AG_MM) {
+            if (p.op == OP_AG_MM && p.startup_gather && !seen_gemm) {
+                // a start-up gather: the TMA producer copies it
+            } else if (p.op == OP_AG_MM) {
                 ok = gather_tile(p, ctl, sm, c, wc);
             } else if (p.op == OP_CONC) {
                 int got = 1;
@@ -1851,6 +1911,7 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
                 ok = reduce_tile<BN, STAGES, CG>(p, ctl, c, wc);
             }
         } else {
+            seen_gemm = true;
             if (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR))
                 ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
             else
@@ -1928,6 +1989,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         for (int i = 0; i < SBARS * NUM_WORKER_WARPS; ++i) mbar_init(&sm.sbar[i], 1);
         mbar_init(sm.lease, 1);
         mbar_init(sm.lease_done, NUM_WORKER_WARPS);
+        mbar_init(sm.gbar, 1);
         for (int i = 0; i < Smem<BN, STAGES, CG>::READY_BITS / 32; ++i) sm.ready_bits[i] = 0u;
         fence_mbar_init();
         uint32_t e = *reinterpret_cast<volatile uint32_t*>(&p.ws->epoch) + 1u;

@@ -167,6 +167,7 @@ struct Cfg {
     int coll_evict_first;
     int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 one box of all sources
     int gather_parts;    // all_gather_matmul: gather items per (row block, shard)
+    int startup_gather;  // all_gather_matmul: 1 = worker copies, 2 = the TMA producer copies start-up gathers
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -222,6 +223,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     // parts measured slower on every shape tried (more claims contending on
     // the comm queue counter and more per-item synchronisation)
     out.gather_parts = c->gather_parts ? c->gather_parts : 1;
+    if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
+    out.startup_gather = c->startup_gather ? c->startup_gather : 1;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
     out.coll_path = c->coll_path;  // 0: chosen per collective (resolve_coll_path)
     return IRIS_OK;
@@ -372,6 +375,36 @@ int make_a_chunk_map(Params& p, const Cfg& c, const void* base, int64_t rows, in
     if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled (A chunks)", static_cast<int>(r));
     p.a_chunked = 1;
     return IRIS_OK;
+}
+
+// all_gather_matmul start-up gathers by the TMA producer: the shards as 3-D
+// {K_l, M, W} (regions rank_stride apart) and the gathered buffer as 3-D
+// {K, M, 1}, both with an unswizzled box {gi, 128, 1}, gi the widest of 256,
+// 128, ..., 8 columns dividing K_l.  A box lands in shared memory as 128 rows
+// of gi columns and leaves the same way.
+int make_gather_maps(Params& p, const iris_b200_heap* heap, size_t off_A, size_t off_gathered, int64_t M,
+                     int64_t K, int64_t K_l) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return IRIS_ECUDA;
+    int gi = 256;
+    while (K_l % gi != 0) gi /= 2;
+    p.gather_box = gi;
+    const CUtensorMapDataType dt = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(gi), BM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    cuuint64_t sdims[3] = {static_cast<cuuint64_t>(K_l), static_cast<cuuint64_t>(M),
+                           static_cast<cuuint64_t>(heap->world)};
+    cuuint64_t sstrides[2] = {static_cast<cuuint64_t>(K_l) * 2, heap->rank_stride};
+    CUresult r = enc(&p.tmGs, dt, 3, static_cast<char*>(heap->base) + off_A, sdims, sstrides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled (gather source)", static_cast<int>(r));
+    cuuint64_t ddims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M), 1};
+    cuuint64_t dstrides[2] = {static_cast<cuuint64_t>(K) * 2, round_up(size_t(M) * K * 2, 16)};
+    r = enc(&p.tmGd, dt, 3, static_cast<char*>(heap->base) + off_gathered, ddims, dstrides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? IRIS_OK : cuda_fail("cuTensorMapEncodeTiled (gather destination)", static_cast<int>(r));
 }
 
 // Concurrent all-reduce / reduce-scatter input for coll_path 3: 3-D fp32
@@ -591,6 +624,9 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     p.has_bias = has_bias;
     p.n_gemm = (M > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
     p.gather_parts = c.gather_parts;
+    // the producer's start-up copies move whole 128-row blocks
+    p.startup_gather = (c.startup_gather == 2 && c.gather_parts == 1 && M > 0 && K_l > 0) ? 1 : 0;
+    if (p.startup_gather && (rc = make_gather_maps(p, heap, off_A, off_gathered, M, K, K_l))) return rc;
     if (int64_t(mblocks) * W * c.gather_parts >= 0x7FFFFFFF) return IRIS_EINVAL;
     p.n_comm = static_cast<uint32_t>(mblocks) * W * c.gather_parts;
     tail_split(p, c, false);

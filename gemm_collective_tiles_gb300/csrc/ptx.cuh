@@ -190,6 +190,14 @@ __device__ __forceinline__ void bulk_store_hint(void* gdst, const void* smem_src
                  : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (bulk-group completion)
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* smem_src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+
 // 4-D tiled store of one box from shared memory (bulk-group completion)
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* smem_src, int c0, int c1,
                                              int c2, int c3) {

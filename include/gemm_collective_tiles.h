@@ -185,6 +185,13 @@ typedef struct {
                               (1..16; 0 = default 1).  More parts spread a
                               shard's copies over more CTAs at the cost of
                               more claims and synchronisation per byte. */
+    int startup_gather;    /* all_gather_matmul: who copies the gathers a CTA
+                              pair claims before its first GEMM tile.  1 (and
+                              0, the default) = the worker threads, 16-byte
+                              copies through registers; 2 = the TMA producer,
+                              with TMA boxes through its still idle pipeline
+                              stages (whole 128-row blocks: needs
+                              gather_parts 1, else the workers copy). */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

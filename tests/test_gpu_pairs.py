@@ -368,3 +368,49 @@ def test_ag_mm_gather_parts_exact(parts, tile_m):
     want_out, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
     assert_exact(bits(outs["gathered"]), want_g)
     assert_exact(bits(outs["out"][0]), want_out)
+
+
+@pytest.mark.parametrize("W,M,N,K", [(2, 256, 256, 256), (4, 392, 520, 256), (8, 200, 136, 576),
+                                     (2, 1, 8, 16), (4, 640, 512, 4 * 2048)])
+@pytest.mark.parametrize("tile_m", [0, 128])   # 0: the default (CTA pairs wherever they apply)
+def test_ag_mm_startup_gather_by_producer_exact(W, M, N, K, tile_m):
+    """The gathers claimed before a CTA's first GEMM tile copied by its TMA
+    producer (boxes of up to 256 columns x 128 rows through the idle stages;
+    ragged rows, shards 9 to 2048 columns wide, one box or several batches):
+    gathered A bit-exact, output exact on integer inputs."""
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "f16", seed=100 + M, dist="int", scale=2, bias=True,
+                                    bias_scale=2)
+    prob = FusedProblem("ag_mm", W, M, N, K, "f16", bias=True, config={"startup_gather": 2, "tile_m": tile_m})
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    outs = prob.outputs()
+    want_out, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    assert_exact(bits(outs["gathered"]), want_g)
+    assert_exact(bits(outs["out"][0]), want_out)
+
+
+def test_ag_mm_startup_gather_stopped_then_exact():
+    """A start-up gather whose ready counter is never completed (test hook)
+    makes the waiting tile's bounded wait give up; the producer's copies
+    drain, IRIS_ETIMEOUT is reported, and the next call on the same
+    workspace is exact."""
+    from gemm_collective_tiles_gb300 import _native
+    W, M, N, K = 4, 256, 512, 256
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=104, dist="int", scale=2)
+    bad = FusedProblem("ag_mm", W, M, N, K, "bf16", config={"startup_gather": 2, "debug_skip_flag": 2,
+                                                            "wait_ns": 50_000_000})
+    bad.upload(x.A, x.B, x.bias)
+    bad.run()
+    assert query_status(bad.ws)[0] == _native.IRIS_ETIMEOUT
+    good = FusedProblem("ag_mm", W, M, N, K, "bf16", config={"startup_gather": 2})
+    good.ws = bad.ws
+    good.upload(x.A, x.B, x.bias)
+    good.poison_outputs()
+    good.run()
+    assert query_status(good.ws)[0] == 0
+    want_out, want_g = oracle.all_gather_matmul(x.A, x.B[0], None)
+    outs = good.outputs()
+    assert_exact(bits(outs["gathered"]), want_g)
+    assert_exact(bits(outs["out"][0]), want_out)
