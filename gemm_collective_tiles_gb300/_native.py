@@ -72,6 +72,7 @@ class iris_b200_config(ctypes.Structure):
         ("coll_path", ctypes.c_int),
         ("gather_parts", ctypes.c_int),
         ("startup_gather", ctypes.c_int),
+        ("gemm_l2_hint", ctypes.c_int),
     ]
 
 

@@ -147,6 +147,7 @@ struct Params {
                                        // 3 one 3-D TMA box per sub-chunk for all W sources
     int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
+    int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
     int startup_gather;                // all_gather_matmul: the TMA producer copies the gathers claimed
                                        // before its CTA's first GEMM item (TMA boxes through its idle stages)
     int gather_box;                    // ... columns per box
@@ -711,6 +712,7 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
     uint32_t issued_phase[STAGES];
     uint32_t used_mask = 0;
     const bool reduce_op = (p.op == OP_MM_RS || p.op == OP_MM_AR);
+    const uint64_t pol = p.gemm_evict_last ? l2_policy_evict_last() : 0ull;
 
     auto load_gemm = [&](uint32_t g) -> bool {
         const GemmCoord gc = decode_gemm(p, g);
@@ -779,23 +781,37 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 const uint32_t fb = mapa_shared(&sm.full[stage], 0);
                 // A: the stage's KS K-chunks of this CTA's 128 rows, 16 KB apart
                 if (p.a_chunked) {
-                    tma_load_4d_pair(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb);
+                    if (p.gemm_evict_last) tma_load_4d_pair_hint(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb, pol);
+                    else tma_load_4d_pair(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < KS; ++j)
-                        tma_load_3d_pair(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row, a_rank,
-                                         fb);
+                    for (int j = 0; j < KS; ++j) {
+                        if (p.gemm_evict_last)
+                            tma_load_3d_pair_hint(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row,
+                                                  a_rank, fb, pol);
+                        else
+                            tma_load_3d_pair(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row,
+                                             a_rank, fb);
+                    }
                 }
                 // B: 64-column chunks of KS x 64 K rows, 64 KS x 128 B apart
                 const int bcol = gc.nb * BN + (hn ? gc.hn * (BN / 2) + ctl.half * (BN / 4) : ctl.half * (BN / CG));
                 if (p.b_chunked && !hn) {
                     // the CTA's BN / CG columns as one box of 64-column chunks
-                    tma_load_4d_pair(sm.b_tile(stage), &p.tmBc, 0, kb * BK, bcol / 64, b_rank, fb);
+                    if (p.gemm_evict_last)
+                        tma_load_4d_pair_hint(sm.b_tile(stage), &p.tmBc, 0, kb * BK, bcol / 64, b_rank, fb, pol);
+                    else
+                        tma_load_4d_pair(sm.b_tile(stage), &p.tmBc, 0, kb * BK, bcol / 64, b_rank, fb);
                 } else {
                     const int nbox = hn ? BN / 4 / 64 : BN / CG / 64;
-                    for (int c = 0; c < nbox; ++c)
-                        tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * KS * 2), &p.tmB, bcol + c * 64, kb * BK,
-                                         b_rank, fb);
+                    for (int c = 0; c < nbox; ++c) {
+                        if (p.gemm_evict_last)
+                            tma_load_3d_pair_hint(sm.b_tile(stage) + c * (64 * BK * KS * 2), &p.tmB, bcol + c * 64,
+                                                  kb * BK, b_rank, fb, pol);
+                        else
+                            tma_load_3d_pair(sm.b_tile(stage) + c * (64 * BK * KS * 2), &p.tmB, bcol + c * 64, kb * BK,
+                                             b_rank, fb);
+                    }
                 }
             }
             issued_phase[stage] = phase;

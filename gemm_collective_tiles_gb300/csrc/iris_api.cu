@@ -168,6 +168,7 @@ struct Cfg {
     int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 one box of all sources
     int gather_parts;    // all_gather_matmul: gather items per (row block, shard)
     int startup_gather;  // all_gather_matmul: 1 = worker copies, 2 = the TMA producer copies start-up gathers
+    int gemm_evict_last; // CTA-pair operand loads with an L2 evict-last policy
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -223,6 +224,11 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     // parts measured slower on every shape tried (more claims contending on
     // the comm queue counter and more per-item synchronisation)
     out.gather_parts = c->gather_parts ? c->gather_parts : 1;
+    // CTA-pair operand loads evict last by default: they then keep their
+    // place in the L2 against the outputs, partial sums and collective data
+    // streaming through it (measured 0.7-1.4 % faster on all four fused ops)
+    if (c->gemm_l2_hint < 0 || c->gemm_l2_hint > 2) return IRIS_EINVAL;
+    out.gemm_evict_last = c->gemm_l2_hint == 2 ? 0 : 1;
     if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
     out.startup_gather = c->startup_gather ? c->startup_gather : 1;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
@@ -470,6 +476,7 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.coll_ring = c.coll_ring;
     p.coll_evict_first = c.coll_evict_first;
     p.coll_path = c.coll_path;
+    p.gemm_evict_last = c.gemm_evict_last;
 }
 
 int launch(Params& p, const Cfg& c, cudaStream_t stream) {
@@ -662,6 +669,10 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     if (K % 8 != 0 || N % 8 != 0 || N_l % 8 != 0) return IRIS_EALIGN;
     Cfg c;
     if ((rc = resolve_cfg(cfg, op, N, c))) return rc;
+    // a rank's A larger than 64 MB: swizzle groups of 16 blocks, so a group's
+    // A panels stay in L2 while its B streams (8192^3 W=8: 4.81 against
+    // 4.86 ms; 4096^3 W=4 keeps 32)
+    if ((!cfg || cfg->group_m == 0) && size_t(M) * size_t(K) * 2 > (size_t(64) << 20)) c.group_m = 16;
     c.reduce_mode = resolve_reduce_mode(cfg, op, N, W);
     if (c.reduce_mode < 0) return IRIS_EINVAL;
     if ((rc = resolve_pair(c, op))) return rc;

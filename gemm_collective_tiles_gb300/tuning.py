@@ -27,7 +27,7 @@ ENV_CACHE = "IRIS_B200_CACHE"
 # knobs a cached entry may set (the rest stay at their defaults)
 TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block", "stages",
            "coll_ring", "coll_l2_hint", "coll_path", "gather_parts",
-           "startup_gather")
+           "startup_gather", "gemm_l2_hint")
 
 # nearest-shape matching: largest accepted distance, in log2 units over the
 # problem sizes (1.0 = one size off by a factor of 2, or two by 2^0.7 each)
@@ -161,9 +161,13 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     # the CTA-pair pipeline the default does not pick for this K (three
     # 128-deep stages up to K = 98304, six 64-deep stages beyond)
     out.append({"stages": 3 if K > 98304 else 6})
-    # the swizzle widths the default does not use (32; 16 in the concurrent mode)
-    for gm in ((32, 8, 64) if op == "concurrent" else (64, 16, 8)):
-        out.append({"group_m": gm})
+    # the swizzle widths the default does not use (32; 16 in the concurrent
+    # mode and for the reduce ops when a rank's A exceeds 64 MB)
+    reduce = op in ("matmul_reduce_scatter", "matmul_all_reduce")
+    default_gm = 16 if op == "concurrent" or (reduce and M * K * 2 > (64 << 20)) else 32
+    for gm in (64, 32, 16, 8):
+        if gm != default_gm:
+            out.append({"group_m": gm})
     pair_tiles = -(-M // 256) * -(-N // 256) * (W if op in ("matmul_reduce_scatter", "matmul_all_reduce") else 1)
     pairs = max(1, sm_count // 2)
     if pair_tiles % pairs and pair_tiles % pairs <= pairs // 2 or pair_tiles < pairs:

@@ -106,7 +106,8 @@ typedef struct {
                               K block, or two in the three-stage CTA-pair
                               pipeline (see stages) */
     int group_m;           /* GROUP_M tile swizzle width in 128-row M blocks
-                              (default 32; 16 in the concurrent mode) */
+                              (default 32; 16 in the concurrent mode and for
+                              the reduce ops when a rank's A exceeds 64 MB) */
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
                               other queue when its own runs dry.  0 = op default
@@ -192,6 +193,11 @@ typedef struct {
                               with TMA boxes through its still idle pipeline
                               stages (whole 128-row blocks: needs
                               gather_parts 1, else the workers copy). */
+    int gemm_l2_hint;      /* L2 policy of the GEMM operand loads of CTA-pair
+                              tiles: 0 = default (evict last), 1 = evict last
+                              (the operands keep their place in the L2 against
+                              the outputs, partial sums and collective data
+                              streaming through it), 2 = none. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

@@ -414,3 +414,45 @@ def test_ag_mm_startup_gather_stopped_then_exact():
     outs = good.outputs()
     assert_exact(bits(outs["gathered"]), want_g)
     assert_exact(bits(outs["out"][0]), want_out)
+
+
+@pytest.mark.parametrize("op", ["ag_mm", "mm_rs", "mm_ag"])
+def test_gemm_operands_without_l2_policy_exact(op):
+    """CTA-pair operand loads without the default L2 evict-last policy
+    (every other test runs with it): outputs stay exact on integer inputs."""
+    W, M, N, K = 4, 520, 512, 256
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=105, dist="int", scale=2, bias=True,
+                                    bias_scale=2)
+    prob = FusedProblem(op, W, M, N, K, "bf16", bias=True, config={"gemm_l2_hint": 2})
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    outs = prob.outputs()
+    if op == "ag_mm":
+        want = [oracle.all_gather_matmul(x.A, x.B[0], x.bias)[0]]
+    elif op == "mm_ag":
+        want = [oracle.matmul_all_gather(x.A, x.B[0], x.bias)]
+    else:
+        want = oracle.matmul_reduce_scatter(x.A, x.B, x.bias)
+    for r, w in enumerate(want):
+        assert_exact(bits(outs["out"][r]), w)
+
+
+def test_concurrent_gemm_evict_last_exact():
+    from gemm_collective_tiles_gb300.runner import ConcurrentProblem
+    W, count = 8, 2 * 16384 + 2048
+    M, N, K = 520, 768, 256
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=106, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=107)
+    prob = ConcurrentProblem(M, N, K, "bf16", "all_reduce", W, count,
+                             config={"gemm_l2_hint": 1, "coll_l2_hint": 1, "comm_block": 16384, "gemm_ctas": 60})
+    prob.upload(A, B, X)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    out = prob.outputs()
+    assert_exact(bits(out["C"]), oracle.gemm(A, B))
+    want = oracle.all_reduce(X)
+    for r in range(W):
+        assert np.array_equal(out["x"][r].numpy().view(np.uint32), want.view(np.uint32))
