@@ -73,6 +73,7 @@ class iris_b200_config(ctypes.Structure):
         ("gather_parts", ctypes.c_int),
         ("startup_gather", ctypes.c_int),
         ("gemm_l2_hint", ctypes.c_int),
+        ("out_l2_hint", ctypes.c_int),
     ]
 
 

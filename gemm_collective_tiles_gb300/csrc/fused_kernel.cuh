@@ -148,6 +148,7 @@ struct Params {
     int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
+    int out_evict_first;               // final 16-bit output stores carry an L2 evict-first policy
     int startup_gather;                // all_gather_matmul: the TMA producer copies the gathers claimed
                                        // before its CTA's first GEMM item (TMA boxes through its idle stages)
     int gather_box;                    // ... columns per box
@@ -1211,6 +1212,9 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
         c_blk = 0;
         if (p.replicate && p.op == OP_AG_MM) c_reg_hi = p.W;
     }
+    // final 16-bit outputs are not read again: evict first (fp32 partials are)
+    const bool out_hint = p.out_evict_first && !reduce_op;
+    const uint64_t opol = out_hint ? l2_policy_evict_first() : 0ull;
     uint32_t ci = 0;
 #pragma unroll 1
     for (int cc = 0; cc < cols_end; cc += 32, ++ci) {
@@ -1275,7 +1279,11 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
         fence_proxy_async_shared();
         __syncwarp();
         if (wc.lane == 0) {
-            for (int rg = c_reg_lo; rg < c_reg_hi; ++rg) tma_store_4d(&p.tmC, stg, col0, c_row, c_blk, rg);
+            if (out_hint) {
+                for (int rg = c_reg_lo; rg < c_reg_hi; ++rg) tma_store_4d_hint(&p.tmC, stg, col0, c_row, c_blk, rg, opol);
+            } else {
+                for (int rg = c_reg_lo; rg < c_reg_hi; ++rg) tma_store_4d(&p.tmC, stg, col0, c_row, c_blk, rg);
+            }
             bulk_commit();
         }
     }
@@ -1466,10 +1474,16 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
                 tma_reduce_add_4d(&p.tmS, stg, col0, c_row, 0, 0);  // S += P_s
             } else if (p.op == OP_MM_RS) {
                 const int rr = col0 / p.N_local;
-                tma_store_4d(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0);
+                if (p.out_evict_first)
+                    tma_store_4d_hint(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0, l2_policy_evict_first());
+                else
+                    tma_store_4d(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0);
             } else {
                 const int nreg = p.replicate ? p.W : 1;
-                for (int rg = 0; rg < nreg; ++rg) tma_store_4d(&p.tmC, stg, col0, c_row, 0, rg);
+                for (int rg = 0; rg < nreg; ++rg) {
+                    if (p.out_evict_first) tma_store_4d_hint(&p.tmC, stg, col0, c_row, 0, rg, l2_policy_evict_first());
+                    else tma_store_4d(&p.tmC, stg, col0, c_row, 0, rg);
+                }
             }
             bulk_commit();
         }

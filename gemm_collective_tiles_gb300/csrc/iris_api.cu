@@ -169,6 +169,7 @@ struct Cfg {
     int gather_parts;    // all_gather_matmul: gather items per (row block, shard)
     int startup_gather;  // all_gather_matmul: 1 = worker copies, 2 = the TMA producer copies start-up gathers
     int gemm_evict_last; // CTA-pair operand loads with an L2 evict-last policy
+    int out_evict_first; // final 16-bit output stores with an L2 evict-first policy
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -229,6 +230,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     // streaming through it (measured 0.7-1.4 % faster on all four fused ops)
     if (c->gemm_l2_hint < 0 || c->gemm_l2_hint > 2) return IRIS_EINVAL;
     out.gemm_evict_last = c->gemm_l2_hint == 2 ? 0 : 1;
+    if (c->out_l2_hint < 0 || c->out_l2_hint > 2) return IRIS_EINVAL;
+    out.out_evict_first = c->out_l2_hint == 1 ? 1 : 0;
     if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
     out.startup_gather = c->startup_gather ? c->startup_gather : 1;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
@@ -477,6 +480,7 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.coll_evict_first = c.coll_evict_first;
     p.coll_path = c.coll_path;
     p.gemm_evict_last = c.gemm_evict_last;
+    p.out_evict_first = c.out_evict_first;
 }
 
 int launch(Params& p, const Cfg& c, cudaStream_t stream) {

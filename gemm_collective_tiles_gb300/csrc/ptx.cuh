@@ -222,6 +222,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
                  : "memory");
 }
 
+// the same with an L2 cache policy operand
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* m, const void* smem_src, int c0, int c1, int c2,
+                                                  int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4}], [%5], %6;" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src)), "l"(policy)
+        : "memory");
+}
+
 // 4-D tiled store of one box from shared memory (bulk-group completion)
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* smem_src, int c0, int c1,
                                              int c2, int c3) {

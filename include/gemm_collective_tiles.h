@@ -198,6 +198,9 @@ typedef struct {
                               (the operands keep their place in the L2 against
                               the outputs, partial sums and collective data
                               streaming through it), 2 = none. */
+    int out_l2_hint;       /* L2 policy of the final 16-bit output stores:
+                              0 = default (none), 1 = evict first (outputs are
+                              not read again), 2 = none. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

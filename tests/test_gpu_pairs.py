@@ -416,14 +416,16 @@ def test_ag_mm_startup_gather_stopped_then_exact():
     assert_exact(bits(outs["out"][0]), want_out)
 
 
-@pytest.mark.parametrize("op", ["ag_mm", "mm_rs", "mm_ag"])
-def test_gemm_operands_without_l2_policy_exact(op):
-    """CTA-pair operand loads without the default L2 evict-last policy
-    (every other test runs with it): outputs stay exact on integer inputs."""
+@pytest.mark.parametrize("op", ["ag_mm", "mm_rs", "mm_ag", "mm_ar"])
+@pytest.mark.parametrize("hints", [{"gemm_l2_hint": 2}, {"out_l2_hint": 1}])
+def test_gemm_l2_policies_exact(op, hints):
+    """CTA-pair operand loads without the default L2 evict-last policy, or
+    final output stores with an evict-first policy, change only the cache
+    state: outputs stay exact on integer inputs."""
     W, M, N, K = 4, 520, 512, 256
     x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=105, dist="int", scale=2, bias=True,
                                     bias_scale=2)
-    prob = FusedProblem(op, W, M, N, K, "bf16", bias=True, config={"gemm_l2_hint": 2})
+    prob = FusedProblem(op, W, M, N, K, "bf16", bias=True, config=hints)
     prob.upload(x.A, x.B, x.bias)
     prob.poison_outputs()
     prob.run()
@@ -433,6 +435,8 @@ def test_gemm_operands_without_l2_policy_exact(op):
         want = [oracle.all_gather_matmul(x.A, x.B[0], x.bias)[0]]
     elif op == "mm_ag":
         want = [oracle.matmul_all_gather(x.A, x.B[0], x.bias)]
+    elif op == "mm_ar":
+        want = [oracle.matmul_all_reduce(x.A, x.B, x.bias)]
     else:
         want = oracle.matmul_reduce_scatter(x.A, x.B, x.bias)
     for r, w in enumerate(want):
