@@ -2,9 +2,10 @@
 
     python -m gemm_collective_tiles_gb300.profile_ops WORKLOAD [LAUNCHES]
 
-WORKLOAD is a fused-op workload name of ``synthetic.WORKLOADS`` or
-``concurrent_ar_w8``; inputs are drawn as the benchmark draws them.  Used by
-the profiling commands recorded under ``profiles/``.
+WORKLOAD is a fused-op workload name of ``synthetic.WORKLOADS``,
+``concurrent_ar_w8`` or ``gemm_bf16_8192`` (the concurrent workload's GEMM
+alone); inputs are drawn as the benchmark draws them.  Used by the profiling
+commands recorded under ``profiles/``.
 """
 from __future__ import annotations
 
@@ -23,13 +24,14 @@ def main(argv):
     name = argv[0]
     launches = int(argv[1]) if len(argv) > 1 else 6
     torch.cuda.set_device(0)
-    if name == "concurrent_ar_w8":
+    if name in ("concurrent_ar_w8", "gemm_bf16_8192"):
         cw = synthetic.CONCURRENT_WORKLOAD
+        coll = name == "concurrent_ar_w8"
         A, B = synthetic.make_gemm_inputs(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], cw["gemm_seed"],
                                           dist="normal", scale=1.0)
-        X = synthetic.make_coll_inputs(cw["W"], cw["count"], cw["coll_dtype"], cw["coll_seed"])
-        prob = ConcurrentProblem(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], "all_reduce", cw["W"], cw["count"],
-                                 coll_dtype=cw["coll_dtype"])
+        X = synthetic.make_coll_inputs(cw["W"], cw["count"], cw["coll_dtype"], cw["coll_seed"]) if coll else None
+        prob = ConcurrentProblem(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], "all_reduce", cw["W"],
+                                 cw["count"] if coll else 0, coll_dtype=cw["coll_dtype"])
         prob.upload(A, B, X)
     else:
         wl = synthetic.WORKLOADS[name]
