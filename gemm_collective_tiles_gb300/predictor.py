@@ -11,8 +11,8 @@ rank (2W transfers per tile), so they need the most CTAs to saturate memory;
 the other collectives move fewer bytes per tile.
 
 Constants are calibrated on GB300 measurements of this library (the GEMM and
-the all-reduce of the concurrent path, each timed alone on 8 to 152 CTAs);
-they can be replaced by the caller.
+the all-reduce of the concurrent path, each timed alone on 38 to 152 CTAs,
+and the GEMM's DRAM bytes under ncu); they can be replaced by the caller.
 
 The GEMM tile is ranked together with the split (PR #544 review excerpt of
 predict_split: tile candidates, a preferred tile and a margin): each tile
@@ -34,9 +34,11 @@ from typing import Dict, List, Optional, Sequence
 class Machine:
     sms: int = 152
     gemm_tflops_per_sm: float = 11.3      # CTA-pair GEMM 8192^3 bf16 (six-stage pipeline) over 152 SMs
-    comm_gbs_per_sm: float = 61.0         # one CTA's collective engine, reads + writes (all-reduce on 38 CTAs)
-    hbm_gbs: float = 5500.0               # reads + writes the all-reduce reaches alone on every SM
+    comm_gbs_per_sm: float = 78.0         # one CTA's collective engine, reads + writes (all-reduce, one box
+                                          # of all sources per sub-chunk, on 38 CTAs)
+    hbm_gbs: float = 6100.0               # reads + writes the all-reduce reaches alone on every SM
     gemm_hbm_share: float = 0.12          # HBM fraction the GEMM operands use when all SMs run it
+    gemm_dram_bytes_per_flop: float = 1.27e-3  # the GEMM's DRAM reads per flop (8192^3 alone: 1.4 GB)
     tile_overhead_us: float = 1.0         # claim + pipeline fill per tile
 
 
@@ -121,20 +123,27 @@ def simulate(wl: Workload, gemm_ctas: int, m: Optional[Machine] = None, tile: Op
     machine's per-SM rate.  With a TileKind, the workers are its units (a CTA
     pair computes one tile and runs each collective tile on both CTAs), a
     unit prefers the GEMM when its first CTA is below gemm_ctas, and a unit
-    that turns from GEMM to collective work first drains its pipeline."""
+    that turns from GEMM to collective work first drains its pipeline.
+
+    Both jobs draw on HBM: a collective tile moves its bytes at its engine's
+    rate, capped by the bandwidth the GEMM leaves; a GEMM tile takes the
+    longer of its tensor time and the time to read its DRAM bytes from what
+    the running collective tiles leave, shared by the running GEMM tiles."""
     m = m or Machine()
     ctas = tile.ctas if tile else 1
     units = max(1, m.sms // ctas)
     gemm_ctas = max(0, min(m.sms, gemm_ctas))
     if tile:
         tiles = math.ceil(wl.M / tile.tile_m) * math.ceil(wl.N / tile.tile_n) if wl.M and wl.N else 0
-        t_gemm = 2.0 * tile.tile_m * tile.tile_n * wl.K / (tile.gemm_tflops_per_cta * ctas * 1e12) * 1e6
+        tile_flops = 2.0 * tile.tile_m * tile.tile_n * wl.K
+        t_flop = tile_flops / (tile.gemm_tflops_per_cta * ctas * 1e12) * 1e6
         lease = tile.lease_us
     else:
         tiles = wl.gemm_tiles() if wl.M and wl.N else 0
-        t_gemm = wl.gemm_tile_flops() / (m.gemm_tflops_per_sm * 1e12) * 1e6
+        tile_flops = wl.gemm_tile_flops()
+        t_flop = tile_flops / (m.gemm_tflops_per_sm * 1e12) * 1e6
         lease = 0.0
-    t_gemm += m.tile_overhead_us
+    tile_dram = tile_flops * m.gemm_dram_bytes_per_flop
     n_g, n_c = tiles, wl.comm_tiles()
     bytes_c = wl.comm_tile_bytes()
     # event queue of (time free, unit); greedy claims in time order
@@ -143,19 +152,24 @@ def simulate(wl: Workload, gemm_ctas: int, m: Optional[Machine] = None, tile: Op
     last_gemm = [False] * units
     g_next = c_next = 0
     active_comm: List[float] = []   # end times of collective tiles in flight
+    active_gemm: List[float] = []   # end times of GEMM tiles in flight
     end = 0.0
     while g_next < n_g or c_next < n_c:
         t, u = heapq.heappop(free)
+        active_comm = [x for x in active_comm if x > t]
+        active_gemm = [x for x in active_gemm if x > t]
         prefer_gemm = u * ctas < gemm_ctas
         take_gemm = (prefer_gemm and g_next < n_g) or (not prefer_gemm and c_next >= n_c)
         if take_gemm:
             g_next += 1
-            done = t + t_gemm
+            comm_demand = len(active_comm) * m.comm_gbs_per_sm * ctas
+            bw = max(1.0, (m.hbm_gbs - min(comm_demand, 0.9 * m.hbm_gbs)) / (len(active_gemm) + 1))
+            done = t + max(t_flop, tile_dram / (bw * 1e9) * 1e6) + m.tile_overhead_us
+            active_gemm.append(done)
         else:
             c_next += 1
-            active_comm = [x for x in active_comm if x > t]
             running = len(active_comm) + 1
-            gemm_running = min(gemm_ctas // ctas, units - running) if g_next < n_g else 0
+            gemm_running = min(len(active_gemm), units - running) if g_next < n_g else len(active_gemm)
             hbm_left = m.hbm_gbs * (1.0 - m.gemm_hbm_share * gemm_running / units)
             bw = min(m.comm_gbs_per_sm * ctas, hbm_left / running)
             done = t + bytes_c / (bw * 1e9) * 1e6 + m.tile_overhead_us + (lease if last_gemm[u] else 0.0)

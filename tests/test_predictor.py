@@ -97,3 +97,26 @@ def test_pair_tile_simulation_matches_closed_form():
     wl = P.Workload(M=256 * 4, N=256 * 7, K=2048, count=0)                  # 28 tiles on 10 pairs
     t_tile = 2 * 256 * 256 * 2048 / (10.0 * 2 * 1e12) * 1e6
     assert P.simulate(wl, 20, m, tk) == pytest.approx(3 * t_tile)
+
+
+def test_ranking_against_measured_sweeps():
+    """The default machine constants (all measured) rank the recorded
+    gemm_ctas sweeps of the concurrent workload: the predicted best split is
+    the measured best in every sweep, and the rank correlation over the
+    eight points is high."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "concurrent_sweeps.json")))
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    tk = next(t for t in P.TILE_KINDS if t.name == P.PREFERRED_TILE)
+    keys = sorted(g["sweeps"][0])
+    pred = {k: P.simulate(wl, int(k), P.Machine(), tk) for k in keys}
+
+    def ranks(d):
+        return {k: i for i, k in enumerate(sorted(keys, key=lambda k: d[k]))}
+    for sweep in g["sweeps"]:
+        assert min(pred, key=pred.get) == min(sweep, key=sweep.get)
+        rp, rm = ranks(pred), ranks(sweep)
+        n = len(keys)
+        rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
+        assert rho >= 0.8, rho
