@@ -74,6 +74,7 @@ class iris_b200_config(ctypes.Structure):
         ("startup_gather", ctypes.c_int),
         ("gemm_l2_hint", ctypes.c_int),
         ("out_l2_hint", ctypes.c_int),
+        ("sum_l2_hint", ctypes.c_int),
     ]
 
 

@@ -149,6 +149,8 @@ struct Params {
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
     int out_evict_first;               // final 16-bit output stores carry an L2 evict-first policy
+    int sum_l2_policy;                 // chained reduce running-sum stores / reduce-adds: 0 none,
+                                       // 1 evict first, 2 evict last
     int startup_gather;                // all_gather_matmul: the TMA producer copies the gathers claimed
                                        // before its CTA's first GEMM item (TMA boxes through its idle stages)
     int gather_box;                    // ... columns per box
@@ -1388,6 +1390,9 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     // only the last rank reads the running sum: the middle ranks add their
     // partial into it at the L2 (TMA reduce-add), in the same rank order
     const bool reads_sum = last && s > 0;
+    const uint64_t spol = p.sum_l2_policy == 1   ? l2_policy_evict_first()
+                          : p.sum_l2_policy == 2 ? l2_policy_evict_last()
+                                                 : 0ull;
     if (reads_sum && nch > 0 && wc.lane == 0) issue_load(0);
 #pragma unroll 1
     for (int ci = 0; ci < nch; ++ci) {
@@ -1469,9 +1474,11 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         __syncwarp();
         if (wc.lane == 0) {
             if (!last && s == 0) {
-                tma_store_4d(&p.tmS, stg, col0, c_row, 0, 0);
+                if (p.sum_l2_policy) tma_store_4d_hint(&p.tmS, stg, col0, c_row, 0, 0, spol);
+                else tma_store_4d(&p.tmS, stg, col0, c_row, 0, 0);
             } else if (!last) {
-                tma_reduce_add_4d(&p.tmS, stg, col0, c_row, 0, 0);  // S += P_s
+                if (p.sum_l2_policy) tma_reduce_add_4d_hint(&p.tmS, stg, col0, c_row, 0, 0, spol);  // S += P_s
+                else tma_reduce_add_4d(&p.tmS, stg, col0, c_row, 0, 0);  // S += P_s
             } else if (p.op == OP_MM_RS) {
                 const int rr = col0 / p.N_local;
                 if (p.out_evict_first)

@@ -170,6 +170,7 @@ struct Cfg {
     int startup_gather;  // all_gather_matmul: 1 = worker copies, 2 = the TMA producer copies start-up gathers
     int gemm_evict_last; // CTA-pair operand loads with an L2 evict-last policy
     int out_evict_first; // final 16-bit output stores with an L2 evict-first policy
+    int sum_l2_policy;   // chained reduce running sum: 0 none, 1 evict first, 2 evict last
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -230,6 +231,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     // streaming through it (measured 0.7-1.4 % faster on all four fused ops)
     if (c->gemm_l2_hint < 0 || c->gemm_l2_hint > 2) return IRIS_EINVAL;
     out.gemm_evict_last = c->gemm_l2_hint == 2 ? 0 : 1;
+    if (c->sum_l2_hint < 0 || c->sum_l2_hint > 3) return IRIS_EINVAL;
+    out.sum_l2_policy = c->sum_l2_hint == 1 ? 1 : c->sum_l2_hint == 2 ? 2 : 0;
     if (c->out_l2_hint < 0 || c->out_l2_hint > 2) return IRIS_EINVAL;
     out.out_evict_first = c->out_l2_hint == 1 ? 1 : 0;
     if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
@@ -481,6 +484,7 @@ void fill_geometry(Params& p, int64_t M_rows, int64_t N, int64_t K, int m_blocks
     p.coll_path = c.coll_path;
     p.gemm_evict_last = c.gemm_evict_last;
     p.out_evict_first = c.out_evict_first;
+    p.sum_l2_policy = c.sum_l2_policy;
 }
 
 int launch(Params& p, const Cfg& c, cudaStream_t stream) {

@@ -251,6 +251,15 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, const vo
         "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src))
         : "memory");
 }
+// the reduce-add with an L2 cache policy operand
+__device__ __forceinline__ void tma_reduce_add_4d_hint(const CUtensorMap* m, const void* smem_src, int c0, int c1,
+                                                       int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4}], [%5], %6;" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src)), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until every committed bulk store has finished READING shared memory
 __device__ __forceinline__ void bulk_wait_read_all() {

@@ -27,7 +27,8 @@ ENV_CACHE = "IRIS_B200_CACHE"
 # knobs a cached entry may set (the rest stay at their defaults)
 TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block", "stages",
            "coll_ring", "coll_l2_hint", "coll_path", "gather_parts",
-           "startup_gather", "gemm_l2_hint", "out_l2_hint")
+           "startup_gather", "gemm_l2_hint", "out_l2_hint",
+           "sum_l2_hint")
 
 # nearest-shape matching: largest accepted distance, in log2 units over the
 # problem sizes (1.0 = one size off by a factor of 2, or two by 2^0.7 each)

@@ -201,6 +201,10 @@ typedef struct {
     int out_l2_hint;       /* L2 policy of the final 16-bit output stores:
                               0 = default (none), 1 = evict first (outputs are
                               not read again), 2 = none. */
+    int sum_l2_hint;       /* reduce ops, chained schedule: L2 policy of the
+                              fp32 running-sum stores and reduce-adds.  0 =
+                              default (none), 1 = evict first, 2 = evict last,
+                              3 = none. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

@@ -417,11 +417,12 @@ def test_ag_mm_startup_gather_stopped_then_exact():
 
 
 @pytest.mark.parametrize("op", ["ag_mm", "mm_rs", "mm_ag", "mm_ar"])
-@pytest.mark.parametrize("hints", [{"gemm_l2_hint": 2}, {"out_l2_hint": 1}])
+@pytest.mark.parametrize("hints", [{"gemm_l2_hint": 2}, {"out_l2_hint": 1}, {"sum_l2_hint": 1}, {"sum_l2_hint": 2}])
 def test_gemm_l2_policies_exact(op, hints):
-    """CTA-pair operand loads without the default L2 evict-last policy, or
-    final output stores with an evict-first policy, change only the cache
-    state: outputs stay exact on integer inputs."""
+    """CTA-pair operand loads without the default L2 evict-last policy,
+    final output stores with an evict-first policy, or running-sum stores
+    and reduce-adds with either policy change only the cache state: outputs
+    stay exact on integer inputs."""
     W, M, N, K = 4, 520, 512, 256
     x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=105, dist="int", scale=2, bias=True,
                                     bias_scale=2)
