@@ -53,3 +53,16 @@ def test_single_process_identity():
     import bench
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.job_throughput(1e12, 1, 10, 10.0) == pytest.approx(1000.0)
+
+
+def test_reference_and_gpu_arms_describe_the_same_workload():
+    """bench.py's two arms build their `config` object with one function, so
+    the reference line and the GPU line name the same workload."""
+    import bench
+    import synthetic
+    wl = dict(synthetic.WORKLOADS[bench.DEFAULT_WORKLOAD])
+    a = bench.bench_config(wl, bench.DEFAULT_WORKLOAD, {}, 1)
+    b = bench.bench_config(wl, bench.DEFAULT_WORKLOAD, {}, 1)
+    assert a == b and a["workload"].startswith("matmul_reduce_scatter W=4 M=4096 N=4096 K=4096 f16")
+    assert {"l2", "parallelism", "op", "M", "N", "K", "seed", "dist"} <= set(a)
+    assert bench.bench_config(wl, bench.DEFAULT_WORKLOAD, {}, 2)["parallelism"] == "replicas x2"
