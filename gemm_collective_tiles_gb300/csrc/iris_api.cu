@@ -853,10 +853,6 @@ static int concurrent_impl(const void* A, const void* B, void* C, int64_t M, int
     }
     const bool launch_gemm = has_gemm && part != 2;
     if ((rc = resolve_pair(c, IRIS_OP_CONCURRENT, launch_gemm))) return rc;
-    // beside a collective the GEMM lends its stages to collective tiles:
-    // six smaller stages drain sooner for each lease (measured 3 % faster
-    // steps than three, though the GEMM alone is faster with three)
-    if (count > 0 && c.cg == 2 && c.stages == 0) c.stages = STAGES_PAIR_STREAM;
     resolve_stages(c, K);
     if (count > 0) {
         if (size_t(c.comm_block) * esz % 16 != 0) return IRIS_EALIGN;

@@ -33,7 +33,7 @@ from typing import Dict, List, Optional, Sequence
 @dataclasses.dataclass
 class Machine:
     sms: int = 152
-    gemm_tflops_per_sm: float = 11.3      # CTA-pair GEMM 8192^3 bf16 (six-stage pipeline) over 152 SMs
+    gemm_tflops_per_sm: float = 11.91     # CTA-pair GEMM 8192^3 bf16 (three-stage pipeline) over 152 SMs
     comm_gbs_per_sm: float = 78.0         # one CTA's collective engine, reads + writes (all-reduce, one box
                                           # of all sources per sub-chunk, on 38 CTAs)
     hbm_gbs: float = 6100.0               # reads + writes the all-reduce reaches alone on every SM
@@ -64,7 +64,7 @@ TILE_KINDS = (
     TileKind("pair3", 256, 256, 2, 11.91, 1.33, {"tile_m": 256, "stages": 3}),
     TileKind("cta128", 128, 256, 1, 10.43, 1.0, {"tile_m": 128}),
 )
-PREFERRED_TILE = "pair6"   # the library's default beside a collective
+PREFERRED_TILE = "pair3"   # the library's default, beside a collective too
 
 
 @dataclasses.dataclass

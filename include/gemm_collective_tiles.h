@@ -119,10 +119,8 @@ typedef struct {
                               (one A and one B TMA box per stage), or, when
                               K > 98304 and the operands stream from DRAM, 6
                               stages of one K block (more, smaller loads in
-                              flight); the concurrent mode with a collective
-                              also takes 6 by default (its stages are lent to
-                              collective tiles and smaller ones drain sooner);
-                              3 or 6 choose.  Other values, or a nonzero value
+                              flight), in every mode, the concurrent one with
+                              a collective included; 3 or 6 choose.  Other values, or a nonzero value
                               with one-CTA tiles: IRIS_EINVAL. */
     int comm_block;        /* concurrent mode: elements per comm tile (default 65536) */
     int replicate_outputs; /* 1: also write the W-1 identical copies of replicated

@@ -101,22 +101,24 @@ def test_pair_tile_simulation_matches_closed_form():
 
 def test_ranking_against_measured_sweeps():
     """The default machine constants (all measured) rank the recorded
-    gemm_ctas sweeps of the concurrent workload: the predicted best split is
-    the measured best in every sweep, and the rank correlation over the
-    eight points is high."""
+    gemm_ctas sweeps of the concurrent workload, each with the tile kind of
+    the pipeline it ran (six- and three-stage CTA pairs): the predicted best
+    split is the measured best in every sweep, and the rank correlation over
+    the eight points is high."""
     import json
     import os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "concurrent_sweeps.json")))
     wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
-    tk = next(t for t in P.TILE_KINDS if t.name == P.PREFERRED_TILE)
-    keys = sorted(g["sweeps"][0])
-    pred = {k: P.simulate(wl, int(k), P.Machine(), tk) for k in keys}
+    for tile, sweeps in (("pair6", g["sweeps"]), ("pair3", g["three_stage"]["sweeps"])):
+        tk = next(t for t in P.TILE_KINDS if t.name == tile)
+        keys = sorted(sweeps[0])
+        pred = {k: P.simulate(wl, int(k), P.Machine(), tk) for k in keys}
 
-    def ranks(d):
-        return {k: i for i, k in enumerate(sorted(keys, key=lambda k: d[k]))}
-    for sweep in g["sweeps"]:
-        assert min(pred, key=pred.get) == min(sweep, key=sweep.get)
-        rp, rm = ranks(pred), ranks(sweep)
-        n = len(keys)
-        rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
-        assert rho >= 0.8, rho
+        def ranks(d):
+            return {k: i for i, k in enumerate(sorted(keys, key=lambda k: d[k]))}
+        for sweep in sweeps:
+            assert min(pred, key=pred.get) == min(sweep, key=sweep.get), tile
+            rp, rm = ranks(pred), ranks(sweep)
+            n = len(keys)
+            rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
+            assert rho >= 0.8, (tile, rho)
