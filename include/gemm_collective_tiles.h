@@ -126,7 +126,10 @@ typedef struct {
     int replicate_outputs; /* 1: also write the W-1 identical copies of replicated
                               outputs into the other heap regions */
     int bias_on_m;         /* 1: bias has one entry per output row (length M) */
-    int grid;              /* persistent CTAs (default: one per SM) */
+    int grid;              /* persistent CTAs (default: one per SM).  A dependent
+                              op with fewer work items (GEMM tiles, gathers,
+                              reduce parts) than CTAs (pairs) launches one CTA
+                              (pair) per item instead. */
     unsigned long long wait_ns; /* limit of every device-side wait (default 2e9 ns) */
     int debug_skip_flag;   /* test hook: 0 = off; k > 0 makes the kernel never
                               release ready-flag k-1, so the tile waiting on it

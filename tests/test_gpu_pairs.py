@@ -461,3 +461,23 @@ def test_concurrent_gemm_evict_last_exact():
     want = oracle.all_reduce(X)
     for r in range(W):
         assert np.array_equal(out["x"][r].numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("op,W,M,N,K", [("ag_mm", 2, 256, 256, 256), ("mm_rs", 2, 256, 512, 128),
+                                        ("mm_ag", 2, 2 * 128, 256, 64), ("mm_ar", 2, 300, 256, 64)])
+def test_small_problem_runs_one_pair_per_item(op, W, M, N, K):
+    """A launch with fewer work items than CTA pairs starts one pair per item
+    (the kernel-entry events of the device timeline count the CTAs that ran),
+    and the result is exact."""
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "f16", seed=2500 + M + N, dist="int", scale=2,
+                                    bias=True, bias_scale=3)
+    want, want_g = oracle_outputs(x)
+    cap = 64
+    tb = torch.zeros(152 * 4 * cap * 2, dtype=torch.int64, device="cuda")
+    outs = run(x, 0, {"trace_buf": tb.data_ptr(), "trace_cap": cap})
+    ran = int((tb.view(152, 4, cap, 2)[:, 0, 0, 0] > 0).sum().item())
+    assert 2 <= ran <= 16 and ran % 2 == 0, ran
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
+    if want_g is not None:
+        assert_exact(bits(outs["gathered"]), want_g)
