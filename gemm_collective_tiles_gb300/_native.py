@@ -22,7 +22,7 @@ IRIS_EUNSUPPORTED = -6
 IRIS_NO_BIAS = ctypes.c_size_t(-1).value
 IRIS_MAX_WORLD = 16
 IRIS_NOALLOC_MAX_FLAGS = 16384
-IRIS_NOALLOC_SCRATCH_BYTES = 256 + 4 * IRIS_NOALLOC_MAX_FLAGS
+IRIS_NOALLOC_SCRATCH_BYTES = 256 + 8 * IRIS_NOALLOC_MAX_FLAGS
 
 IRIS_F16, IRIS_BF16, IRIS_F32 = 0, 1, 2
 IRIS_COLL_ALL_GATHER, IRIS_COLL_ALL_REDUCE, IRIS_COLL_REDUCE_SCATTER = 0, 1, 2

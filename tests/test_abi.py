@@ -146,6 +146,10 @@ def test_ctypes_structs_match_the_c_header(tmp_path):
         src.append(f'printf("{f} %zu\\n", offsetof(iris_b200_config, {f}));')
     for f in ("base", "rank_stride", "world"):
         src.append(f'printf("heap.{f} %zu\\n", offsetof(iris_b200_heap, {f}));')
+    # every numeric constant the binding mirrors, as the C compiler sees it
+    consts = [n for n in dir(N) if n.startswith("IRIS_") and isinstance(getattr(N, n), int)]
+    for n in consts:
+        src.append(f'printf("const.{n} %lld\\n", (long long)({n}));')
     src.append("return 0; }")
     c = tmp_path / "probe.c"
     c.write_text("\n".join(src))
@@ -162,3 +166,7 @@ def test_ctypes_structs_match_the_c_header(tmp_path):
         assert int(out[f]) == getattr(N.iris_b200_config, f).offset, f
     for f in ("base", "rank_stride", "world"):
         assert int(out["heap." + f]) == getattr(N.iris_b200_heap, f).offset, f
+    for n in consts:
+        want = getattr(N, n)
+        got = int(out["const." + n])
+        assert got == want or got == want - (1 << 64), n
