@@ -4,8 +4,10 @@
 
 WORKLOAD is a fused-op workload name of ``synthetic.WORKLOADS``,
 ``concurrent_ar_w8`` or ``gemm_bf16_8192`` (the concurrent workload's GEMM
-alone); inputs are drawn as the benchmark draws them.  Used by the profiling
-commands recorded under ``profiles/``.
+alone), with inputs drawn as the benchmark draws them; or an
+all_gather_matmul shape ``ag_mm_w<W>_<M>x<N>x<K>`` (bf16, N(0, 0.02) drawn on
+the device, as the shape sweep draws them).  Used by the profiling commands
+recorded under ``profiles/``.
 """
 from __future__ import annotations
 
@@ -33,6 +35,14 @@ def main(argv):
         prob = ConcurrentProblem(cw["M"], cw["N"], cw["K"], cw["gemm_dtype"], "all_reduce", cw["W"],
                                  cw["count"] if coll else 0, coll_dtype=cw["coll_dtype"])
         prob.upload(A, B, X)
+    elif name not in synthetic.WORKLOADS and name.startswith("ag_mm_w"):
+        w_part, shape = name[len("ag_mm_w"):].split("_", 1)
+        W = int(w_part)
+        M, N, K = (int(v) for v in shape.split("x"))
+        prob = FusedProblem("ag_mm", W, M, N, K, "bf16")
+        for r in range(W):
+            synthetic.fill_device_(prob.heap.view(prob.A, r), 7 + r)
+        synthetic.fill_device_(prob.heap.view(prob.B, 0), 99)
     else:
         wl = synthetic.WORKLOADS[name]
         x = synthetic.make_fused_inputs(**wl)
