@@ -75,6 +75,7 @@ class iris_b200_config(ctypes.Structure):
         ("gemm_l2_hint", ctypes.c_int),
         ("out_l2_hint", ctypes.c_int),
         ("sum_l2_hint", ctypes.c_int),
+        ("k_split", ctypes.c_int),
     ]
 
 

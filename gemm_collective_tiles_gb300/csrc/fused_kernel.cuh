@@ -149,6 +149,9 @@ struct Params {
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
     int out_evict_first;               // final 16-bit output stores carry an L2 evict-first policy
+    int split;                         // all_gather_matmul split-K: K chunks per output tile (0 / 1: none)
+    int kb_chunk;                      // ... K blocks per chunk (a whole number of stages)
+    unsigned long long* chain;         // ... chained-reduce tile counters (after the gather counters)
     int sum_l2_policy;                 // chained reduce running-sum stores / reduce-adds: 0 none,
                                        // 1 evict first, 2 evict last
     int startup_gather;                // all_gather_matmul: the TMA producer copies the gathers claimed
@@ -298,6 +301,15 @@ __device__ __forceinline__ bool drain_bar(const Ctl& c, uint64_t* bar, uint32_t 
     return true;
 }
 
+// Split-K all_gather_matmul: each output tile's K range is cut into
+// p.split chunks of p.kb_chunk K blocks; chunk j of a tile is a GEMM item of
+// its own, and the chunks' fp32 partials are summed in chunk order through the
+// chained reduce of the reduce ops (chunk j plays rank j), so the tiles
+// running at once stay short and share their operand blocks in L2.
+__device__ __forceinline__ bool split_k(const Params& p) { return p.op == OP_AG_MM && p.split > 1; }
+// the "ranks" a chained reduce sums over: the W ranks, or the K chunks
+__device__ __forceinline__ int chain_ranks(const Params& p) { return p.op == OP_AG_MM ? p.split : p.W; }
+
 // GROUP_M swizzle: linear output-tile id -> (m block, n block).  Tiles run
 // over groups of group_m m-blocks; inside a group the m index moves fastest so
 // consecutive tiles share B columns and neighbouring A rows in L2.
@@ -338,15 +350,16 @@ __device__ __forceinline__ uint32_t group_tiles(const Params& p) {
 __device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t item) {
     GemmCoord gc;
     const uint32_t g = tile_item(p, item, gc.hn);
-    if (p.op == OP_MM_RS || p.op == OP_MM_AR) {
+    if (p.op == OP_MM_RS || p.op == OP_MM_AR || split_k(p)) {
+        const uint32_t R = static_cast<uint32_t>(chain_ranks(p));
         if (p.rank_inner) {
-            gc.tile = g / p.W;
-            gc.rank = static_cast<int>(g % p.W);
+            gc.tile = g / R;
+            gc.rank = static_cast<int>(g % R);
         } else {
             const uint32_t T = group_tiles(p);
-            const uint32_t sg = g / (T * p.W);
+            const uint32_t sg = g / (T * R);
             const uint32_t Tsg = min(T, static_cast<uint32_t>(p.n_tiles) - sg * T);
-            const uint32_t local = g - sg * T * p.W;
+            const uint32_t local = g - sg * T * R;
             gc.rank = static_cast<int>(local / Tsg);
             gc.tile = sg * T + (local - static_cast<uint32_t>(gc.rank) * Tsg);
         }
@@ -406,6 +419,24 @@ __device__ __forceinline__ GatherCoord decode_gather(const Params& p, uint32_t c
 // order first visits its m-blocks in order, so the need grows by one block
 // per item there and stays at the whole group afterwards (monotonic in x).
 __device__ __forceinline__ uint32_t gather_need(const Params& p, uint32_t x) {
+    if (split_k(p)) {
+        // x is an item: chunk j of a tile of swizzle group sg; the chunk needs
+        // the shards up to the one holding its last K block, and in the
+        // group's shard-major numbering the gathers of earlier shards of
+        // every m-block come first
+        const uint32_t T = group_tiles(p), R = static_cast<uint32_t>(p.split);
+        const uint32_t sg = x / (T * R);
+        const uint32_t Tsg = min(T, static_cast<uint32_t>(p.n_tiles) - sg * T);
+        const uint32_t local = x - sg * T * R;
+        const int j = static_cast<int>(local / Tsg);
+        const int t_local = static_cast<int>(local - static_cast<uint32_t>(j) * Tsg);
+        const int first_m = static_cast<int>(sg) * p.group_m;
+        const int gsz = min(p.m_blocks - first_m, p.group_m);
+        const int kb_end = min(p.k_blocks, (j + 1) * p.kb_chunk);
+        const int s_hi = min(p.W - 1, (kb_end * BK - 1) / p.K_local);
+        return static_cast<uint32_t>(p.gather_parts) *
+               (static_cast<uint32_t>(first_m) * p.W + static_cast<uint32_t>(s_hi * gsz + min(t_local, gsz - 1) + 1));
+    }
     const uint32_t group_size = static_cast<uint32_t>(p.group_m) * p.n_blocks;
     const uint32_t group = x / group_size;
     const int first_m = static_cast<int>(group) * p.group_m;
@@ -745,7 +776,10 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             }
         }
         constexpr int KS = Smem<BN, STAGES, CG>::KS;
-        for (int kb = 0; kb < p.k_blocks; kb += KS) {
+        // split-K: this item's chunk of the K blocks
+        const int kb_lo = split_k(p) ? gc.rank * p.kb_chunk : 0;
+        const int kb_hi = split_k(p) ? min(p.k_blocks, kb_lo + p.kb_chunk) : p.k_blocks;
+        for (int kb = kb_lo; kb < kb_hi; kb += KS) {
             if (p.op == OP_AG_MM && acquired < p.W) {
                 const int s_hi = min(p.W - 1, ((kb + KS) * BK - 1) / p.K_local);
                 if (s_hi >= acquired) {
@@ -899,7 +933,13 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         const uint32_t d = tmem + buf * BN;
         bool ok = true;
         constexpr int KS = Smem<BN, STAGES, CG>::KS;
-        for (int kb = 0; kb < p.k_blocks; kb += KS) {
+        // split-K: this item's chunk of the K blocks (the producer's range)
+        int kb_lo = 0, kb_hi = p.k_blocks;
+        if (split_k(p)) {
+            kb_lo = decode_gemm(p, item).rank * p.kb_chunk;
+            kb_hi = min(p.k_blocks, kb_lo + p.kb_chunk);
+        }
+        for (int kb = kb_lo; kb < kb_hi; kb += KS) {
             if (!wait_bar(ctl, &sm.full[stage], phase, WAIT_SMEM_FULL)) {
                 ok = false;
                 break;
@@ -914,7 +954,7 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             const uint64_t bdesc = smem_desc(smem_u32(sm.b_tile(stage)), 64 * BK * KS * 2, 1024);
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-                if (kb + j >= p.k_blocks) break;  // K tail: the chunk past K holds zeros
+                if (kb + j >= kb_hi) break;  // K tail: the chunk past K holds zeros
                 const uint64_t adesc = smem_desc(a_addr + j * (BM * BK * 2), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -922,7 +962,7 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                     // B by 16 rows (2 KB); descriptors hold addresses >> 4
                     umma_f16<CG>(d, adesc + static_cast<uint64_t>(k * 2),
                                  bdesc + static_cast<uint64_t>((j * (BK / UMMA_K) + k) * 128), idesc,
-                                 (kb | j | k) != 0 ? 1u : 0u);
+                                 ((kb - kb_lo) | j | k) != 0 ? 1u : 0u);
                 }
             }
             // the stage is free again in both CTAs of a pair
@@ -1340,18 +1380,23 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     const int colbase = gc.nb * BN + (gc.hn >= 0 ? gc.hn * (BN / 2) : 0) + wc.h * COLS;
     // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
     const int nch = max(0, min(gc.hn >= 0 ? NCH / 2 : NCH, (p.N - colbase) / 32));
-    if (gc.rank == p.W - 1 && gc.rank > 0 && blk * BM < p.M && wc.lane == 0) {
+    const int R = chain_ranks(p);
+    if (gc.rank == R - 1 && gc.rank > 0 && blk * BM < p.M && wc.lane == 0) {
         // the last rank will read this warp's running-sum rows: pull them into
         // L2 while the tile's MMAs still run
         for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, 0, 0);
     }
     const int s = gc.rank;
+    // the reduce ops add each rank's own bias; a split all_gather_matmul adds
+    // its one bias (region 0) with the first chunk
+    const bool add_bias = p.has_bias && (p.op != OP_AG_MM || s == 0);
+    const int bias_region = p.op == OP_AG_MM ? 0 : s;
     const char* bias_base =
-        p.has_bias ? p.heap + static_cast<size_t>(s) * p.rank_stride + p.off_bias : nullptr;
+        add_bias ? p.heap + static_cast<size_t>(bias_region) * p.rank_stride + p.off_bias : nullptr;
     // per-column bias of the warp's columns, fetched while the MMAs still run:
     // lane l holds the 8 values of columns colbase + 8l .. 8l + 7
     uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
-    if (p.has_bias && !p.bias_on_m && wc.lane < nch * 4)
+    if (add_bias && !p.bias_on_m && wc.lane < nch * 4)
         bias8 = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(colbase + wc.lane * 8) * 2);
     if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
     tc_fence_after();
@@ -1364,13 +1409,14 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         if (wc.lane == 0) release_acc(sm, buf);
         return true;
     }
-    const bool last = (s == p.W - 1);
+    const bool last = (s == R - 1);
     const int row = blk * BM + wc.q * 32 + wc.lane;
     float row_bias = 0.f;
-    if (p.has_bias && p.bias_on_m && row < p.M)
+    if (add_bias && p.bias_on_m && row < p.M)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
     // one counter per BM-row block and column block
-    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.flags) + (blk * p.n_blocks + gc.nb);
+    unsigned long long* ctr = (split_k(p) ? p.chain : reinterpret_cast<unsigned long long*>(p.flags)) +
+                              (blk * p.n_blocks + gc.nb);
     const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
     if (s > 0) {
         int ok = 1;
@@ -1411,7 +1457,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-        if (p.has_bias) {
+        if (add_bias) {
             if (p.bias_on_m) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = x[i] + row_bias;
@@ -1949,7 +1995,7 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
             }
         } else {
             seen_gemm = true;
-            if (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR))
+            if (split_k(p) || (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR)))
                 ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
             else
                 ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);

@@ -28,6 +28,13 @@ constexpr int BN_NARROW = 128, STAGES_NARROW = 6;
 constexpr int STAGES_PAIR = 3;
 constexpr int STAGES_PAIR_STREAM = 6;
 constexpr int64_t STREAM_K = 98304;  // K above which the six-stage pipeline is the default
+// all_gather_matmul split-K by default above 2 x SPLIT_K_CHUNK, in chunks of
+// about SPLIT_K_CHUNK K: the tiles running at once then stay short enough to
+// share their operand blocks in L2, as at K = 16384 (measured, 8 x 16384-row
+// or 8192-row shapes: +9 % at K = 49152, +1-15 % at 65536, +27-49 % at 131072
+// and 262144; at K <= 32768 a split loses or gains nothing; chunks of 8192 or
+// 32768 lose to 16384 at every long K tried)
+constexpr int64_t SPLIT_K_CHUNK = 16384;
 constexpr size_t WS_HEADER = 256;
 constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
 
@@ -171,6 +178,7 @@ struct Cfg {
     int gemm_evict_last; // CTA-pair operand loads with an L2 evict-last policy
     int out_evict_first; // final 16-bit output stores with an L2 evict-first policy
     int sum_l2_policy;   // chained reduce running sum: 0 none, 1 evict first, 2 evict last
+    int k_split;         // all_gather_matmul: requested K chunks per tile (0 auto, 1 none)
 };
 
 int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
@@ -235,6 +243,8 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     out.sum_l2_policy = c->sum_l2_hint == 1 ? 1 : c->sum_l2_hint == 2 ? 2 : 0;
     if (c->out_l2_hint < 0 || c->out_l2_hint > 2) return IRIS_EINVAL;
     out.out_evict_first = c->out_l2_hint == 1 ? 1 : 0;
+    if (c->k_split < 0 || c->k_split > 4096) return IRIS_EINVAL;
+    out.k_split = c->k_split;
     if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
     out.startup_gather = c->startup_gather ? c->startup_gather : 1;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
@@ -270,6 +280,28 @@ void resolve_stages(Cfg& c, int64_t K) {
     if (c.stages == 0) c.stages = K > STREAM_K ? STAGES_PAIR_STREAM : STAGES_PAIR;
 }
 
+// all_gather_matmul split-K: the K chunks per output tile and the K blocks per
+// chunk (a whole number of two-K-block stages), or {1, 0} for none.  It needs
+// CTA pairs, the chained reduce's whole 32-column chunks (N % 32 == 0) and
+// K > 0; by default it applies above 2 x SPLIT_K_CHUNK.
+struct SplitK {
+    int split, kb_chunk;
+};
+SplitK resolve_split(int k_split, bool pairs, int64_t M, int64_t N, int64_t K) {
+    SplitK r{1, 0};
+    if (!pairs || M <= 0 || K <= 0 || N % 32 != 0 || k_split == 1) return r;
+    const int64_t want = k_split > 1 ? k_split : (K > 2 * SPLIT_K_CHUNK ? cdiv(K, SPLIT_K_CHUNK) : 1);
+    if (want <= 1) return r;
+    const int64_t kblocks = cdiv(K, BK);
+    int64_t kbc = cdiv(kblocks, want);
+    kbc += kbc & 1;
+    const int64_t split = cdiv(kblocks, kbc);
+    if (split <= 1) return r;
+    r.split = static_cast<int>(split);
+    r.kb_chunk = static_cast<int>(kbc);
+    return r;
+}
+
 int resolve_pair(Cfg& c, iris_op op, bool has_gemm = true) {
     const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
     const bool applies = has_gemm && c.tile_n == BN_WIDE && (!reduce_op || c.reduce_mode == 3);
@@ -294,19 +326,21 @@ struct WsLayout {
     size_t flags_off, n_flags, partial_off, partial_elems, total;
 };
 
-WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n, int reduce_mode) {
+WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n, int reduce_mode, int split = 1) {
     WsLayout L{};
     L.flags_off = WS_HEADER;
     const int64_t mb = cdiv(M, BM), nb = cdiv(N, tile_n);
     const bool reduce_op = op == IRIS_OP_MATMUL_REDUCE_SCATTER || op == IRIS_OP_MATMUL_ALL_REDUCE;
     if (op == IRIS_OP_ALL_GATHER_MATMUL)
-        L.n_flags = 2 * static_cast<size_t>(W) * mb;  // 8-byte ready counters per (128-row block, shard)
+        // 8-byte ready counters per (128-row block, shard); split-K: then one
+        // 8-byte chained-reduce counter per tile
+        L.n_flags = 2 * static_cast<size_t>(W) * mb + (split > 1 ? 2 * static_cast<size_t>(mb) * nb : 0);
     else if (reduce_op)
         L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte tile counters
     L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
-    if (reduce_op) L.partial_elems = static_cast<size_t>(M) * N;
+    if (reduce_op || (op == IRIS_OP_ALL_GATHER_MATMUL && split > 1)) L.partial_elems = static_cast<size_t>(M) * N;
     // one fp32 running sum (chained) or one fp32 partial per rank
-    const size_t copies = L.partial_elems ? (reduce_mode == 3 ? 1 : W) : 0;
+    const size_t copies = L.partial_elems ? ((reduce_mode == 3 || !reduce_op) ? 1 : W) : 0;
     L.total = round_up(L.partial_off + L.partial_elems * 4 * copies, 256);
     return L;
 }
@@ -557,11 +591,14 @@ bool dims_ok(int64_t M, int64_t N, int64_t K) {
 
 int prepare_ws(Params& p, void* ws, size_t ws_bytes, iris_op op, int64_t M, int64_t N, int W,
                const Cfg& c) {
-    const WsLayout L = ws_layout(op, M, N, W, c.tile_n, c.reduce_mode);
+    const int split = (op == IRIS_OP_ALL_GATHER_MATMUL && p.split > 1) ? p.split : 1;
+    const WsLayout L = ws_layout(op, M, N, W, c.tile_n, c.reduce_mode, split);
     if (!ws || ws_bytes < L.total) return IRIS_ENOWS;
     if (!aligned16(reinterpret_cast<uintptr_t>(ws))) return IRIS_EALIGN;
     p.ws = reinterpret_cast<WsHeader*>(ws);
     p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.flags_off);
+    // split-K: the chained-reduce counters follow the W x m-block gather counters
+    p.chain = reinterpret_cast<unsigned long long*>(p.flags) + static_cast<size_t>(W) * cdiv(M, BM);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partial_off);
     p.partial_elems = L.partial_elems;
     return IRIS_OK;
@@ -609,7 +646,16 @@ int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int wo
         mode = resolve_reduce_mode(cfg, op, N, world);
         if (mode < 0) return IRIS_EINVAL;
     }
-    *bytes = ws_layout(op, Mrows, N, world, tile_n, mode).total;
+    int split = 1;
+    if (op == IRIS_OP_ALL_GATHER_MATMUL) {
+        // sized for CTA pairs wherever the config allows them (a launch that
+        // ends up on one-CTA tiles does not split and uses less)
+        const int ks = cfg ? cfg->k_split : 0;
+        if (ks < 0 || ks > 4096) return IRIS_EINVAL;
+        const bool pairs = !(cfg && (cfg->tile_m == BM || (cfg->tile_n != 0 && cfg->tile_n != 256))) && N > 128;
+        split = resolve_split(ks, pairs, M, N, K).split;
+    }
+    *bytes = ws_layout(op, Mrows, N, world, tile_n, mode, split).total;
     return IRIS_OK;
 }
 
@@ -627,7 +673,9 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_ALL_GATHER_MATMUL, N, c))) return rc;
     if ((rc = resolve_pair(c, IRIS_OP_ALL_GATHER_MATMUL))) return rc;
-    resolve_stages(c, K);
+    const SplitK sk = resolve_split(c.k_split, c.cg == 2, M, N, K);
+    // the pipeline by the K one item runs
+    resolve_stages(c, sk.split > 1 ? int64_t(sk.kb_chunk) * BK : K);
     if ((rc = check_region(heap, off_A, size_t(M) * K_l * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -652,13 +700,28 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     p.off_bias = has_bias ? off_bias : 0;
     p.has_bias = has_bias;
     p.n_gemm = (M > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
+    if (sk.split > 1) {
+        // chunk j of every tile is an item; the chunks' partials are summed
+        // in chunk order by the chained reduce (one fp32 running sum)
+        if (uint64_t(p.n_gemm) * sk.split >= 0x7FFFFFFFull) return IRIS_EINVAL;
+        p.split = sk.split;
+        p.kb_chunk = sk.kb_chunk;
+        p.n_gemm *= static_cast<uint32_t>(sk.split);
+        p.reduce_mode = 3;
+        p.rank_inner = 0;
+        // gathers claimed a whole swizzle group (all its chunks) ahead
+        p.lookahead *= static_cast<uint32_t>(sk.split);
+    }
     p.gather_parts = c.gather_parts;
     // the producer's start-up copies move whole 128-row blocks
     p.startup_gather = (c.startup_gather == 2 && c.gather_parts == 1 && M > 0 && K_l > 0) ? 1 : 0;
     if (p.startup_gather && (rc = make_gather_maps(p, heap, off_A, off_gathered, M, K, K_l))) return rc;
     if (int64_t(mblocks) * W * c.gather_parts >= 0x7FFFFFFF) return IRIS_EINVAL;
     p.n_comm = static_cast<uint32_t>(mblocks) * W * c.gather_parts;
-    tail_split(p, c, false);
+    if (sk.split > 1)
+        p.g_split = p.n_gemm;  // no column-half tail items (the chain counts whole tiles)
+    else
+        tail_split(p, c, false);
     if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_ALL_GATHER_MATMUL, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         char* g = p.heap + off_gathered;
@@ -671,6 +734,10 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     }
     if (p.n_gemm > 0 &&
         (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M, 1, W, N * 2, size_t(M) * N * 2, heap->rank_stride)))
+        return rc;
+    // split-K: the fp32 running sum of the chunks
+    if (p.split > 1 &&
+        (rc = make_out_map(&p.tmS, p.partials, 2, N, M, 1, 1, N * 4, size_t(M) * N * 4, size_t(M) * N * 4)))
         return rc;
     return launch(p, c, stream);
 }
@@ -1030,7 +1097,14 @@ extern "C" int iris_b200_all_gather_matmul_noalloc(const iris_b200_heap* heap, s
     const size_t used = WS_HEADER + size_t(flags) * 8;
     e = cudaMemsetAsync(scratch, 0, used, stream);
     if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync (no-alloc scratch)", static_cast<int>(e));
-    return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, cfg,
+    // no split-K here: the static scratch has no room for its running sum
+    iris_b200_config local;
+    if (cfg)
+        local = *cfg;
+    else
+        std::memset(&local, 0, sizeof(local));
+    local.k_split = 1;
+    return iris_b200_all_gather_matmul(heap, off_A, off_B, off_bias, off_out, off_gathered, M, N, K, dtype, &local,
                                        scratch, IRIS_NOALLOC_SCRATCH_BYTES, stream);
 }
 

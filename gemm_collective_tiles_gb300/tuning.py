@@ -28,7 +28,7 @@ ENV_CACHE = "IRIS_B200_CACHE"
 TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block", "stages",
            "coll_ring", "coll_l2_hint", "coll_path", "gather_parts",
            "startup_gather", "gemm_l2_hint", "out_l2_hint",
-           "sum_l2_hint")
+           "sum_l2_hint", "k_split")
 
 # nearest-shape matching: largest accepted distance, in log2 units over the
 # problem sizes (1.0 = one size off by a factor of 2, or two by 2^0.7 each)
@@ -161,7 +161,9 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     out: List[dict] = [{}]
     # the CTA-pair pipeline the default does not pick for this K (three
     # 128-deep stages up to K = 98304, six 64-deep stages beyond)
-    out.append({"stages": 3 if K > 98304 else 6})
+    # (a split all_gather_matmul picks it by the K of one chunk)
+    k_item = 16384 if (op == "all_gather_matmul" and K > 32768 and N % 32 == 0) else K
+    out.append({"stages": 3 if k_item > 98304 else 6})
     # the swizzle widths the default does not use (32; 16 in the concurrent
     # mode and for the reduce ops when a rank's A exceeds 64 MB)
     reduce = op in ("matmul_reduce_scatter", "matmul_all_reduce")
@@ -179,6 +181,9 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
         out.append({"tile_n": 128})
     if op in ("matmul_reduce_scatter", "matmul_all_reduce"):
         out += [{"reduce_mode": 2}, {"reduce_mode": 1}, {"group_m": 64, "reduce_mode": 3}]
+    if op == "all_gather_matmul" and K > 16384 and N % 32 == 0:
+        # split-K: the default splits above K = 32768 into chunks of ~16384
+        out.insert(1, {"k_split": 1} if K > 32768 else {"k_split": 2})
     if op == "concurrent":
         if count > 0:
             # (tile, split) pairs ranked by the work-stealing makespan model

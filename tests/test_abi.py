@@ -170,3 +170,37 @@ def test_ctypes_structs_match_the_c_header(tmp_path):
         want = getattr(N, n)
         got = int(out["const." + n])
         assert got == want or got == want - (1 << 64), n
+
+
+def test_split_k_workspace():
+    """all_gather_matmul above K = 32768 splits K by default (chunks of about
+    16384) and its workspace then holds one 8-byte chained-reduce counter per
+    tile after the gather counters, and an M x N fp32 running sum; k_split 1
+    (or one-CTA tiles) leaves the workspace as without the split."""
+    lib = N.load()
+    out = ctypes.c_size_t(0)
+    W, M, Nn, K = 8, 16384, 16384, 131072
+    mb, nb = M // 128, Nn // 256
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, M, Nn, K, W, N.IRIS_BF16, None,
+                                        ctypes.byref(out)) == 0
+    flags = (2 * W * mb + 2 * mb * nb) * 4
+    assert out.value == 256 + ((flags + 255) // 256) * 256 + M * Nn * 4
+    for cfg in (gct.make_config(k_split=1), gct.make_config(tile_m=128)):
+        assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, M, Nn, K, W, N.IRIS_BF16,
+                                            ctypes.byref(cfg), ctypes.byref(out)) == 0
+        assert out.value == 256 + ((2 * W * mb * 4 + 255) // 256) * 256
+    # K = 32768: no split by default; an explicit k_split asks for it
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 256, 256, 32768, W, N.IRIS_BF16, None,
+                                        ctypes.byref(out)) == 0
+    assert out.value == 256 + 256
+    cfg = gct.make_config(k_split=4)
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 256, 256, 32768, W, N.IRIS_BF16,
+                                        ctypes.byref(cfg), ctypes.byref(out)) == 0
+    assert out.value == 256 + 256 + 256 * 256 * 4
+    # N not a multiple of 32: the chained reduce does not apply, no split
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 256, 264, 131072, W, N.IRIS_BF16, None,
+                                        ctypes.byref(out)) == 0
+    assert out.value == 256 + 256
+    bad = gct.make_config(k_split=-1)
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 256, 256, 65536, W, N.IRIS_BF16,
+                                        ctypes.byref(bad), ctypes.byref(out)) == N.IRIS_EINVAL

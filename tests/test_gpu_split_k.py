@@ -1,0 +1,99 @@
+"""Split-K all_gather_matmul against the oracle.
+
+With k_split > 1 (by default above K = 32768) every output tile's K range is
+cut into chunks; chunk j of a tile is a GEMM item of its own, and the chunks'
+fp32 partials are summed in chunk order through the chained reduce's running
+sum before the one rounding to 16 bits.  On small-integer inputs every
+partial and every sum is exact, so the output must equal the oracle's bits
+whatever the chunking; the gathered A is a copy and must always match.  Row
+counts leave the last pair tile full, partial or half empty; N = 288 leaves a
+partial last 64-column chunk of B."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gemm_collective_tiles_gb300 import query_status
+from gemm_collective_tiles_gb300.runner import FusedProblem
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_exact(got, want):
+    assert got.shape == want.shape
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+def run(x, cfg, bias_on_m=False):
+    prob = FusedProblem("ag_mm", x.W, x.M, x.N, x.K, x.dtype, bias=x.bias is not None, bias_on_m=bias_on_m,
+                        config=cfg)
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    return prob.outputs()
+
+
+# (W, M, N, K, k_split): chunks of whole shards, chunks inside a shard,
+# chunks across shard boundaries, an odd K-block count, and more chunks than
+# shards
+CASES = [
+    (4, 300, 256, 8192, 4), (2, 512, 288, 4096, 3), (8, 200, 512, 8192, 2),
+    (4, 640, 256, 4160, 5), (2, 129, 320, 2048, 16), (8, 256, 256, 16384, 8),
+]
+
+
+@pytest.mark.parametrize("W,M,N,K,ks", CASES)
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_split_k_exact_integer(W, M, N, K, ks, dt):
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, dt, seed=4100 + M + N + ks, dist="int", scale=1,
+                                    bias=True, bias_scale=3)
+    want, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    outs = run(x, {"k_split": ks})
+    assert_exact(bits(outs["gathered"]), want_g)
+    assert_exact(bits(outs["out"][0]), want)
+
+
+@pytest.mark.parametrize("extra", [{"grid": 2}, {"grid": 6, "group_m": 2}, {"replicate_outputs": 1},
+                                   {"gather_parts": 4}, {"startup_gather": 2}, {"stages": 6}])
+def test_split_k_schedules_exact(extra):
+    """A grid of one or three pairs (the rings wrap many times), narrow
+    swizzle groups, replicated outputs, gathers cut into row parts or copied
+    by the TMA producer, and the six-stage pipeline."""
+    W, M, N, K = 4, 520, 256, 8192
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=4200, dist="int", scale=1, bias=True,
+                                    bias_scale=3)
+    want, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    outs = run(x, {"k_split": 4, **extra})
+    assert_exact(bits(outs["gathered"]), want_g)
+    for r in range(W if extra.get("replicate_outputs") else 1):
+        assert_exact(bits(outs["out"][r]), want)
+
+
+def test_split_k_row_bias_exact():
+    W, M, N, K = 2, 300, 256, 4096
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "f16", seed=4300, dist="int", scale=1, bias=True,
+                                    bias_scale=3, bias_len=M)
+    want, _ = oracle.all_gather_matmul(x.A, x.B[0], x.bias, bias_on_m=True)
+    assert_exact(bits(run(x, {"k_split": 4}, bias_on_m=True)["out"][0]), want)
+
+
+def test_split_k_random_within_tolerance_of_unsplit():
+    """Random inputs: the chunked sum rounds differently from one fp32
+    accumulation over all of K, within the GEMM tolerance of the oracle."""
+    W, M, N, K = 8, 512, 512, 16384
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=4400, dist="normal", scale=0.5, bias=True)
+    want, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    ref = torch.from_numpy(want.view(np.int16)).view(torch.bfloat16).float()
+    for ks in (1, 4, 8):
+        outs = run(x, {"k_split": ks})
+        assert_exact(bits(outs["gathered"]), want_g)
+        got = outs["out"][0].float()
+        err = float((got - ref).abs().max() / ref.abs().max())
+        assert err <= 5e-3, (ks, err)

@@ -67,11 +67,18 @@ def test_candidates():
     r = tuning.candidates("matmul_reduce_scatter", 4, 4096, 4096, 4096, 152, top_k=50)
     assert {"reduce_mode": 1} in r and {"reduce_mode": 2} in r
     assert len(tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)) == 3
-    # the CTA-pair pipeline the default does not pick for this K is tried early
+    # the CTA-pair pipeline the default does not pick for the K one item runs
+    # is tried early: all_gather_matmul splits K above 32768 into chunks of
+    # ~16384 (so the three-stage default), the reduce ops do not
     short_k = tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)
-    long_k = tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152, top_k=3)
+    split_k = tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152, top_k=3)
+    long_k = tuning.candidates("matmul_all_reduce", 8, 4096, 4096, 131072, 152, top_k=3)
     assert {"stages": 6} in short_k and {"stages": 3} not in short_k
+    assert {"k_split": 1} in split_k and {"stages": 6} in split_k and {"stages": 3} not in split_k
     assert {"stages": 3} in long_k and {"stages": 6} not in long_k
+    # unsplit all_gather_matmul with a long K (N not a multiple of 32)
+    odd_n = tuning.candidates("all_gather_matmul", 8, 4096, 4104, 131072, 152, top_k=3)
+    assert {"stages": 3} in odd_n and not any("k_split" in c for c in odd_n)
 
 
 def test_all_tuned_knobs_exist_in_the_config_struct():
