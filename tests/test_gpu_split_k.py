@@ -97,3 +97,16 @@ def test_split_k_random_within_tolerance_of_unsplit():
         got = outs["out"][0].float()
         err = float((got - ref).abs().max() / ref.abs().max())
         assert err <= 5e-3, (ks, err)
+
+
+@pytest.mark.parametrize("W,M,N,K,extra", [(4, 300, 256, 8192, {"tile_m": 128}), (2, 256, 264, 4096, {}),
+                                           (2, 256, 136, 65536, {"k_split": 0})])
+def test_split_k_where_it_does_not_apply(W, M, N, K, extra):
+    """A split asked for (or, above K = 32768, the default one) on one-CTA
+    tiles or with N not a multiple of 32 runs unsplit: exact all the same."""
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=4500 + N, dist="int", scale=1, bias=True,
+                                    bias_scale=3)
+    want, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    outs = run(x, {"k_split": 4, **extra})
+    assert_exact(bits(outs["gathered"]), want_g)
+    assert_exact(bits(outs["out"][0]), want)
