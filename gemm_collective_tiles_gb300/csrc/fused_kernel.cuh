@@ -149,7 +149,7 @@ struct Params {
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
     int out_evict_first;               // final 16-bit output stores carry an L2 evict-first policy
-    int split;                         // all_gather_matmul split-K: K chunks per output tile (0 / 1: none)
+    int split;                         // split-K: K chunks per (rank's) output tile (0 / 1: none)
     int kb_chunk;                      // ... K blocks per chunk (a whole number of stages)
     unsigned long long* chain;         // ... chained-reduce tile counters (after the gather counters)
     int sum_l2_policy;                 // chained reduce running-sum stores / reduce-adds: 0 none,
@@ -301,14 +301,16 @@ __device__ __forceinline__ bool drain_bar(const Ctl& c, uint64_t* bar, uint32_t 
     return true;
 }
 
-// Split-K all_gather_matmul: each output tile's K range is cut into
-// p.split chunks of p.kb_chunk K blocks; chunk j of a tile is a GEMM item of
-// its own, and the chunks' fp32 partials are summed in chunk order through the
-// chained reduce of the reduce ops (chunk j plays rank j), so the tiles
-// running at once stay short and share their operand blocks in L2.
-__device__ __forceinline__ bool split_k(const Params& p) { return p.op == OP_AG_MM && p.split > 1; }
-// the "ranks" a chained reduce sums over: the W ranks, or the K chunks
-__device__ __forceinline__ int chain_ranks(const Params& p) { return p.op == OP_AG_MM ? p.split : p.W; }
+// Split-K (all_gather_matmul and the chained reduce ops): each output tile's
+// K range is cut into p.split chunks of p.kb_chunk K blocks; chunk j of a
+// tile (of a rank) is a GEMM item of its own, and all partials are summed
+// through the chained reduce in (rank, chunk) order, so the tiles running at
+// once stay short and share their operand blocks in L2.
+__device__ __forceinline__ bool split_k(const Params& p) { return p.split > 1; }
+// the links of a tile's reduce chain: W ranks (reduce ops) x the K chunks
+__device__ __forceinline__ int chain_ranks(const Params& p) {
+    return (p.op == OP_AG_MM ? 1 : p.W) * max(1, p.split);
+}
 
 // GROUP_M swizzle: linear output-tile id -> (m block, n block).  Tiles run
 // over groups of group_m m-blocks; inside a group the m index moves fastest so
@@ -330,6 +332,8 @@ __device__ __forceinline__ void swizzle_tile(const Params& p, uint32_t t, int& m
 // time; with rank_inner the rank index moves fastest instead.
 struct GemmCoord {
     int rank, mb, nb;
+    int chunk;  // split-K: the item's K chunk (0 when not split)
+    int link;   // chained reduce: the item's place in its tile's chain, rank * split + chunk
     uint32_t tile;
     int hn;  // -1: the whole tile; 0 / 1: column half of a split tail tile
 };
@@ -352,20 +356,27 @@ __device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t item)
     const uint32_t g = tile_item(p, item, gc.hn);
     if (p.op == OP_MM_RS || p.op == OP_MM_AR || split_k(p)) {
         const uint32_t R = static_cast<uint32_t>(chain_ranks(p));
+        int link;
         if (p.rank_inner) {
             gc.tile = g / R;
-            gc.rank = static_cast<int>(g % R);
+            link = static_cast<int>(g % R);
         } else {
             const uint32_t T = group_tiles(p);
             const uint32_t sg = g / (T * R);
             const uint32_t Tsg = min(T, static_cast<uint32_t>(p.n_tiles) - sg * T);
             const uint32_t local = g - sg * T * R;
-            gc.rank = static_cast<int>(local / Tsg);
-            gc.tile = sg * T + (local - static_cast<uint32_t>(gc.rank) * Tsg);
+            link = static_cast<int>(local / Tsg);
+            gc.tile = sg * T + (local - static_cast<uint32_t>(link) * Tsg);
         }
+        const int S = max(1, p.split);
+        gc.link = link;
+        gc.chunk = link % S;
+        gc.rank = p.op == OP_AG_MM ? 0 : link / S;
     } else {
         gc.tile = g;
         gc.rank = 0;
+        gc.chunk = 0;
+        gc.link = 0;
     }
     swizzle_tile(p, gc.tile, gc.mb, gc.nb);
     if (p.op == OP_MM_AG) gc.rank = gc.mb / p.mb_per_rank;
@@ -419,7 +430,7 @@ __device__ __forceinline__ GatherCoord decode_gather(const Params& p, uint32_t c
 // order first visits its m-blocks in order, so the need grows by one block
 // per item there and stays at the whole group afterwards (monotonic in x).
 __device__ __forceinline__ uint32_t gather_need(const Params& p, uint32_t x) {
-    if (split_k(p)) {
+    if (p.op == OP_AG_MM && split_k(p)) {
         // x is an item: chunk j of a tile of swizzle group sg; the chunk needs
         // the shards up to the one holding its last K block, and in the
         // group's shard-major numbering the gathers of earlier shards of
@@ -777,7 +788,7 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         }
         constexpr int KS = Smem<BN, STAGES, CG>::KS;
         // split-K: this item's chunk of the K blocks
-        const int kb_lo = split_k(p) ? gc.rank * p.kb_chunk : 0;
+        const int kb_lo = split_k(p) ? gc.chunk * p.kb_chunk : 0;
         const int kb_hi = split_k(p) ? min(p.k_blocks, kb_lo + p.kb_chunk) : p.k_blocks;
         for (int kb = kb_lo; kb < kb_hi; kb += KS) {
             if (p.op == OP_AG_MM && acquired < p.W) {
@@ -936,7 +947,7 @@ __device__ void run_mma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         // split-K: this item's chunk of the K blocks (the producer's range)
         int kb_lo = 0, kb_hi = p.k_blocks;
         if (split_k(p)) {
-            kb_lo = decode_gemm(p, item).rank * p.kb_chunk;
+            kb_lo = decode_gemm(p, item).chunk * p.kb_chunk;
             kb_hi = min(p.k_blocks, kb_lo + p.kb_chunk);
         }
         for (int kb = kb_lo; kb < kb_hi; kb += KS) {
@@ -1381,16 +1392,16 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
     const int nch = max(0, min(gc.hn >= 0 ? NCH / 2 : NCH, (p.N - colbase) / 32));
     const int R = chain_ranks(p);
-    if (gc.rank == R - 1 && gc.rank > 0 && blk * BM < p.M && wc.lane == 0) {
+    if (gc.link == R - 1 && gc.link > 0 && blk * BM < p.M && wc.lane == 0) {
         // the last rank will read this warp's running-sum rows: pull them into
         // L2 while the tile's MMAs still run
         for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, 0, 0);
     }
-    const int s = gc.rank;
-    // the reduce ops add each rank's own bias; a split all_gather_matmul adds
-    // its one bias (region 0) with the first chunk
-    const bool add_bias = p.has_bias && (p.op != OP_AG_MM || s == 0);
-    const int bias_region = p.op == OP_AG_MM ? 0 : s;
+    const int s = gc.link;
+    // the reduce ops add each rank's own bias, all_gather_matmul its one bias
+    // (region 0); with split-K, with the rank's first chunk
+    const bool add_bias = p.has_bias && gc.chunk == 0;
+    const int bias_region = p.op == OP_AG_MM ? 0 : gc.rank;
     const char* bias_base =
         add_bias ? p.heap + static_cast<size_t>(bias_region) * p.rank_stride + p.off_bias : nullptr;
     // per-column bias of the warp's columns, fetched while the MMAs still run:
@@ -1415,7 +1426,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     if (add_bias && p.bias_on_m && row < p.M)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
     // one counter per BM-row block and column block
-    unsigned long long* ctr = (split_k(p) ? p.chain : reinterpret_cast<unsigned long long*>(p.flags)) +
+    unsigned long long* ctr = (p.op == OP_AG_MM ? p.chain : reinterpret_cast<unsigned long long*>(p.flags)) +
                               (blk * p.n_blocks + gc.nb);
     const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
     if (s > 0) {

@@ -765,7 +765,9 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     c.reduce_mode = resolve_reduce_mode(cfg, op, N, W);
     if (c.reduce_mode < 0) return IRIS_EINVAL;
     if ((rc = resolve_pair(c, op))) return rc;
-    resolve_stages(c, K);
+    // split-K rides on the chained reduce: the chain then runs over (rank, chunk)
+    const SplitK sk = c.reduce_mode == 3 ? resolve_split(c.k_split, c.cg == 2, M, N, K) : SplitK{1, 0};
+    resolve_stages(c, sk.split > 1 ? int64_t(sk.kb_chunk) * BK : K);
     if ((rc = check_region(heap, off_A, size_t(M) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N_l * 2))) return rc;
@@ -788,11 +790,18 @@ static int mm_reduce_common(iris_op op, const iris_b200_heap* heap, size_t off_A
     p.off_bias = has_bias ? off_bias : 0;
     p.has_bias = has_bias;
     const uint64_t tiles = (M > 0 && N > 0) ? uint64_t(p.n_tiles) : 0;
-    if (tiles * W >= 0x7FFFFFFFull) return IRIS_EINVAL;
-    p.n_gemm = static_cast<uint32_t>(tiles * W);
+    if (tiles * W * sk.split >= 0x7FFFFFFFull) return IRIS_EINVAL;
+    p.n_gemm = static_cast<uint32_t>(tiles * W * sk.split);
     p.n_comm = c.reduce_mode == 1 ? static_cast<uint32_t>(tiles) : 0u;
     p.n_parts = c.reduce_mode == 2 ? static_cast<uint32_t>(tiles * W) : 0u;
-    tail_split(p, c, true);
+    if (sk.split > 1) {
+        p.split = sk.split;
+        p.kb_chunk = sk.kb_chunk;
+        p.rank_inner = 0;
+        p.g_split = p.n_gemm;  // no column-half tail items
+    } else {
+        tail_split(p, c, true);
+    }
     if ((rc = prepare_ws(p, workspace, workspace_bytes, op, M, N, W, c))) return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M, W, K * 2, heap->rank_stride, BK, BM))) return rc;

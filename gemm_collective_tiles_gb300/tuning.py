@@ -162,7 +162,8 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     # the CTA-pair pipeline the default does not pick for this K (three
     # 128-deep stages up to K = 98304, six 64-deep stages beyond)
     # (a split all_gather_matmul picks it by the K of one chunk)
-    k_item = 16384 if (op == "all_gather_matmul" and K > 32768 and N % 32 == 0) else K
+    splits = op in ("all_gather_matmul", "matmul_reduce_scatter", "matmul_all_reduce") and N % 32 == 0
+    k_item = 16384 if (splits and K > 32768) else K
     out.append({"stages": 3 if k_item > 98304 else 6})
     # the swizzle widths the default does not use (32; 16 in the concurrent
     # mode and for the reduce ops when a rank's A exceeds 64 MB)
@@ -181,7 +182,7 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
         out.append({"tile_n": 128})
     if op in ("matmul_reduce_scatter", "matmul_all_reduce"):
         out += [{"reduce_mode": 2}, {"reduce_mode": 1}, {"group_m": 64, "reduce_mode": 3}]
-    if op == "all_gather_matmul" and K > 16384 and N % 32 == 0:
+    if splits and K > 16384:
         # split-K: the default splits above K = 32768 into chunks of ~16384
         out.insert(1, {"k_split": 1} if K > 32768 else {"k_split": 2})
     if op == "concurrent":

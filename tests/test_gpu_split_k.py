@@ -86,11 +86,14 @@ def test_split_k_row_bias_exact():
 
 def test_split_k_random_within_tolerance_of_unsplit():
     """Random inputs: the chunked sum rounds differently from one fp32
-    accumulation over all of K, within the GEMM tolerance of the oracle."""
+    accumulation over all of K, within the GEMM tolerance of the oracle.
+    fp16 outputs, whose rounding step (2^-11 relative) is well below the
+    tolerance; a bf16 step (up to 2^-7) is above it, so there a single
+    legitimate rounding flip at the largest output could fail the bound."""
     W, M, N, K = 8, 512, 512, 16384
-    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "bf16", seed=4400, dist="normal", scale=0.5, bias=True)
+    x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "f16", seed=4400, dist="normal", scale=0.5, bias=True)
     want, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
-    ref = torch.from_numpy(want.view(np.int16)).view(torch.bfloat16).float()
+    ref = torch.from_numpy(want.view(np.int16)).view(torch.float16).float()
     for ks in (1, 4, 8):
         outs = run(x, {"k_split": ks})
         assert_exact(bits(outs["gathered"]), want_g)
@@ -110,3 +113,58 @@ def test_split_k_where_it_does_not_apply(W, M, N, K, extra):
     outs = run(x, {"k_split": 4, **extra})
     assert_exact(bits(outs["gathered"]), want_g)
     assert_exact(bits(outs["out"][0]), want)
+
+
+def reduce_want(x):
+    if x.op == "mm_rs":
+        return oracle.matmul_reduce_scatter(x.A, x.B, x.bias)
+    return [oracle.matmul_all_reduce(x.A, x.B, x.bias)]
+
+
+def run_reduce(x, cfg):
+    prob = FusedProblem(x.op, x.W, x.M, x.N, x.K, x.dtype, bias=x.bias is not None, config=cfg)
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    return prob.outputs()
+
+
+# (op, W, M, N, K, k_split): the chained reduce then runs over (rank, chunk);
+# each rank's bias is added once, with its first chunk
+REDUCE_CASES = [
+    ("mm_rs", 4, 300, 512, 4096, 3), ("mm_rs", 2, 256, 256, 8192, 4), ("mm_rs", 2, 129, 1024, 2048, 16),
+    ("mm_ar", 2, 520, 256, 4160, 5), ("mm_ar", 3, 256, 320, 8192, 2), ("mm_ar", 8, 100, 256, 4096, 4),
+]
+
+
+@pytest.mark.parametrize("op,W,M,N,K,ks", REDUCE_CASES)
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_split_k_reduce_ops_exact_integer(op, W, M, N, K, ks, dt):
+    x = synthetic.make_fused_inputs(op, W, M, N, K, dt, seed=4600 + M + N + ks, dist="int", scale=1, bias=True,
+                                    bias_scale=3)
+    want = reduce_want(x)
+    outs = run_reduce(x, {"k_split": ks})
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
+
+
+@pytest.mark.parametrize("op", ["mm_rs", "mm_ar"])
+def test_split_k_reduce_ops_schedules(op):
+    """Replicated outputs, a grid of one pair, and random inputs within the
+    GEMM tolerance of the oracle (fp16 outputs, as in the test above)."""
+    W, M, N, K = 4, 300, 512, 8192
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=4700, dist="int", scale=1, bias=True, bias_scale=3)
+    want = reduce_want(x)
+    for extra in ({"replicate_outputs": 1}, {"grid": 2}):
+        outs = run_reduce(x, {"k_split": 4, **extra})
+        n = W if (op == "mm_rs" or extra.get("replicate_outputs")) else 1
+        for r in range(n):
+            assert_exact(bits(outs["out"][r]), want[r if op == "mm_rs" else 0])
+    y = synthetic.make_fused_inputs(op, W, M, N, K, "f16", seed=4701, dist="normal", scale=0.5, bias=True)
+    want = reduce_want(y)
+    outs = run_reduce(y, {"k_split": 4})
+    for r in range(W if op == "mm_rs" else 1):
+        ref = torch.from_numpy(want[r].view(np.int16)).view(torch.float16).float()
+        err = float((outs["out"][r].float() - ref).abs().max() / ref.abs().max())
+        assert err <= 5e-3, (r, err)
