@@ -1,9 +1,10 @@
-"""Split-K all_gather_matmul against the oracle.
+"""Split-K all_gather_matmul and reduce ops against the oracle.
 
 With k_split > 1 (by default above K = 32768) every output tile's K range is
 cut into chunks; chunk j of a tile is a GEMM item of its own, and the chunks'
-fp32 partials are summed in chunk order through the chained reduce's running
-sum before the one rounding to 16 bits.  On small-integer inputs every
+fp32 partials are summed in chunk order (for the reduce ops in (rank, chunk)
+order) through the chained reduce's running sum before the one rounding to
+16 bits.  On small-integer inputs every
 partial and every sum is exact, so the output must equal the oracle's bits
 whatever the chunking; the gathered A is a copy and must always match.  Row
 counts leave the last pair tile full, partial or half empty; N = 288 leaves a
