@@ -169,3 +169,22 @@ def test_split_k_reduce_ops_schedules(op):
         ref = torch.from_numpy(want[r].view(np.int16)).view(torch.float16).float()
         err = float((outs["out"][r].float() - ref).abs().max() / ref.abs().max())
         assert err <= 5e-3, (r, err)
+
+
+@pytest.mark.parametrize("op", ["mm_rs", "mm_ar"])
+def test_split_k_reduce_ops_row_bias_and_rank_inner(op):
+    """Per-row bias (each rank's, added with its first chunk) and a request
+    for the rank-fastest item order, which a split overrides: exact."""
+    W, M, N, K = 2, 300, 256, 4096
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "f16", seed=4800, dist="int", scale=1, bias=True, bias_scale=3,
+                                    bias_len=M)
+    want = (oracle.matmul_reduce_scatter(x.A, x.B, x.bias, bias_on_m=True) if op == "mm_rs"
+            else [oracle.matmul_all_reduce(x.A, x.B, x.bias, bias_on_m=True)])
+    prob = FusedProblem(op, W, M, N, K, "f16", bias=True, bias_on_m=True, config={"k_split": 3, "rank_inner": 1})
+    prob.upload(x.A, x.B, x.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    outs = prob.outputs()
+    for r in range(W if op == "mm_rs" else 1):
+        assert_exact(bits(outs["out"][r]), want[r])
