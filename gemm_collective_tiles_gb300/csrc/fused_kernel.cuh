@@ -301,15 +301,16 @@ __device__ __forceinline__ bool drain_bar(const Ctl& c, uint64_t* bar, uint32_t 
     return true;
 }
 
-// Split-K (all_gather_matmul and the chained reduce ops): each output tile's
-// K range is cut into p.split chunks of p.kb_chunk K blocks; chunk j of a
-// tile (of a rank) is a GEMM item of its own, and all partials are summed
-// through the chained reduce in (rank, chunk) order, so the tiles running at
-// once stay short and share their operand blocks in L2.
+// Split-K (every fused op): each output tile's K range is cut into p.split
+// chunks of p.kb_chunk K blocks; chunk j of a tile (of a rank) is a GEMM item
+// of its own, and the partials are summed through the chained reduce, in
+// (rank, chunk) order for the reduce ops and in chunk order otherwise, so the
+// tiles running at once stay short and share their operand blocks in L2.
 __device__ __forceinline__ bool split_k(const Params& p) { return p.split > 1; }
+__device__ __forceinline__ bool reduce_op_of(const Params& p) { return p.op == OP_MM_RS || p.op == OP_MM_AR; }
 // the links of a tile's reduce chain: W ranks (reduce ops) x the K chunks
 __device__ __forceinline__ int chain_ranks(const Params& p) {
-    return (p.op == OP_AG_MM ? 1 : p.W) * max(1, p.split);
+    return (reduce_op_of(p) ? p.W : 1) * max(1, p.split);
 }
 
 // GROUP_M swizzle: linear output-tile id -> (m block, n block).  Tiles run
@@ -371,7 +372,7 @@ __device__ __forceinline__ GemmCoord decode_gemm(const Params& p, uint32_t item)
         const int S = max(1, p.split);
         gc.link = link;
         gc.chunk = link % S;
-        gc.rank = p.op == OP_AG_MM ? 0 : link / S;
+        gc.rank = reduce_op_of(p) ? link / S : 0;  // matmul_all_gather: set from the m-block below
     } else {
         gc.tile = g;
         gc.rank = 0;
@@ -1387,6 +1388,12 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     constexpr int COLS = BN * 4 / NUM_WORKER_WARPS;
     constexpr int NCH = COLS / 32;
     const int c_row = blk * BM + wc.q * 32;
+    // matmul_all_gather (split-K): the running sum holds every rank's rows
+    // (block coordinate = the rank), and its tiles are counted per rank
+    const int s_blk = p.op == OP_MM_AG ? gc.rank : 0;
+    // (a valid block is below ceil(M_l / BM): blocks past the rank's rows
+    // leave before the counter is touched)
+    const int cblk = p.op == OP_MM_AG ? gc.rank * ((p.M + BM - 1) / BM) + blk : blk;
     // a column half of a split tail tile (only the last rank's tiles are split)
     const int colbase = gc.nb * BN + (gc.hn >= 0 ? gc.hn * (BN / 2) : 0) + wc.h * COLS;
     // number of 32-column chunks inside the matrix (N is a multiple of 32 here)
@@ -1395,13 +1402,13 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     if (gc.link == R - 1 && gc.link > 0 && blk * BM < p.M && wc.lane == 0) {
         // the last rank will read this warp's running-sum rows: pull them into
         // L2 while the tile's MMAs still run
-        for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, 0, 0);
+        for (int ci = 0; ci < nch; ++ci) tma_prefetch_l2_4d(&p.tmS, colbase + ci * 32, c_row, s_blk, 0);
     }
     const int s = gc.link;
     // the reduce ops add each rank's own bias, all_gather_matmul its one bias
     // (region 0); with split-K, with the rank's first chunk
     const bool add_bias = p.has_bias && gc.chunk == 0;
-    const int bias_region = p.op == OP_AG_MM ? 0 : gc.rank;
+    const int bias_region = reduce_op_of(p) ? gc.rank : 0;
     const char* bias_base =
         add_bias ? p.heap + static_cast<size_t>(bias_region) * p.rank_stride + p.off_bias : nullptr;
     // per-column bias of the warp's columns, fetched while the MMAs still run:
@@ -1426,8 +1433,8 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     if (add_bias && p.bias_on_m && row < p.M)
         row_bias = bits16_to_float(reinterpret_cast<const uint16_t*>(bias_base)[row], p.bf16);
     // one counter per BM-row block and column block
-    unsigned long long* ctr = (p.op == OP_AG_MM ? p.chain : reinterpret_cast<unsigned long long*>(p.flags)) +
-                              (blk * p.n_blocks + gc.nb);
+    unsigned long long* ctr = (reduce_op_of(p) ? reinterpret_cast<unsigned long long*>(p.flags) : p.chain) +
+                              (cblk * p.n_blocks + gc.nb);
     const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
     if (s > 0) {
         int ok = 1;
@@ -1442,7 +1449,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         // the staging half must be free: earlier stores have read it
         bulk_wait_read_all();
         mbar_arrive_expect_tx(&lbar[ci & 1], 32 * 32 * 4);
-        tma_load_4d(stg_base + (ci & 1) * 4096, &p.tmS, colbase + ci * 32, c_row, 0, 0, &lbar[ci & 1]);
+        tma_load_4d(stg_base + (ci & 1) * 4096, &p.tmS, colbase + ci * 32, c_row, s_blk, 0, &lbar[ci & 1]);
     };
     // only the last rank reads the running sum: the middle ranks add their
     // partial into it at the L2 (TMA reduce-add), in the same rank order
@@ -1531,11 +1538,11 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         __syncwarp();
         if (wc.lane == 0) {
             if (!last && s == 0) {
-                if (p.sum_l2_policy) tma_store_4d_hint(&p.tmS, stg, col0, c_row, 0, 0, spol);
-                else tma_store_4d(&p.tmS, stg, col0, c_row, 0, 0);
+                if (p.sum_l2_policy) tma_store_4d_hint(&p.tmS, stg, col0, c_row, s_blk, 0, spol);
+                else tma_store_4d(&p.tmS, stg, col0, c_row, s_blk, 0);
             } else if (!last) {
-                if (p.sum_l2_policy) tma_reduce_add_4d_hint(&p.tmS, stg, col0, c_row, 0, 0, spol);  // S += P_s
-                else tma_reduce_add_4d(&p.tmS, stg, col0, c_row, 0, 0);  // S += P_s
+                if (p.sum_l2_policy) tma_reduce_add_4d_hint(&p.tmS, stg, col0, c_row, s_blk, 0, spol);  // S += P_s
+                else tma_reduce_add_4d(&p.tmS, stg, col0, c_row, s_blk, 0);  // S += P_s
             } else if (p.op == OP_MM_RS) {
                 const int rr = col0 / p.N_local;
                 if (p.out_evict_first)
@@ -1543,10 +1550,14 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
                 else
                     tma_store_4d(&p.tmC, stg, col0 - rr * p.N_local, c_row, rr, 0);
             } else {
+                // all-reduce / all_gather_matmul: row block 0; matmul_all_gather:
+                // the rank's block of the gathered output
                 const int nreg = p.replicate ? p.W : 1;
                 for (int rg = 0; rg < nreg; ++rg) {
-                    if (p.out_evict_first) tma_store_4d_hint(&p.tmC, stg, col0, c_row, 0, rg, l2_policy_evict_first());
-                    else tma_store_4d(&p.tmC, stg, col0, c_row, 0, rg);
+                    if (p.out_evict_first)
+                        tma_store_4d_hint(&p.tmC, stg, col0, c_row, s_blk, rg, l2_policy_evict_first());
+                    else
+                        tma_store_4d(&p.tmC, stg, col0, c_row, s_blk, rg);
                 }
             }
             bulk_commit();

@@ -335,10 +335,14 @@ WsLayout ws_layout(iris_op op, int64_t M, int64_t N, int W, int tile_n, int redu
         // 8-byte ready counters per (128-row block, shard); split-K: then one
         // 8-byte chained-reduce counter per tile
         L.n_flags = 2 * static_cast<size_t>(W) * mb + (split > 1 ? 2 * static_cast<size_t>(mb) * nb : 0);
+    else if (op == IRIS_OP_MATMUL_ALL_GATHER && split > 1)
+        // split-K: one 8-byte chained-reduce counter per (rank, 128-row block, tile column)
+        L.n_flags = 2 * static_cast<size_t>(W) * static_cast<size_t>(cdiv(M / std::max(W, 1), BM)) * nb;
     else if (reduce_op)
         L.n_flags = static_cast<size_t>(std::max(W, 2)) * mb * nb;  // also 8-byte tile counters
     L.partial_off = round_up(L.flags_off + L.n_flags * 4, 256);
-    if (reduce_op || (op == IRIS_OP_ALL_GATHER_MATMUL && split > 1)) L.partial_elems = static_cast<size_t>(M) * N;
+    if (reduce_op || ((op == IRIS_OP_ALL_GATHER_MATMUL || op == IRIS_OP_MATMUL_ALL_GATHER) && split > 1))
+        L.partial_elems = static_cast<size_t>(M) * N;
     // one fp32 running sum (chained) or one fp32 partial per rank
     const size_t copies = L.partial_elems ? ((reduce_mode == 3 || !reduce_op) ? 1 : W) : 0;
     L.total = round_up(L.partial_off + L.partial_elems * 4 * copies, 256);
@@ -591,14 +595,16 @@ bool dims_ok(int64_t M, int64_t N, int64_t K) {
 
 int prepare_ws(Params& p, void* ws, size_t ws_bytes, iris_op op, int64_t M, int64_t N, int W,
                const Cfg& c) {
-    const int split = (op == IRIS_OP_ALL_GATHER_MATMUL && p.split > 1) ? p.split : 1;
+    const int split = ((op == IRIS_OP_ALL_GATHER_MATMUL || op == IRIS_OP_MATMUL_ALL_GATHER) && p.split > 1) ? p.split : 1;
     const WsLayout L = ws_layout(op, M, N, W, c.tile_n, c.reduce_mode, split);
     if (!ws || ws_bytes < L.total) return IRIS_ENOWS;
     if (!aligned16(reinterpret_cast<uintptr_t>(ws))) return IRIS_EALIGN;
     p.ws = reinterpret_cast<WsHeader*>(ws);
     p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.flags_off);
-    // split-K: the chained-reduce counters follow the W x m-block gather counters
-    p.chain = reinterpret_cast<unsigned long long*>(p.flags) + static_cast<size_t>(W) * cdiv(M, BM);
+    // split-K: the chained-reduce counters (all_gather_matmul: after the W x
+    // m-block gather counters)
+    p.chain = reinterpret_cast<unsigned long long*>(p.flags) +
+              (op == IRIS_OP_ALL_GATHER_MATMUL ? static_cast<size_t>(W) * cdiv(M, BM) : 0);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partial_off);
     p.partial_elems = L.partial_elems;
     return IRIS_OK;
@@ -647,13 +653,15 @@ int iris_b200_workspace_size(iris_op op, int64_t M, int64_t N, int64_t K, int wo
         if (mode < 0) return IRIS_EINVAL;
     }
     int split = 1;
-    if (op == IRIS_OP_ALL_GATHER_MATMUL) {
+    if (op == IRIS_OP_ALL_GATHER_MATMUL || op == IRIS_OP_MATMUL_ALL_GATHER) {
         // sized for CTA pairs wherever the config allows them (a launch that
         // ends up on one-CTA tiles does not split and uses less)
         const int ks = cfg ? cfg->k_split : 0;
         if (ks < 0 || ks > 4096) return IRIS_EINVAL;
         const bool pairs = !(cfg && (cfg->tile_m == BM || (cfg->tile_n != 0 && cfg->tile_n != 256))) && N > 128;
-        split = resolve_split(ks, pairs, M, N, K).split;
+        const int64_t rows = op == IRIS_OP_MATMUL_ALL_GATHER ? M / world : M;
+        split = resolve_split(ks, pairs, rows, N, K).split;
+        if (op == IRIS_OP_MATMUL_ALL_GATHER && split > 1) Mrows = M;  // counters and the running sum
     }
     *bytes = ws_layout(op, Mrows, N, world, tile_n, mode, split).total;
     return IRIS_OK;
@@ -861,7 +869,8 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     Cfg c;
     if ((rc = resolve_cfg(cfg, IRIS_OP_MATMUL_ALL_GATHER, N, c))) return rc;
     if ((rc = resolve_pair(c, IRIS_OP_MATMUL_ALL_GATHER))) return rc;
-    resolve_stages(c, K);
+    const SplitK sk = resolve_split(c.k_split, c.cg == 2, M_l, N, K);
+    resolve_stages(c, sk.split > 1 ? int64_t(sk.kb_chunk) * BK : K);
     if ((rc = check_region(heap, off_A, size_t(M_l) * K * 2))) return rc;
     if ((rc = check_region(heap, off_B, size_t(K) * N * 2))) return rc;
     if ((rc = check_region(heap, off_out, size_t(M) * N * 2))) return rc;
@@ -884,8 +893,21 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     p.has_bias = has_bias;
     p.n_gemm = (M_l > 0 && N > 0) ? static_cast<uint32_t>(p.n_tiles) : 0u;
     p.n_comm = 0;
-    tail_split(p, c, false);
-    if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_MATMUL_ALL_GATHER, 0, N, W, c))) return rc;
+    if (sk.split > 1) {
+        // chunk j of every tile is an item; the chunks' partials are summed in
+        // chunk order by the chained reduce (a running sum of all W x M_l rows)
+        if (uint64_t(p.n_gemm) * sk.split >= 0x7FFFFFFFull) return IRIS_EINVAL;
+        p.split = sk.split;
+        p.kb_chunk = sk.kb_chunk;
+        p.n_gemm *= static_cast<uint32_t>(sk.split);
+        p.reduce_mode = 3;
+        p.rank_inner = 0;
+        p.g_split = p.n_gemm;
+    } else {
+        tail_split(p, c, false);
+    }
+    if ((rc = prepare_ws(p, workspace, workspace_bytes, IRIS_OP_MATMUL_ALL_GATHER, p.split > 1 ? M : 0, N, W, c)))
+        return rc;
     if (p.n_gemm > 0 && K > 0) {
         if ((rc = make_map(&p.tmA, p.heap + off_A, p.bf16, K, M_l, W, K * 2, heap->rank_stride, BK, BM))) return rc;
         if ((rc = make_a_chunk_map(p, c, p.heap + off_A, M_l, K, W, heap->rank_stride))) return rc;
@@ -896,6 +918,10 @@ int iris_b200_matmul_all_gather(const iris_b200_heap* heap, size_t off_A, size_t
     }
     if (p.n_gemm > 0 && (rc = make_out_map(&p.tmC, p.heap + off_out, p.bf16, N, M_l, W, W, N * 2,
                                            size_t(M_l) * N * 2, heap->rank_stride)))
+        return rc;
+    // split-K: the fp32 running sum, one block of M_l rows per rank
+    if (p.split > 1 && (rc = make_out_map(&p.tmS, p.partials, 2, N, M_l, W, 1, N * 4, size_t(M_l) * N * 4,
+                                          size_t(M) * N * 4)))
         return rc;
     return launch(p, c, stream);
 }

@@ -162,7 +162,8 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     # the CTA-pair pipeline the default does not pick for this K (three
     # 128-deep stages up to K = 98304, six 64-deep stages beyond)
     # (a split all_gather_matmul picks it by the K of one chunk)
-    splits = op in ("all_gather_matmul", "matmul_reduce_scatter", "matmul_all_reduce") and N % 32 == 0
+    splits = op in ("all_gather_matmul", "matmul_reduce_scatter", "matmul_all_reduce",
+                    "matmul_all_gather") and N % 32 == 0
     k_item = 16384 if (splits and K > 32768) else K
     out.append({"stages": 3 if k_item > 98304 else 6})
     # the swizzle widths the default does not use (32; 16 in the concurrent

@@ -206,15 +206,15 @@ typedef struct {
                               fp32 running-sum stores and reduce-adds.  0 =
                               default (none), 1 = evict first, 2 = evict last,
                               3 = none. */
-    int k_split;           /* all_gather_matmul, and matmul_reduce_scatter /
-                              matmul_all_reduce with the chained reduce, on CTA
-                              pairs (N % 32 == 0): K chunks per output tile (of
-                              each rank).  Chunk j of a tile is a GEMM item of
-                              its own; all partials are summed in (rank, chunk)
-                              order through the fp32 running sum in the
-                              workspace (for all_gather_matmul M x N fp32 more,
-                              counted by iris_b200_workspace_size) before the
-                              one rounding to 16 bits.  0 = default: chunks of about 16384
+    int k_split;           /* the fused ops on CTA pairs (N % 32 == 0; the
+                              reduce ops with the chained reduce): K chunks per
+                              output tile (of each rank).  Chunk j of a tile is
+                              a GEMM item of its own; all partials are summed
+                              in (rank, chunk) order through an fp32 running
+                              sum in the workspace (all_gather_matmul and
+                              matmul_all_gather: M x N fp32 more, counted by
+                              iris_b200_workspace_size) before the one rounding
+                              to 16 bits.  0 = default: chunks of about 16384
                               K when K > 32768 (shorter tiles keep the tiles
                               running at once on nearby K, where they share
                               their operand blocks in L2), else none; 1 = none;

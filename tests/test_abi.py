@@ -204,3 +204,20 @@ def test_split_k_workspace():
     bad = gct.make_config(k_split=-1)
     assert lib.iris_b200_workspace_size(N.IRIS_OP_ALL_GATHER_MATMUL, 256, 256, 65536, W, N.IRIS_BF16,
                                         ctypes.byref(bad), ctypes.byref(out)) == N.IRIS_EINVAL
+
+
+def test_split_k_workspace_matmul_all_gather():
+    """matmul_all_gather needs no workspace beyond the header unless it
+    splits K; then one 8-byte counter per (rank, 128-row block, tile column)
+    and a running sum of all W x M_l rows."""
+    lib = N.load()
+    out = ctypes.c_size_t(0)
+    W, M, Nn, K = 4, 4 * 1024, 1024, 65536
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_ALL_GATHER, M, Nn, K, W, N.IRIS_BF16, None,
+                                        ctypes.byref(out)) == 0
+    flags = 2 * W * (1024 // 128) * (Nn // 256) * 4
+    assert out.value == ((256 + flags + 255) // 256) * 256 + M * Nn * 4
+    cfg = gct.make_config(k_split=1)
+    assert lib.iris_b200_workspace_size(N.IRIS_OP_MATMUL_ALL_GATHER, M, Nn, K, W, N.IRIS_BF16, ctypes.byref(cfg),
+                                        ctypes.byref(out)) == 0
+    assert out.value == 256

@@ -1,4 +1,4 @@
-"""Split-K all_gather_matmul and reduce ops against the oracle.
+"""Split-K for every fused op against the oracle.
 
 With k_split > 1 (by default above K = 32768) every output tile's K range is
 cut into chunks; chunk j of a tile is a GEMM item of its own, and the chunks'
@@ -188,3 +188,48 @@ def test_split_k_reduce_ops_row_bias_and_rank_inner(op):
     outs = prob.outputs()
     for r in range(W if op == "mm_rs" else 1):
         assert_exact(bits(outs["out"][r]), want[r])
+
+
+# matmul_all_gather: rank r's M_l rows land at rows r * M_l of the output; with
+# split-K every rank's tiles chain over the K chunks through a running sum of
+# all W x M_l rows.  M_l = 100 and 300 leave the last pair tile of every rank
+# half or partly empty.
+MM_AG_CASES = [(4, 4 * 100, 256, 4096, 4), (2, 2 * 300, 512, 8192, 3), (8, 8 * 256, 288, 2048, 16)]
+
+
+@pytest.mark.parametrize("W,M,N,K,ks", MM_AG_CASES)
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_split_k_matmul_all_gather_exact_integer(W, M, N, K, ks, dt):
+    x = synthetic.make_fused_inputs("mm_ag", W, M, N, K, dt, seed=4900 + M + N + ks, dist="int", scale=1,
+                                    bias=True, bias_scale=3)
+    want = oracle.matmul_all_gather(x.A, x.B[0], x.bias)
+    outs = run_reduce(x, {"k_split": ks})
+    assert_exact(bits(outs["out"][0]), want)
+
+
+def test_split_k_matmul_all_gather_schedules():
+    """Replicated outputs, per-row bias, a grid of one pair, and random inputs
+    within the GEMM tolerance (fp16 outputs)."""
+    W, M, N, K = 2, 2 * 300, 256, 8192
+    x = synthetic.make_fused_inputs("mm_ag", W, M, N, K, "f16", seed=4950, dist="int", scale=1, bias=True,
+                                    bias_scale=3)
+    want = oracle.matmul_all_gather(x.A, x.B[0], x.bias)
+    for extra in ({"replicate_outputs": 1}, {"grid": 2}):
+        outs = run_reduce(x, {"k_split": 4, **extra})
+        for r in range(W if extra.get("replicate_outputs") else 1):
+            assert_exact(bits(outs["out"][r]), want)
+    y = synthetic.make_fused_inputs("mm_ag", W, M, N, K, "f16", seed=4951, dist="int", scale=1, bias=True,
+                                    bias_scale=3, bias_len=M // W)
+    want = oracle.matmul_all_gather(y.A, y.B[0], y.bias, bias_on_m=True)
+    prob = FusedProblem("mm_ag", W, M, N, K, "f16", bias=True, bias_on_m=True, config={"k_split": 4})
+    prob.upload(y.A, y.B, y.bias)
+    prob.poison_outputs()
+    prob.run()
+    assert query_status(prob.ws)[0] == 0
+    assert_exact(bits(prob.outputs()["out"][0]), want)
+    z = synthetic.make_fused_inputs("mm_ag", W, M, N, K, "f16", seed=4952, dist="normal", scale=0.5, bias=True)
+    want = oracle.matmul_all_gather(z.A, z.B[0], z.bias)
+    ref = torch.from_numpy(want.view(np.int16)).view(torch.float16).float()
+    got = run_reduce(z, {"k_split": 4})["out"][0].float()
+    err = float((got - ref).abs().max() / ref.abs().max())
+    assert err <= 5e-3, err

@@ -68,13 +68,13 @@ def test_candidates():
     assert {"reduce_mode": 1} in r and {"reduce_mode": 2} in r
     assert len(tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)) == 3
     # the CTA-pair pipeline the default does not pick for the K one item runs
-    # is tried early: all_gather_matmul and the reduce ops split K above 32768
-    # into chunks of ~16384 (so the three-stage default), matmul_all_gather
-    # does not
+    # is tried early: every fused op splits K above 32768 into chunks of
+    # ~16384 (so the three-stage default) when N is a multiple of 32
     short_k = tuning.candidates("all_gather_matmul", 8, 4096, 14336, 4096, 152, top_k=3)
     split_k = tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152, top_k=3)
-    assert tuning.candidates("matmul_all_reduce", 8, 4096, 4096, 131072, 152, top_k=3)[1] == {"k_split": 1}
-    long_k = tuning.candidates("matmul_all_gather", 8, 4096, 4096, 131072, 152, top_k=3)
+    for op in ("matmul_all_reduce", "matmul_reduce_scatter", "matmul_all_gather"):
+        assert tuning.candidates(op, 8, 4096, 4096, 131072, 152, top_k=3)[1] == {"k_split": 1}
+    long_k = tuning.candidates("matmul_all_gather", 8, 4096, 4104, 131072, 152, top_k=3)
     assert {"stages": 6} in short_k and {"stages": 3} not in short_k
     assert {"k_split": 1} in split_k and {"stages": 6} in split_k and {"stages": 3} not in split_k
     assert {"stages": 3} in long_k and {"stages": 6} not in long_k
