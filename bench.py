@@ -446,7 +446,7 @@ def concurrent_measure(cfg, steps, warm, sweep=False, two_stream=False):
     if sweep:
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         pts = {}
-        for frac in (0.25, 0.35, 0.45, 0.55, 0.65, 0.75, 0.85, 0.9):
+        for frac in (0.25, 0.35, 0.45, 0.55, 0.65, 0.7, 0.75, 0.85, 0.9):
             conf = dict(cfg)
             conf["gemm_ctas"] = max(1, int(round(frac * sms)))
             pr = make(conf)

@@ -76,6 +76,7 @@ class iris_b200_config(ctypes.Structure):
         ("out_l2_hint", ctypes.c_int),
         ("sum_l2_hint", ctypes.c_int),
         ("k_split", ctypes.c_int),
+        ("coll_out_stage", ctypes.c_int),
     ]
 
 

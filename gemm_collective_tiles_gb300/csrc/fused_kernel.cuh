@@ -146,6 +146,7 @@ struct Params {
     int coll_path;                     // concurrent collectives: 1 TMA, 2 TMA loads + register stores,
                                        // 3 one 3-D TMA box per sub-chunk for all W sources
     int coll_box_rows;                 // coll_path 3: 1 KB rows per source in one box (R)
+    int coll_out_stage;                // summing collectives: 0 staged for all-reduce, 1 in place, 2 staged
     int gather_parts;                  // all_gather_matmul: gather items (row parts) per (row block, shard)
     int gemm_evict_last;               // CTA-pair operand loads carry an L2 evict-last policy
     int out_evict_first;               // final 16-bit output stores carry an L2 evict-first policy
@@ -1800,10 +1801,15 @@ __device__ __forceinline__ CollRange coll_range(const Params& p, uint32_t c) {
 // ring of p.coll_ring buffers; for each sub-chunk of its slice of tile c it
 // bulk-loads the sources (all W ranks for all-reduce / reduce-scatter, rank s
 // for all-gather) into the next buffer while earlier ones are summed in rank
-// order (fp32) and bulk-stored to the destinations.  While a warp waits for
-// a sub-chunk, up to coll_ring loads are in flight.  With p.coll_evict_first the copies carry an L2
-// evict-first policy, so the streamed collective data does not push the
-// concurrent GEMM's operands out of the L2.
+// order (fp32) and bulk-stored to the destinations.  Staged (the default
+// for all-reduce, whose stores go to every region), a sub-chunk that fits
+// half of the warp's 8 KB staging buffer is summed into that half (the two
+// halves alternate), so the load buffer takes its next load right after the
+// sum and all coll_ring loads stay in flight; otherwise the sum stays in the
+// load buffer, which is refilled once the stores have read it (coll_ring - 1
+// loads in flight).  With p.coll_evict_first the copies
+// carry an L2 evict-first policy, so the streamed collective data does not
+// push the concurrent GEMM's operands out of the L2.
 template <int BN, int STAGES, int CG>
 __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t c, WorkerCtx& wc) {
     constexpr uint32_t AREA = STAGES * Smem<BN, STAGES, CG>::STAGE_BYTES / NUM_WORKER_WARPS;
@@ -1836,6 +1842,31 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         if (hint) bulk_store_hint(g, s, n, pol);
         else bulk_store(g, s, n);
     };
+    // lane 0: bulk-store n bytes at byte offset o of the slice from smem `from`
+    // to every destination of the collective, as one bulk group
+    auto store_out = [&](const uint8_t* from, size_t o, uint32_t n) {
+        if (p.coll == COLL_RS) {
+            // the item may cross a rank boundary: split the store there
+            size_t done = 0;
+            while (done < n) {
+                const size_t e = b0 + o + done;  // byte index into the summed vector
+                const int rr = static_cast<int>(e / cw_bytes);
+                const size_t piece = min(static_cast<size_t>(n) - done, (rr + 1) * cw_bytes - e);
+                store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
+                      from + done, static_cast<uint32_t>(piece));
+                done += piece;
+            }
+        } else if (dst_all) {
+            for (int r = 0; r < p.W; ++r) store(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + o, from, n);
+        } else {
+            store(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base + o, from, n);
+        }
+        bulk_commit();
+    };
+    constexpr uint32_t OUT_HALF = Smem<BN, STAGES, CG>::STAGE_OUT_BYTES / 2;
+    const bool staged = src_n > 1 && p.coll_path != 2 && sub <= OUT_HALF &&
+                        (p.coll_out_stage == 2 || (p.coll_out_stage == 0 && p.coll == COLL_AR));
+    uint8_t* const outb = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
     // load sub-chunk i into buffer i % nb (whose earlier store has read it)
     auto issue = [&](int i) {
         const size_t o = s_lo + static_cast<size_t>(i) * sub;
@@ -1858,16 +1889,20 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
         }
     };
     int issued = 0;  // lane 0: sub-chunks whose loads were issued
-    if (wc.lane == 0)
-        for (; issued < min(nb - 1, nsub); ++issued) issue(issued);
+    if (wc.lane == 0) {
+        // staged: an earlier epilogue's stores may still read the staging buffer
+        if (staged) bulk_wait_read_all();
+        for (; issued < min(staged ? nb : nb - 1, nsub); ++issued) issue(issued);
+    }
     int i = 0;
     bool ok = true;
     for (; i < nsub; ++i) {
         int got = 1;
         if (wc.lane == 0) {
-            // keep nb loads in flight: the next one goes into the buffer of
-            // sub-chunk i - 1, whose store (the newest group) must have read it
-            if (issued < nsub) {
+            // in place: keep nb - 1 loads in flight; the next one goes into
+            // the buffer of sub-chunk i - 1, whose stores (the newest group)
+            // must have read it
+            if (!staged && issued < nsub) {
                 bulk_wait_read_all();
                 issue(issued);
                 ++issued;
@@ -1916,6 +1951,37 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
             __syncwarp();  // the buffer is free for the next load once every lane has read it
             continue;
         }
+        if (staged) {
+            // this staging half was last stored from two sub-chunks ago: its
+            // group (every group but the newest) has finished reading it
+            if (wc.lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            uint8_t* ob = outb + (i & 1) * OUT_HALF;
+            for (uint32_t q = wc.lane; q < n / 16; q += 32) {
+                float4 a = *reinterpret_cast<const float4*>(buf + q * 16);
+                for (int r = 1; r < src_n; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(buf + r * sub + q * 16);
+                    a.x = a.x + v.x;
+                    a.y = a.y + v.y;
+                    a.z = a.z + v.z;
+                    a.w = a.w + v.w;
+                }
+                *reinterpret_cast<float4*>(ob + q * 16) = a;
+            }
+            // the sums are visible to the stores, and the lanes' reads of the
+            // load buffer are ordered before the load that refills it
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (wc.lane == 0) {
+                store_out(ob, o, n);
+                if (issued < nsub) {
+                    issue(issued);  // into buffer i % nb, just summed
+                    ++issued;
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         if (src_n > 1) {
             // rank-order fp32 sum into the rank-0 slot
             for (uint32_t q = wc.lane; q < n / 16; q += 32) {
@@ -1932,25 +1998,7 @@ __device__ bool coll_tile_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, 
             fence_proxy_async_shared();
         }
         __syncwarp();
-        if (wc.lane == 0) {
-            if (p.coll == COLL_RS) {
-                // the item may cross a rank boundary: split the store there
-                size_t done = 0;
-                while (done < n) {
-                    const size_t e = b0 + o + done;  // byte index into the summed vector
-                    const int rr = static_cast<int>(e / cw_bytes);
-                    const size_t piece = min(static_cast<size_t>(n) - done, (rr + 1) * cw_bytes - e);
-                    store(p.heap + static_cast<size_t>(rr) * p.rank_stride + p.off_cout + (e - rr * cw_bytes),
-                          buf + done, static_cast<uint32_t>(piece));
-                    done += piece;
-                }
-            } else if (dst_all) {
-                for (int r = 0; r < p.W; ++r) store(p.heap + static_cast<size_t>(r) * p.rank_stride + dst_base + o, buf, n);
-            } else {
-                store(p.heap + static_cast<size_t>(dst_region) * p.rank_stride + dst_base + o, buf, n);
-            }
-            bulk_commit();
-        }
+        if (wc.lane == 0) store_out(buf, o, n);
         __syncwarp();
     }
     if (!ok && wc.lane == 0) {

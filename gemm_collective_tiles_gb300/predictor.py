@@ -196,7 +196,7 @@ def predict_split(wl: Workload, candidates: Optional[Sequence[int]] = None, m: O
     floor = comm_floor(wl.coll, sms=m.sms)
     if candidates is None:
         candidates = sorted({max(1, int(round(f * m.sms))) for f in
-                             (0.25, 0.35, 0.45, 0.5, 0.55, 0.6, 0.65, 0.75, 0.85, 0.9)})
+                             (0.25, 0.35, 0.45, 0.5, 0.55, 0.6, 0.65, 0.7, 0.75, 0.85, 0.9)})
     ranked = []
     for g in candidates:
         if wl.comm_tiles() > 0 and m.sms - g < floor:

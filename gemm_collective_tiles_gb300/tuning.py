@@ -28,7 +28,7 @@ ENV_CACHE = "IRIS_B200_CACHE"
 TUNABLE = ("tile_m", "tile_n", "group_m", "gemm_ctas", "reduce_mode", "rank_inner", "comm_block", "stages",
            "coll_ring", "coll_l2_hint", "coll_path", "gather_parts",
            "startup_gather", "gemm_l2_hint", "out_l2_hint",
-           "sum_l2_hint", "k_split")
+           "sum_l2_hint", "k_split", "coll_out_stage")
 
 # nearest-shape matching: largest accepted distance, in log2 units over the
 # problem sizes (1.0 = one size off by a factor of 2, or two by 2^0.7 each)
@@ -191,7 +191,7 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
             # (tile, split) pairs ranked by the work-stealing makespan model
             return concurrent_candidates(M, N, K, coll, W, count, sm_count, top_k)
         else:
-            for frac in (0.65, 0.55, 0.75, 0.45, 0.85):
+            for frac in (0.7, 0.6, 0.8, 0.5, 0.85):
                 out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
     # drop duplicates, keep order
     seen, uniq = set(), []

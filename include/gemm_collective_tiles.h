@@ -111,7 +111,7 @@ typedef struct {
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
                               other queue when its own runs dry.  0 = op default
-                              (concurrent: 65% of the grid; the dependent ops: all
+                              (concurrent: 70% of the grid; the dependent ops: all
                               CTAs); -1 = balanced (every CTA draws from both queues
                               so that both finish together). */
     int stages;            /* CTA-pair tiles: shared-memory pipeline (192 KB either
@@ -219,6 +219,18 @@ typedef struct {
                               running at once on nearby K, where they share
                               their operand blocks in L2), else none; 1 = none;
                               n = n chunks. */
+    int coll_out_stage;    /* concurrent all-reduce and reduce-scatter: where a
+                              worker warp sums a sub-chunk of its W sources
+                              before storing it.  Staged: into its own 4 KB
+                              staging halves (when a sub-chunk fits, e.g. the
+                              3 KB of W = 8 with the default ring), so the
+                              load buffer is refilled right after the sum and
+                              all coll_ring loads stay in flight.  In place:
+                              in the load buffer, refilled once the stores
+                              have read it.  0 = default (staged for
+                              all-reduce, whose stores go to all W regions; in
+                              place for reduce-scatter), 1 = in place,
+                              2 = staged. */
 } iris_b200_config;
 
 /* Symmetric heap: W regions of rank_stride bytes starting at base (device memory). */

@@ -253,6 +253,37 @@ def test_concurrent_collective_bit_exact(coll, gemm_ctas):
             assert np.array_equal(out["x"][r].contiguous().view(torch.uint8).numpy(), want)
 
 
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter"])
+@pytest.mark.parametrize("W", [4, 8, 16])
+@pytest.mark.parametrize("stage", [1, 2])
+def test_concurrent_sum_in_place_or_staged_bit_exact(coll, W, stage):
+    """The summing collectives with the sums in the load buffer (1) or in the
+    warp's staging halves (2; applies where a sub-chunk fits 4 KB: W = 8 and
+    16 with the default ring, not W = 4), over several items per warp so
+    both staging halves and both load buffers are reused; with one and three
+    ring buffers too."""
+    count = W * (5 * 16384 + 1024)   # items of 64Ki elements cross the reduce-scatter slices
+    M, N, K = 256, 256, 128
+    A, B = synthetic.make_gemm_inputs(M, N, K, "bf16", seed=69, dist="int", scale=3)
+    X = synthetic.make_coll_inputs(W, count, "f32", seed=70 + W)
+    want = oracle.all_reduce(X) if coll == "all_reduce" else oracle.reduce_scatter(X)
+    for ring in (2, 1, 3):
+        prob = ConcurrentProblem(M, N, K, "bf16", coll, W, count,
+                                 config={"comm_block": 65536, "gemm_ctas": 30, "coll_out_stage": stage,
+                                         "coll_ring": ring})
+        prob.upload(A, B, X)
+        prob.poison_outputs()
+        prob.run()
+        torch.cuda.synchronize()
+        from gemm_collective_tiles_gb300 import query_status
+        assert query_status(prob.ws)[0] == 0
+        out = prob.outputs()
+        assert_exact(bits(out["C"]), oracle.gemm(A, B))
+        for r in range(W):
+            w = want if coll == "all_reduce" else want[r]
+            assert np.array_equal(out["x"][r].numpy().view(np.uint32), w.view(np.uint32)), (ring, r)
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_concurrent_all_to_all_and_broadcast_bit_exact(dt):
     W = 8
