@@ -122,3 +122,27 @@ def test_ranking_against_measured_sweeps():
             n = len(keys)
             rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
             assert rho >= 0.8, (tile, rho)
+
+
+def test_ranking_against_staged_sweeps():
+    """The sweeps measured after the all-reduce sums moved into the staging
+    buffers, with 106 GEMM CTAs among the points: the model's best split (99)
+    is not the measured best (106), but it costs at most 3 % over it, and
+    the rank correlation over the nine points stays high."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "concurrent_sweeps.json")))
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    tk = next(t for t in P.TILE_KINDS if t.name == "pair3")
+    for sweep in g["staged_sums"]["sweeps"]:
+        keys = sorted(sweep)
+        pred = {k: P.simulate(wl, int(k), P.Machine(), tk) for k in keys}
+        best_pred, best = min(pred, key=pred.get), min(sweep.values())
+        assert sweep[best_pred] <= 1.03 * best, (best_pred, sweep[best_pred], best)
+
+        def ranks(d):
+            return {k: i for i, k in enumerate(sorted(keys, key=lambda k: d[k]))}
+        rp, rm = ranks(pred), ranks(sweep)
+        n = len(keys)
+        rho = 1.0 - 6.0 * sum((rp[k] - rm[k]) ** 2 for k in keys) / (n * (n * n - 1))
+        assert rho >= 0.8, rho
