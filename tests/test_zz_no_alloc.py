@@ -103,6 +103,28 @@ def test_noalloc_call_after_a_stopped_call_is_exact():
     assert np.array_equal(_bits(got["out"][0]), want_out)
 
 
+def test_noalloc_graph_replays_exact():
+    # captured once in a CUDA graph (the scratch clear is a memset node, the
+    # epoch lives in the static array) and replayed three times
+    W, M, N, K = 4, 300, 264, 256
+    x, prob = _setup(W, M, N, K, "bf16", 95, "int", 2)
+    want_out, want_g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+    assert _noalloc(prob, M, N, K, _native.IRIS_BF16) == _native.IRIS_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rc = _noalloc(prob, M, N, K, _native.IRIS_BF16)
+    assert rc == _native.IRIS_OK
+    torch.cuda.synchronize()
+    for replay in range(3):
+        prob.poison_outputs()
+        g.replay()
+        torch.cuda.synchronize()
+        got = prob.outputs()
+        assert np.array_equal(_bits(got["gathered"]), want_g), replay
+        assert np.array_equal(_bits(got["out"][0]), want_out), replay
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = _native.load()
     heap = _native.iris_b200_heap(1 << 20, 1 << 20, 8)
