@@ -202,7 +202,12 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     // the concurrent mode, whose GEMM shares the L2 with a streaming
     // collective (8192^3 beside an 8 x 64Mi all-reduce: 1.144 against 1.180 ms)
     out.group_m = c->group_m ? c->group_m : (op == IRIS_OP_CONCURRENT ? 16 : 32);
-    out.comm_block = c->comm_block ? c->comm_block : 65536;
+    // concurrent mode: 128Ki elements per collective item.  Beside an 8192^3
+    // bf16 GEMM, W=8 fp32, 131072 against 65536: all-reduce 1.150 against
+    // 1.175 ms, reduce-scatter 0.960 / 0.989, all-gather (8Mi) 0.993 / 1.012,
+    // all-to-all 1.204 / 1.301, broadcast 0.998 / 1.019 (fewer stage leases
+    // per byte); 262144 leaves too few items to balance (all-reduce 1.31 ms)
+    out.comm_block = c->comm_block ? c->comm_block : 131072;
     if (out.comm_block < 0 || out.comm_block % 8 != 0) return IRIS_EINVAL;
     out.replicate = c->replicate_outputs ? 1 : 0;
     out.bias_on_m = c->bias_on_m ? 1 : 0;
@@ -213,11 +218,12 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->gemm_ctas < -1 || c->gemm_ctas > out.grid) return IRIS_EINVAL;
     if (c->gemm_ctas != 0)
         out.gemm_ctas = c->gemm_ctas;
-    else  // concurrent: 70% of the CTAs prefer the GEMM; others: all.  Beside an 8192^3
-          // bf16 GEMM, W=8 fp32, 106 against 99 GEMM CTAs (65 %): all-reduce and
-          // reduce-scatter of 64Mi 1.2-1.4 % faster, all-to-all 0.5 %, all-gather of
-          // 8Mi and broadcast of 64Mi 3.5-4.2 %
-        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? std::max(1, (out.grid * 70 + 50) / 100) : out.grid;
+    else  // concurrent: 65% of the CTAs prefer the GEMM; others: all.  Beside an 8192^3
+          // bf16 GEMM, W=8 fp32, 128Ki-element items, ms at 99 / 106 / 114 GEMM CTAs:
+          // all-reduce 1.140 / 1.152 / 1.176, reduce-scatter 0.928 / 0.947 / 0.952,
+          // all-to-all 1.193 / 1.198 / 1.205, all-gather (8Mi) 0.991 / 0.985 / 0.965,
+          // broadcast 0.998 / 0.990 / 0.970 (with 64Ki-element items 106 was best)
+        out.gemm_ctas = (op == IRIS_OP_CONCURRENT) ? std::max(1, (out.grid * 65 + 50) / 100) : out.grid;
     out.wait_ns = c->wait_ns ? c->wait_ns : DEFAULT_WAIT_NS;
     if (c->debug_skip_flag < 0) return IRIS_EINVAL;
     out.debug_skip = static_cast<uint32_t>(c->debug_skip_flag);

@@ -78,7 +78,7 @@ class Workload:
     elem_bytes: int = 4
     tile_m: int = 128
     tile_n: int = 256
-    comm_block: int = 65536
+    comm_block: int = 131072
 
     def gemm_tiles(self) -> int:
         return math.ceil(self.M / self.tile_m) * math.ceil(self.N / self.tile_n)

@@ -191,7 +191,7 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
             # (tile, split) pairs ranked by the work-stealing makespan model
             return concurrent_candidates(M, N, K, coll, W, count, sm_count, top_k)
         else:
-            for frac in (0.7, 0.6, 0.8, 0.5, 0.85):
+            for frac in (0.65, 0.55, 0.75, 0.45, 0.85):
                 out.append({"gemm_ctas": max(1, int(round(frac * sm_count)))})
     # drop duplicates, keep order
     seen, uniq = set(), []
@@ -286,7 +286,7 @@ def tune_fused(op: str, W: int, M: int, N: int, K: int, dtype: str, seed: int = 
 
 
 def concurrent_candidates(M: int, N: int, K: int, coll: str, W: int, count: int, sm_count: int,
-                          top_k: int = 6, elem_bytes: int = 4, comm_block: int = 65536) -> List[dict]:
+                          top_k: int = 6, elem_bytes: int = 4, comm_block: int = 131072) -> List[dict]:
     """Ranked candidate configs of the concurrent mode: the static default
     first, then the predictor's joint ranking of (tile kind, gemm_ctas)."""
     from . import predictor

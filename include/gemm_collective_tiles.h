@@ -111,7 +111,7 @@ typedef struct {
     int gemm_ctas;         /* CTAs whose first choice is the GEMM queue; the rest
                               prefer the comm queue and every CTA spills to the
                               other queue when its own runs dry.  0 = op default
-                              (concurrent: 70% of the grid; the dependent ops: all
+                              (concurrent: 65% of the grid; the dependent ops: all
                               CTAs); -1 = balanced (every CTA draws from both queues
                               so that both finish together). */
     int stages;            /* CTA-pair tiles: shared-memory pipeline (192 KB either
@@ -122,7 +122,7 @@ typedef struct {
                               flight), in every mode, the concurrent one with
                               a collective included; 3 or 6 choose.  Other values, or a nonzero value
                               with one-CTA tiles: IRIS_EINVAL. */
-    int comm_block;        /* concurrent mode: elements per comm tile (default 65536) */
+    int comm_block;        /* concurrent mode: elements per comm tile (default 131072) */
     int replicate_outputs; /* 1: also write the W-1 identical copies of replicated
                               outputs into the other heap regions */
     int bias_on_m;         /* 1: bias has one entry per output row (length M) */

@@ -108,7 +108,8 @@ def test_ranking_against_measured_sweeps():
     import json
     import os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "concurrent_sweeps.json")))
-    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    # the sweeps ran with 64Ki-element collective items, the default then
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024, comm_block=65536)
     for tile, sweeps in (("pair6", g["sweeps"]), ("pair3", g["three_stage"]["sweeps"])):
         tk = next(t for t in P.TILE_KINDS if t.name == tile)
         keys = sorted(sweeps[0])
@@ -132,7 +133,7 @@ def test_ranking_against_staged_sweeps():
     import json
     import os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "concurrent_sweeps.json")))
-    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024)
+    wl = P.Workload(M=8192, N=8192, K=8192, coll="all_reduce", W=8, count=64 * 1024 * 1024, comm_block=65536)
     tk = next(t for t in P.TILE_KINDS if t.name == "pair3")
     for sweep in g["staged_sums"]["sweeps"]:
         keys = sorted(sweep)
