@@ -288,10 +288,16 @@ def tune_fused(op: str, W: int, M: int, N: int, K: int, dtype: str, seed: int = 
 def concurrent_candidates(M: int, N: int, K: int, coll: str, W: int, count: int, sm_count: int,
                           top_k: int = 6, elem_bytes: int = 4, comm_block: int = 131072) -> List[dict]:
     """Ranked candidate configs of the concurrent mode: the static default
-    first, then the predictor's joint ranking of (tile kind, gemm_ctas)."""
+    first, then the default split with half and with 1.5x its collective
+    items (the item size moved the step time by 2-8 % beside every
+    collective), then the predictor's joint ranking of (tile kind,
+    gemm_ctas)."""
     from . import predictor
     out: List[dict] = [{}]
     if count > 0 and M > 0 and N > 0:
+        # collective items of other sizes, where the collective has items to spare
+        if count >= 8 * comm_block:
+            out += [{"comm_block": comm_block // 2}, {"comm_block": comm_block * 3 // 2}]
         wl = predictor.Workload(M=M, N=N, K=K, coll=coll, W=W, count=count, elem_bytes=elem_bytes,
                                 comm_block=comm_block)
         for d in predictor.predict_split(wl, m=predictor.Machine(sms=sm_count), top_k=4 * top_k,

@@ -43,8 +43,9 @@ def test_tune_then_auto(tmp_path, monkeypatch):
 
 
 def test_tune_concurrent_then_auto(tmp_path, monkeypatch):
-    """Tune a small concurrent GEMM + all-reduce (the static default and the
-    predictor's top (tile, split) candidates, measured on the device), the
+    """Tune a small concurrent GEMM + all-reduce (the static default, two
+    other collective item sizes and the predictor's top (tile, split)
+    candidates, measured on the device), the
     winner is cached under the concurrent key and never slower than the
     default; config="auto" then runs it: the GEMM exact on integer inputs and
     the all-reduce bit-exact against the oracle."""

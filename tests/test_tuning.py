@@ -146,7 +146,13 @@ def test_nearest_shape_concurrent_needs_the_same_collective(tmp_path):
 def test_concurrent_candidates_rank_tiles_and_splits():
     c = tuning.concurrent_candidates(8192, 8192, 8192, "all_reduce", 8, 64 << 20, 152, top_k=6)
     assert c[0] == {} and len(c) == 6
-    assert all("gemm_ctas" in x and "tile_m" in x for x in c[1:])
+    # the default split with smaller and larger collective items, then the
+    # predictor's (tile, split) ranking
+    assert c[1] == {"comm_block": 65536} and c[2] == {"comm_block": 196608}
+    assert all("gemm_ctas" in x and "tile_m" in x for x in c[3:])
+    # a collective with few items keeps its item size
+    small = tuning.concurrent_candidates(8192, 8192, 8192, "all_reduce", 8, 1 << 19, 152, top_k=6)
+    assert all("comm_block" not in x for x in small)
     assert len({json.dumps(x, sort_keys=True) for x in c}) == len(c)
     # the fused-op candidate helper hands the concurrent mode to it
     assert tuning.candidates("concurrent", 8, 8192, 8192, 8192, 152, top_k=6, coll="all_reduce",
