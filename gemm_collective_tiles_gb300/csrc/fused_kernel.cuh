@@ -232,6 +232,18 @@ __device__ __forceinline__ uint32_t arrive_count(unsigned long long* ctr, uint32
     }
 }
 
+// A gather copy counts itself into its (block, shard) ready counter.  With one
+// copy per counter (gather_parts 1, the default) the counter is complete at
+// the first arrival, so the copy publishes (epoch, 1) with one release store
+// instead of a read and a compare-and-swap: two L2 round trips fewer on the
+// path from the copy to the GEMM tiles that wait for it.
+__device__ __forceinline__ void arrive_gather(const Params& p, unsigned long long* ctr, uint32_t epoch) {
+    if (p.gather_parts == 1)
+        st_release_gpu_u64(ctr, (static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    else
+        arrive_count(ctr, epoch);
+}
+
 // Bounded wait on an mbarrier phase. false = gave up (timeout or abort).
 // `cluster`: the barrier receives release-arrivals from the peer CTA of a
 // pair, so the wait acquires at cluster scope.
@@ -743,7 +755,7 @@ __device__ bool tma_gather(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>
     fence_proxy_async_global();
     __threadfence();
     const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
-    if (p.debug_skip != fi + 1) arrive_count(gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
+    if (p.debug_skip != fi + 1) arrive_gather(p, gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
     return true;
 }
 
@@ -1633,7 +1645,7 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
     const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
     if (wc.w == 0 && wc.lane == 0 && !(p.debug_skip == fi + 1 && gq.part == 0)) {
         __threadfence();
-        arrive_count(gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
+        arrive_gather(p, gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
     }
     return true;
 }
@@ -2193,14 +2205,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_gemm_coll_kernel(const _
         __threadfence();
         const uint32_t done = atomicAdd(&p.ws->done_ctr, 1u);
         if (done == gridDim.x - 1) {
-            // last CTA of the launch: reset the queues for the next launch on
-            // this workspace and publish the epoch
-            atomicExch(&p.ws->gemm_ctr, 0u);
-            atomicExch(&p.ws->comm_ctr, 0u);
-            atomicExch(&p.ws->part_ctr, 0u);
-            atomicExch(&p.ws->done_ctr, 0u);
-            __threadfence();
-            atomicExch(&p.ws->epoch, ctl.epoch);
+            // last CTA of the launch (every other CTA has counted itself out
+            // and touches the header no more): publish the epoch and reset
+            // the queues for the next launch on this workspace.  The epoch
+            // and the three counters after it are one 16-byte store; the next
+            // launch sees them after the kernel boundary.
+            p.ws->part_ctr = 0u;
+            *reinterpret_cast<uint4*>(p.ws) = make_uint4(ctl.epoch, 0u, 0u, 0u);
         }
         ktr.rec(EV_KERNEL_END, blockIdx.x);
         ktr.finish();
