@@ -790,10 +790,13 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
             if (cacheable && (sm.ready_bits[gc.mb >> 5] >> (gc.mb & 31) & 1u)) {
                 acquired = p.W;
             } else {
+                // W relaxed loads in flight at once (acquire loads would run one
+                // after another), then one acquire fence if all were complete
                 uint32_t seen = 0;
                 for (int s = 0; s < p.W; ++s)
-                    seen += ld_acquire_gpu_u64(gather_ctr(p, blk * p.W + s)) == gather_done(p, ctl.epoch) ? 1u : 0u;
+                    seen += ld_relaxed_gpu_u64(gather_ctr(p, blk * p.W + s)) == gather_done(p, ctl.epoch) ? 1u : 0u;
                 if (seen == static_cast<uint32_t>(p.W)) {
+                    fence_acq_rel_gpu();
                     acquired = p.W;
                     fence_proxy_async_global();
                     if (cacheable) sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
