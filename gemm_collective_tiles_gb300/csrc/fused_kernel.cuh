@@ -753,7 +753,7 @@ __device__ bool tma_gather(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>
     bulk_wait_all();
     if (!ok) return false;
     fence_proxy_async_global();
-    __threadfence();
+    if (p.gather_parts != 1) __threadfence();  // the release store of one copy per counter orders the rest
     const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
     if (p.debug_skip != fi + 1) arrive_gather(p, gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
     return true;
@@ -1589,7 +1589,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
             fence_proxy_async_global();
         }
         __syncwarp();
-        __threadfence();
+        fence_acq_rel_gpu();  // release side: the barrier, then one release store
         if (!worker_sync(ctl, sm, wc)) return false;
         if (wc.w == 0 && wc.lane == 0 && p.debug_skip != g + 1)
             st_release_gpu_u64(ctr, tag | static_cast<uint32_t>(s + 1));
@@ -1641,13 +1641,15 @@ __device__ bool gather_tile(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
         }
     }
     fence_proxy_async_global();
-    __threadfence();
+    fence_acq_rel_gpu();  // release side: the barrier, then one arrival
     if (!worker_sync(ctl, sm, wc)) return false;
     // count this part in; the block's counter completes with the last part
     // (the test hook drops part 0's arrival of one block)
     const uint32_t fi = static_cast<uint32_t>(mb * p.W + s);
     if (wc.w == 0 && wc.lane == 0 && !(p.debug_skip == fi + 1 && gq.part == 0)) {
-        __threadfence();
+        // a release store orders the copies (each thread fenced its own before
+        // the barrier); the compare-and-swap of row parts needs the fence
+        if (p.gather_parts != 1) __threadfence();
         arrive_gather(p, gather_ctr(p, static_cast<int>(fi)), ctl.epoch);
     }
     return true;
