@@ -474,3 +474,41 @@ def test_missing_flag_times_out_and_context_survives(op, skip):
         want = oracle.matmul_reduce_scatter(x.A, x.B, None)
         for r in range(W):
             assert_exact(bits(outs["out"][r]), want[r])
+
+
+@pytest.mark.parametrize("op", ["ag_mm", "mm_rs"])
+def test_one_workspace_many_launches_varying_schedules(op):
+    """Forty launches on one workspace, cycling through grids of 2 to 152
+    CTAs, one-CTA and pair tiles and different splits: the last CTA of each
+    launch resets the queues and publishes the epoch with one store, and the
+    flags of earlier launches (other layouts) carry older epochs, so every
+    launch must still give the oracle's bits (small-integer inputs)."""
+    W, M, N, K = 4, 300, 512, 256
+    x = synthetic.make_fused_inputs(op, W, M, N, K, "bf16", seed=72, dist="int", scale=1, bias=True, bias_scale=3)
+    if op == "ag_mm":
+        out, g = oracle.all_gather_matmul(x.A, x.B[0], x.bias)
+        want, want_g = [out], g
+    else:
+        want, want_g = oracle.matmul_reduce_scatter(x.A, x.B, x.bias), None
+    # sized for the schedule that needs the most workspace (W fp32 partials)
+    big = {"tile_m": 128, "reduce_mode": 2} if op == "mm_rs" else {"tile_m": 128}
+    prob = FusedProblem(op, W, M, N, K, "bf16", bias=True, config=big)
+    prob.upload(x.A, x.B, x.bias)
+    from gemm_collective_tiles_gb300 import make_config, query_status
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cfgs = [{}, {"grid": 2}, {"grid": 6, "group_m": 2}, {"tile_m": 128}, {"tile_m": 128, "grid": 3},
+            {"gemm_ctas": 20}, {"grid": sms - sms % 2}, {"tile_m": 128, "gemm_ctas": -1}]
+    if op == "mm_rs":
+        cfgs += [{"tile_m": 128, "reduce_mode": 2}, {"tile_m": 128, "reduce_mode": 1, "grid": 5}]
+    for launch in range(40):
+        cfg = cfgs[launch % len(cfgs)]
+        prob.config = make_config(**cfg) if cfg else None
+        prob.poison_outputs()
+        prob.run()
+        torch.cuda.synchronize()
+        assert query_status(prob.ws)[0] == 0, (launch, cfg)
+        outs = prob.outputs()
+        for r in range(W if op == "mm_rs" else 1):
+            assert_exact(bits(outs["out"][r]), want[r])
+        if want_g is not None:
+            assert_exact(bits(outs["gathered"]), want_g)
