@@ -1397,7 +1397,7 @@ __device__ bool epilogue(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& 
 // claimed earlier and never waits on this one.
 template <int BN, int STAGES, int CG>
 __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& sm, uint32_t tmem, uint32_t g,
-                               uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps) {
+                               uint32_t acc_i, WorkerCtx& wc, Tracer& tr, PartState& ps, bool stages_idle) {
     const uint32_t buf = acc_i & 1, ause = acc_i >> 1;
     const GemmCoord gc = decode_gemm(p, g);
     const int blk = own_block<CG>(p, gc, ctl.half);
@@ -1432,17 +1432,9 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
     if (add_bias && !p.bias_on_m && wc.lane < nch * 4)
         bias8 = *reinterpret_cast<const uint4*>(bias_base + static_cast<size_t>(colbase + wc.lane * 8) * 2);
-    if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
-    tc_fence_after();
-    tr.rec(EV_READY, g);
-    if (CG == 2 && blk * BM >= p.M) {
-        // this CTA's half of the pair tile lies below the last row: no
-        // partial, no sum; release the accumulator in step with the pair
-        tc_fence_before();
-        __syncwarp();
-        if (wc.lane == 0) release_acc(sm, buf);
-        return true;
-    }
+    // this CTA's half of a pair tile may lie below the last row: no partial,
+    // no sum, no counter
+    const bool below = CG == 2 && blk * BM >= p.M;
     const bool last = (s == R - 1);
     const int row = blk * BM + wc.q * 32 + wc.lane;
     float row_bias = 0.f;
@@ -1452,11 +1444,23 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     unsigned long long* ctr = (reduce_op_of(p) ? reinterpret_cast<unsigned long long*>(p.flags) : p.chain) +
                               (cblk * p.n_blocks + gc.nb);
     const unsigned long long tag = static_cast<unsigned long long>(ctl.epoch) << 32;
-    if (s > 0) {
+    // the previous link's hand-off, checked while this tile's MMAs still run
+    // (it waits on an item with a smaller index, never on this accumulator)
+    if (s > 0 && !below) {
         int ok = 1;
         if (wc.lane == 0) ok = wait_count(ctl, ctr, tag | static_cast<uint32_t>(s), WAIT_CHAIN, static_cast<int>(g));
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
         if (wc.lane == 0) fence_proxy_async_global();  // S[t] was written by the TMA of another SM
+    }
+    if (!wait_bar_working<BN>(p, ctl, &sm.acc_full[buf], ause & 1, WAIT_ACC_FULL, ps, wc)) return false;
+    tc_fence_after();
+    tr.rec(EV_READY, g);
+    if (below) {
+        // release the accumulator in step with the pair
+        tc_fence_before();
+        __syncwarp();
+        if (wc.lane == 0) release_acc(sm, buf);
+        return true;
     }
     const uint32_t tbase = tmem + (static_cast<uint32_t>(wc.q * 32) << 16) + buf * BN + wc.h * COLS;
     uint8_t* stg_base = sm.stage_out + wc.w * Smem<BN, STAGES, CG>::STAGE_OUT_BYTES;
@@ -1473,10 +1477,24 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
     const uint64_t spol = p.sum_l2_policy == 1   ? l2_policy_evict_first()
                           : p.sum_l2_policy == 2 ? l2_policy_evict_last()
                                                  : 0ull;
-    if (reads_sum && nch > 0 && wc.lane == 0) issue_load(0);
+    // The CTA's last GEMM item (its pipeline stages idle once the accumulator
+    // is full): the warp loads every chunk of its running-sum rows at once,
+    // into its quarter of the stages, instead of one chunk ahead through its
+    // staging buffer -- this epilogue is the one the launch cannot hide
+    constexpr uint32_t STAGE_QUARTER = Smem<BN, STAGES, CG>::TILES_BYTES / NUM_WORKER_WARPS;
+    static_assert(STAGE_QUARTER >= NCH * 4096u, "a warp's quarter of the stages holds all its running-sum chunks");
+    const bool burst = reads_sum && stages_idle && nch > 0;
+    uint8_t* const sbase = sm.tiles + wc.w * STAGE_QUARTER;
+    if (burst && wc.lane == 0) {
+        mbar_arrive_expect_tx(&lbar[0], static_cast<uint32_t>(nch) * 32 * 32 * 4);
+        for (int ci = 0; ci < nch; ++ci)
+            tma_load_4d(sbase + ci * 4096, &p.tmS, colbase + ci * 32, c_row, s_blk, 0, &lbar[0]);
+    } else if (reads_sum && nch > 0 && wc.lane == 0) {
+        issue_load(0);
+    }
 #pragma unroll 1
     for (int ci = 0; ci < nch; ++ci) {
-        uint8_t* stg = stg_base + (ci & 1) * 4096;
+        uint8_t* stg = burst ? sbase + ci * 4096 : stg_base + (ci & 1) * 4096;
         uint32_t r[32];
         if (p.k_blocks > 0) {
             tmem_ld_32x32b_x32(tbase + ci * 32, r);
@@ -1486,7 +1504,7 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
             for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
         const int col0 = colbase + ci * 32;
-        if (reads_sum && ci + 1 < nch && wc.lane == 0) issue_load(ci + 1);
+        if (reads_sum && !burst && ci + 1 < nch && wc.lane == 0) issue_load(ci + 1);
         // P_s = acc + bias_s (fp32)
         float x[32];
 #pragma unroll
@@ -1513,13 +1531,19 @@ __device__ __noinline__ bool epilogue_chain(const Params& p, const Ctl& ctl, Sme
         }
         if (reads_sum) {
             // S_new = S_old + P_s (S_old holds ranks 0..s-1 in order)
-            int ok = 1;
-            if (wc.lane == 0) {
-                const uint32_t par = (wc.sphase >> (ci & 1)) & 1u;
-                ok = wait_bar(ctl, &lbar[ci & 1], par, WAIT_CHAIN_LOAD) ? 1 : 0;
+            if (!burst || ci == 0) {
+                // one chunk's load, or (burst) all of them, on one barrier
+                const int lb = burst ? 0 : (ci & 1);
+                int ok = 1;
+                if (wc.lane == 0) {
+                    const uint32_t par = (wc.sphase >> lb) & 1u;
+                    ok = wait_bar(ctl, &lbar[lb], par, WAIT_CHAIN_LOAD) ? 1 : 0;
+                    // stopped: the burst's other chunks still land in the stages
+                    if (!ok && burst) drain_bar(ctl, &lbar[lb], par, WAIT_CHAIN_LOAD);
+                }
+                wc.sphase ^= 1u << lb;
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
             }
-            wc.sphase ^= 1u << (ci & 1);
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 o = *reinterpret_cast<const float4*>(stg + wc.lane * 128 + ((c ^ (wc.lane & 7)) << 4));
@@ -2083,7 +2107,18 @@ __device__ void run_workers(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG
         } else {
             seen_gemm = true;
             if (split_k(p) || (p.reduce_mode == 3 && (p.op == OP_MM_RS || p.op == OP_MM_AR)))
-                ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
+            {
+                // the next ring entry already published as the end marker: this
+                // is the CTA's last GEMM item, so its stages fall idle once the
+                // accumulator is full (no further loads are issued)
+                int idle = 0;
+                if (lane == 0) {
+                    const uint32_t nslot = ring_n % RING, nuse = ring_n / RING;
+                    idle = try_bar(&sm.item_full[nslot], nuse & 1, CG == 2) && sm.ring[nslot] == ITEM_END;
+                }
+                idle = __shfl_sync(0xFFFFFFFFu, idle, 0);
+                ok = epilogue_chain(p, ctl, sm, tmem, item, acc_i, wc, tr, ps, idle != 0);
+            }
             else
                 ok = epilogue(p, ctl, sm, tmem, item, acc_i, wc, tr, ps);
             ++acc_i;
