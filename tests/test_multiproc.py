@@ -66,3 +66,20 @@ def test_reference_and_gpu_arms_describe_the_same_workload():
     assert a == b and a["workload"].startswith("matmul_reduce_scatter W=4 M=4096 N=4096 K=4096 f16")
     assert {"l2", "parallelism", "op", "M", "N", "K", "seed", "dist"} <= set(a)
     assert bench.bench_config(wl, bench.DEFAULT_WORKLOAD, {}, 2)["parallelism"] == "replicas x2"
+
+
+def test_recorded_traffic_is_used_only_on_the_kernel_source_it_was_taken_on(tmp_path, monkeypatch):
+    """The bench line's roofline.traffic comes from a committed ncu record
+    only while the kernel sources hash to the value stored beside it."""
+    import bench
+    csrc = tmp_path / "gemm_collective_tiles_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cuh").write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = tmp_path / "profiles" / "traffic_w.txt"
+    rec.write_text(f"# one launch\ndram_bytes_per_launch: 123456\nkernel_source_sha256_16: {bench.kernel_source_hash()}\n")
+    assert bench.recorded_traffic("w") == 123456
+    (csrc / "k.cuh").write_text("kernel v2\n")
+    assert bench.recorded_traffic("w") is None
+    assert bench.recorded_traffic("absent") is None
