@@ -67,7 +67,7 @@ extern "C" {
 #define IRIS_ENOWS (-3)       /* workspace missing or smaller than iris_b200_workspace_size() */
 #define IRIS_ECUDA (-4)       /* CUDA runtime / driver error (launch, attribute, tensor map) */
 #define IRIS_ETIMEOUT (-5)    /* a bounded device wait gave up (reported by query_status) */
-#define IRIS_EUNSUPPORTED (-6) /* valid request this build does not implement */
+#define IRIS_EUNSUPPORTED (-6) /* valid request the library does not implement */
 
 #define IRIS_NO_BIAS ((size_t)-1)
 #define IRIS_MAX_WORLD 16
