@@ -692,6 +692,35 @@ def short_clocks(c):
             "reasons": c.get("reasons")}
 
 
+def back_to_back_us(prob, stream, n=200):
+    """Mean microseconds per call over n calls back to back: issued one by
+    one, and replayed from a CUDA graph captured around one call."""
+    from gemm_collective_tiles_gb300 import query_status
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(torch.cuda.current_stream())
+        for _ in range(n):
+            fn()
+        e1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return round(e0.elapsed_time(e1) * 1e3 / n, 2)
+
+    eager = timed(lambda: prob.run(stream))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        prob.run()
+    torch.cuda.synchronize()
+    replay = timed(g.replay)
+    rc = query_status(prob.ws, stream)
+    if rc[0] != 0:
+        raise RuntimeError(f"device status after the back-to-back calls: {rc}")
+    return {"eager": eager, "graph_replay": replay}
+
+
 def run_other_configs(args, cfg, stream, flush):
     """Every other workload of the family on this GPU, one compact JSON line
     each; returns {name: summary} for the headline line."""
@@ -712,6 +741,11 @@ def run_other_configs(args, cfg, stream, flush):
                 "roofline": {"bound": "tensor", "frac": tf / peak, "peak": peak,
                              "peak_source": f"{peak_kind} bf16 burst"},
                 "pages_mi300x_tflops": base, "gpu_launches": steps, "clocks": short_clocks(clocks)}
+        if wl["M"] * wl["N"] * wl["K"] <= 1 << 27:
+            # launch-bound: calls back to back with no flush, issued one by one
+            # and replayed from a CUDA graph that holds one call (no host work
+            # per call), the kernel's own floor beside the flushed steps
+            line["back_to_back_us"] = back_to_back_us(prob, stream)
         print(json.dumps(line), flush=True)
         summary[name] = {"value": round(tf, 1), "ms": round(mean_ms, 4), "frac": round(tf / peak, 4),
                          "steps": steps}
