@@ -808,24 +808,14 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
         const int kb_lo = split_k(p) ? gc.chunk * p.kb_chunk : 0;
         const int kb_hi = split_k(p) ? min(p.k_blocks, kb_lo + p.kb_chunk) : p.k_blocks;
         for (int kb = kb_lo; kb < kb_hi; kb += KS) {
-            if (p.op == OP_AG_MM && acquired < p.W) {
-                const int s_hi = min(p.W - 1, ((kb + KS) * BK - 1) / p.K_local);
-                if (s_hi >= acquired) {
-                    for (int s = acquired; s <= s_hi; ++s) {
-                        const int fi = blk * p.W + s;
-                        if (!wait_count(ctl, gather_ctr(p, fi), gather_done(p, ctl.epoch), WAIT_FLAG_GATHER, fi))
-                            return false;
-                    }
-                    acquired = s_hi + 1;
-                    fence_proxy_async_global();
-                    if (acquired == p.W && gc.mb < Smem<BN, STAGES, CG>::READY_BITS)
-                        sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
-                }
-            }
             if (!wait_bar(ctl, &sm.empty[stage], phase ^ 1, WAIT_SMEM_EMPTY)) return false;
+            // B first: it depends on no gather, so its loads are in flight
+            // while this stage's A shards may still be on their way
+            constexpr uint32_t HALF_BYTES = Smem<BN, STAGES, CG>::A_BYTES + Smem<BN, STAGES, CG>::B_BYTES / 2;
+            const bool hn = gc.hn >= 0;
+            const uint32_t fb = CG == 2 ? mapa_shared(&sm.full[stage], 0) : 0u;
             if (CG == 1) {
                 mbar_arrive_expect_tx(&sm.full[stage], Smem<BN, STAGES, CG>::STAGE_BYTES);
-                tma_load_3d(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, &sm.full[stage]);
                 if (p.b_chunked) {
                     tma_load_4d(sm.b_tile(stage), &p.tmBc, 0, kb * BK, gc.nb * (BN / 64), b_rank, &sm.full[stage]);
                 } else {
@@ -839,26 +829,8 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                 // expects the pair's bytes (the odd CTA's may land first: the
                 // transaction count may dip below zero inside a phase).  A
                 // column half (N = BN / 2) loads one 64-column box per CTA.
-                constexpr uint32_t HALF_BYTES = Smem<BN, STAGES, CG>::A_BYTES + Smem<BN, STAGES, CG>::B_BYTES / 2;
-                const bool hn = gc.hn >= 0;
                 if (ctl.half == 0)
                     mbar_arrive_expect_tx(&sm.full[stage], (hn ? HALF_BYTES : Smem<BN, STAGES, CG>::STAGE_BYTES) * CG);
-                const uint32_t fb = mapa_shared(&sm.full[stage], 0);
-                // A: the stage's KS K-chunks of this CTA's 128 rows, 16 KB apart
-                if (p.a_chunked) {
-                    if (p.gemm_evict_last) tma_load_4d_pair_hint(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb, pol);
-                    else tma_load_4d_pair(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < KS; ++j) {
-                        if (p.gemm_evict_last)
-                            tma_load_3d_pair_hint(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row,
-                                                  a_rank, fb, pol);
-                        else
-                            tma_load_3d_pair(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row,
-                                             a_rank, fb);
-                    }
-                }
                 // B: 64-column chunks of KS x 64 K rows, 64 KS x 128 B apart
                 const int bcol = gc.nb * BN + (hn ? gc.hn * (BN / 2) + ctl.half * (BN / 4) : ctl.half * (BN / CG));
                 if (p.b_chunked && !hn) {
@@ -879,12 +851,50 @@ __device__ void run_tma(const Params& p, const Ctl& ctl, Smem<BN, STAGES, CG>& s
                     }
                 }
             }
+            // all_gather_matmul: the shards this stage's A rows come from
+            bool flags_ok = true;
+            if (p.op == OP_AG_MM && acquired < p.W) {
+                const int s_hi = min(p.W - 1, ((kb + KS) * BK - 1) / p.K_local);
+                if (s_hi >= acquired) {
+                    for (int s = acquired; s <= s_hi && flags_ok; ++s) {
+                        const int fi = blk * p.W + s;
+                        flags_ok = wait_count(ctl, gather_ctr(p, fi), gather_done(p, ctl.epoch), WAIT_FLAG_GATHER, fi);
+                    }
+                    if (flags_ok) {
+                        acquired = s_hi + 1;
+                        fence_proxy_async_global();
+                        if (acquired == p.W && gc.mb < Smem<BN, STAGES, CG>::READY_BITS)
+                            sm.ready_bits[gc.mb >> 5] |= 1u << (gc.mb & 31);
+                    }
+                }
+            }
+            // A (issued even when a wait gave up, so that the stage's
+            // transaction completes before the CTA stops; the launch is
+            // aborting then and its results are discarded)
+            if (CG == 1) {
+                tma_load_3d(sm.a_tile(stage), &p.tmA, kb * BK, a_row, a_rank, &sm.full[stage]);
+            } else if (p.a_chunked) {
+                // the stage's KS K-chunks of this CTA's 128 rows, 16 KB apart
+                if (p.gemm_evict_last) tma_load_4d_pair_hint(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb, pol);
+                else tma_load_4d_pair(sm.a_tile(stage), &p.tmAc, 0, a_row, kb, a_rank, fb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    if (p.gemm_evict_last)
+                        tma_load_3d_pair_hint(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row,
+                                              a_rank, fb, pol);
+                    else
+                        tma_load_3d_pair(sm.a_tile(stage) + j * (BM * BK * 2), &p.tmA, (kb + j) * BK, a_row, a_rank,
+                                         fb);
+                }
+            }
             issued_phase[stage] = phase;
             used_mask |= 1u << stage;
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
             }
+            if (!flags_ok) return false;
         }
         return true;
     };
