@@ -71,9 +71,9 @@ def pages_tflops(op, W, M, N, K):
 # ------------------------------------------------------------------ helpers
 
 def release_memory():
-    """Return the cached device memory of a finished workload to the driver,
-    then wait until the driver has cleared it.  The driver zeroes freed device
-    memory in the background: right after 150 GB were freed, the headline
+    """Return the cached device memory of a finished workload to the CUDA
+    driver, then wait until it has been cleared: the GPU driver zeroes freed
+    device memory in the background: right after 150 GB were freed, the headline
     kernel ran 486-501 us per step instead of 350-360 for about 42 ms, the
     time that clearing takes at ~3.6 TB/s.  Waiting at 2 TB/s of freed bytes
     keeps that clearing out of the next workload's timed steps."""
@@ -493,7 +493,7 @@ def concurrent_measure(cfg, steps, warm, sweep=False, two_stream=False):
             str(g): time_two({**cfg, "gemm_ctas": g}, s_g, s_c)
             for g in (sms_all // 2, int(sms_all * 0.55), int(sms_all * 0.45))}
         # the same on two green contexts with disjoint SM sets (the split
-        # enforced by the driver): the GEMM stream gets at least g SMs
+        # enforced by the CUDA driver): the GEMM stream gets at least g SMs
         green = {}
         for g in (72, 80, 88, 96):
             s_gemm, s_comm, gs, cs = sm_partition_streams(g)

@@ -346,7 +346,7 @@ def test_two_stream_mode_bit_exact(coll):
 @pytest.mark.parametrize("coll", ["all_reduce", "all_gather", "all_to_all"])
 def test_two_stream_mode_on_sm_partition(coll):
     """The two-stream mode on streams of two green contexts with disjoint SM
-    sets (the split enforced by the driver, not by occupancy): results bit for
+    sets (the split enforced by the CUDA driver, not by occupancy): results bit for
     bit as before."""
     from gemm_collective_tiles_gb300 import query_status, sm_partition_release, sm_partition_streams
     W, count = 8, 8 * 16384
