@@ -174,7 +174,7 @@ struct Cfg {
     int coll_evict_first;
     int coll_path;       // concurrent collectives: 1 TMA, 2 TMA loads + register stores, 3 one box of all sources
     int gather_parts;    // all_gather_matmul: gather items per (row block, shard)
-    int startup_gather;  // all_gather_matmul: 1 = worker copies, 2 = the TMA producer copies start-up gathers
+    int startup_gather;  // all_gather_matmul: 0 = by M, 1 = worker copies, 2 = the TMA producer copies start-up gathers
     int gemm_evict_last; // CTA-pair operand loads with an L2 evict-last policy
     int out_evict_first; // final 16-bit output stores with an L2 evict-first policy
     int sum_l2_policy;   // chained reduce running sum: 0 none, 1 evict first, 2 evict last
@@ -258,7 +258,7 @@ int resolve_cfg(const iris_b200_config* c, iris_op op, int64_t N, Cfg& out) {
     if (c->coll_out_stage < 0 || c->coll_out_stage > 2) return IRIS_EINVAL;
     out.coll_out_stage = c->coll_out_stage;
     if (c->startup_gather < 0 || c->startup_gather > 2) return IRIS_EINVAL;
-    out.startup_gather = c->startup_gather ? c->startup_gather : 1;
+    out.startup_gather = c->startup_gather;
     if (c->coll_path < 0 || c->coll_path > 3) return IRIS_EINVAL;
     out.coll_path = c->coll_path;  // 0: chosen per collective (resolve_coll_path)
     return IRIS_OK;
@@ -734,8 +734,13 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
         p.lookahead *= static_cast<uint32_t>(sk.split);
     }
     p.gather_parts = c.gather_parts;
-    // the producer's start-up copies move whole 128-row blocks
-    p.startup_gather = (c.startup_gather == 2 && c.gather_parts == 1 && M > 0 && K_l > 0) ? 1 : 0;
+    // the producer's start-up copies move whole 128-row blocks.  By default
+    // the producer takes them up to 16384 rows, where the first swizzle
+    // group's gathers hold back a larger share of the launch (0.4-2.4 %
+    // faster over the PR #506 shapes of that size, about 1 us off a 256^3
+    // launch), and the workers beyond (within 0.5 % either way there).
+    const int startup = c.startup_gather ? c.startup_gather : (M <= 16384 ? 2 : 1);
+    p.startup_gather = (startup == 2 && c.gather_parts == 1 && M > 0 && K_l > 0) ? 1 : 0;
     if (p.startup_gather && (rc = make_gather_maps(p, heap, off_A, off_gathered, M, K, K_l))) return rc;
     if (int64_t(mblocks) * W * c.gather_parts >= 0x7FFFFFFF) return IRIS_EINVAL;
     p.n_comm = static_cast<uint32_t>(mblocks) * W * c.gather_parts;

@@ -187,11 +187,10 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
         # split-K: the default splits above K = 32768 into chunks of ~16384
         out.insert(1, {"k_split": 1} if K > 32768 else {"k_split": 2})
     if op == "all_gather_matmul" and M <= 16384:
-        # the TMA producer copying the start-up gathers: 0.4-2.4 % faster on
-        # the PR #506 shapes of up to 16384 rows, where the first swizzle
-        # group's gathers hold back a larger share of the launch; within
-        # +-0.5 % on the larger ones
-        out.insert(min(3, len(out)), {"startup_gather": 2})
+        # the default lets the TMA producer copy the start-up gathers up to
+        # 16384 rows (0.4-2.4 % faster than the worker threads on the PR #506
+        # shapes of that size); the workers remain the alternative
+        out.insert(min(3, len(out)), {"startup_gather": 1})
     if op == "concurrent":
         if count > 0:
             # (tile, split) pairs ranked by the work-stealing makespan model

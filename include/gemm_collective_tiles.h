@@ -188,12 +188,13 @@ typedef struct {
                               shard's copies over more CTAs at the cost of
                               more claims and synchronisation per byte. */
     int startup_gather;    /* all_gather_matmul: who copies the gathers a CTA
-                              pair claims before its first GEMM tile.  1 (and
-                              0, the default) = the worker threads, 16-byte
-                              copies through registers; 2 = the TMA producer,
-                              with TMA boxes through its still idle pipeline
-                              stages (whole 128-row blocks: needs
-                              gather_parts 1, else the workers copy). */
+                              pair claims before its first GEMM tile.  1 = the
+                              worker threads, 16-byte copies through
+                              registers; 2 = the TMA producer, with TMA boxes
+                              through its still idle pipeline stages (whole
+                              128-row blocks: needs gather_parts 1, else the
+                              workers copy); 0 = default: 2 for M <= 16384,
+                              else 1. */
     int gemm_l2_hint;      /* L2 policy of the GEMM operand loads of CTA-pair
                               tiles: 0 = default (evict last), 1 = evict last
                               (the operands keep their place in the L2 against

@@ -373,14 +373,16 @@ def test_ag_mm_gather_parts_exact(parts, tile_m):
 @pytest.mark.parametrize("W,M,N,K", [(2, 256, 256, 256), (4, 392, 520, 256), (8, 200, 136, 576),
                                      (2, 1, 8, 16), (4, 640, 512, 4 * 2048)])
 @pytest.mark.parametrize("tile_m", [0, 128])   # 0: the default (CTA pairs wherever they apply)
-def test_ag_mm_startup_gather_by_producer_exact(W, M, N, K, tile_m):
+@pytest.mark.parametrize("startup", [1, 2])
+def test_ag_mm_startup_gather_by_producer_exact(W, M, N, K, tile_m, startup):
     """The gathers claimed before a CTA's first GEMM tile copied by its TMA
-    producer (boxes of up to 256 columns x 128 rows through the idle stages;
-    ragged rows, shards 9 to 2048 columns wide, one box or several batches):
-    gathered A bit-exact, output exact on integer inputs."""
+    producer (2, the default at these sizes: boxes of up to 256 columns x 128
+    rows through the idle stages; ragged rows, shards 8 to 2048 columns wide,
+    one box or several batches) or by the worker threads (1): gathered A
+    bit-exact, output exact on integer inputs."""
     x = synthetic.make_fused_inputs("ag_mm", W, M, N, K, "f16", seed=100 + M, dist="int", scale=2, bias=True,
                                     bias_scale=2)
-    prob = FusedProblem("ag_mm", W, M, N, K, "f16", bias=True, config={"startup_gather": 2, "tile_m": tile_m})
+    prob = FusedProblem("ag_mm", W, M, N, K, "f16", bias=True, config={"startup_gather": startup, "tile_m": tile_m})
     prob.upload(x.A, x.B, x.bias)
     prob.poison_outputs()
     prob.run()

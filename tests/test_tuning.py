@@ -81,11 +81,12 @@ def test_candidates():
     # unsplit all_gather_matmul with a long K (N not a multiple of 32)
     odd_n = tuning.candidates("all_gather_matmul", 8, 4096, 4104, 131072, 152, top_k=3)
     assert {"stages": 3} in odd_n and not any("k_split" in c for c in odd_n)
-    # start-up gathers by the TMA producer: tried up to 16384 rows
-    assert {"startup_gather": 2} in tuning.candidates("all_gather_matmul", 8, 4096, 4096, 4096, 152)
-    assert {"startup_gather": 2} in tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152)
-    assert {"startup_gather": 2} not in tuning.candidates("all_gather_matmul", 8, 131072, 16384, 16384, 152)
-    assert {"startup_gather": 2} not in tuning.candidates("matmul_all_gather", 8, 4096, 4096, 4096, 152)
+    # start-up gathers by the worker threads (the default up to 16384 rows is
+    # the TMA producer): tried where the default differs
+    assert {"startup_gather": 1} in tuning.candidates("all_gather_matmul", 8, 4096, 4096, 4096, 152)
+    assert {"startup_gather": 1} in tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152)
+    assert not any("startup_gather" in c for c in tuning.candidates("all_gather_matmul", 8, 131072, 16384, 16384, 152))
+    assert not any("startup_gather" in c for c in tuning.candidates("matmul_all_gather", 8, 4096, 4096, 4096, 152))
 
 
 def test_all_tuned_knobs_exist_in_the_config_struct():
