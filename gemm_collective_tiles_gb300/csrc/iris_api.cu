@@ -735,11 +735,14 @@ int iris_b200_all_gather_matmul(const iris_b200_heap* heap, size_t off_A, size_t
     }
     p.gather_parts = c.gather_parts;
     // the producer's start-up copies move whole 128-row blocks.  By default
-    // the producer takes them up to 16384 rows, where the first swizzle
-    // group's gathers hold back a larger share of the launch (0.4-2.4 %
-    // faster over the PR #506 shapes of that size, about 1 us off a 256^3
-    // launch), and the workers beyond (within 0.5 % either way there).
-    const int startup = c.startup_gather ? c.startup_gather : (M <= 16384 ? 2 : 1);
+    // the producer takes them up to 16384 rows when an item's K is at most
+    // 32768 (split or not), where the first swizzle group's gathers hold
+    // back a larger share of the launch (0.4-2.4 % faster over the PR #506
+    // shapes of that size, about 1 us off a 256^3 launch); the workers take
+    // them beyond 16384 rows (within 0.5 % either way there) and for unsplit
+    // long K, where the producer's copies delay its own first tile
+    const int64_t item_k = sk.split > 1 ? int64_t(sk.kb_chunk) * BK : K;
+    const int startup = c.startup_gather ? c.startup_gather : (M <= 16384 && item_k <= 32768 ? 2 : 1);
     p.startup_gather = (startup == 2 && c.gather_parts == 1 && M > 0 && K_l > 0) ? 1 : 0;
     if (p.startup_gather && (rc = make_gather_maps(p, heap, off_A, off_gathered, M, K, K_l))) return rc;
     if (int64_t(mblocks) * W * c.gather_parts >= 0x7FFFFFFF) return IRIS_EINVAL;

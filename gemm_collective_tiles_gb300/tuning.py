@@ -186,10 +186,11 @@ def candidates(op: str, W: int, M: int, N: int, K: int, sm_count: int, top_k: in
     if splits and K > 16384:
         # split-K: the default splits above K = 32768 into chunks of ~16384
         out.insert(1, {"k_split": 1} if K > 32768 else {"k_split": 2})
-    if op == "all_gather_matmul" and M <= 16384:
+    if op == "all_gather_matmul" and M <= 16384 and k_item <= 32768:
         # the default lets the TMA producer copy the start-up gathers up to
-        # 16384 rows (0.4-2.4 % faster than the worker threads on the PR #506
-        # shapes of that size); the workers remain the alternative
+        # 16384 rows when an item's K is at most 32768 (0.4-2.4 % faster than
+        # the worker threads on the PR #506 shapes of that size); the workers
+        # remain the alternative
         out.insert(min(3, len(out)), {"startup_gather": 1})
     if op == "concurrent":
         if count > 0:

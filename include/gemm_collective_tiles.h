@@ -193,8 +193,9 @@ typedef struct {
                               registers; 2 = the TMA producer, with TMA boxes
                               through its still idle pipeline stages (whole
                               128-row blocks: needs gather_parts 1, else the
-                              workers copy); 0 = default: 2 for M <= 16384,
-                              else 1. */
+                              workers copy); 0 = default: 2 for M <= 16384
+                              when a work item's K (a split-K chunk's, or
+                              all of K) is at most 32768, else 1. */
     int gemm_l2_hint;      /* L2 policy of the GEMM operand loads of CTA-pair
                               tiles: 0 = default (evict last), 1 = evict last
                               (the operands keep their place in the L2 against

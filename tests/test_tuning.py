@@ -87,6 +87,8 @@ def test_candidates():
     assert {"startup_gather": 1} in tuning.candidates("all_gather_matmul", 8, 16384, 16384, 131072, 152)
     assert not any("startup_gather" in c for c in tuning.candidates("all_gather_matmul", 8, 131072, 16384, 16384, 152))
     assert not any("startup_gather" in c for c in tuning.candidates("matmul_all_gather", 8, 4096, 4096, 4096, 152))
+    # unsplit long K (N not a multiple of 32): the workers are the default there
+    assert not any("startup_gather" in c for c in tuning.candidates("all_gather_matmul", 8, 4096, 4104, 131072, 152))
 
 
 def test_all_tuned_knobs_exist_in_the_config_struct():
